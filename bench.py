@@ -1,0 +1,456 @@
+"""Benchmark of the KDA state path on GB300.
+
+One step = one pass of the prefill path over the batched workload (4 sequences x 8192
+tokens, H = 16, d = 128, bf16 inputs, fp32 state, chunk 64, checkpoints at every 4th
+512-token hash-block end into a pool of 64 KiB pages): host checkpoint plan and page
+allocation, one prefill launch (conv, chunked recurrence, outputs, checkpoint streaming,
+final-state write), then the checkpoint pages are released for the next step.  The decode
+step (256 requests x 32 heads through a permuted page table) and checkpoint write/restore
+copies are measured in the same run and reported beside the headline number.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch under torch.distributed.run: each rank runs its own batch on its own GPU
+(weak scaling, no data-path collective); timings are maxed over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s and decode step µs at B=256; % of tensor/HBM roofline"
+WORKLOAD = "batched"
+
+
+# --------------------------------------------------------------------------- helpers
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def _kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "kda_state_chunked_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str, source_files, scale: float):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)[kernel]
+    except Exception:
+        return None
+    if t.get("source_hash") != _kernel_source_hash(source_files):
+        return None
+    return float(t["dram_bytes_per_unit"]) * scale
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        import torch
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.dev).uuid)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", uuid, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- workload
+class BatchedPrefill:
+    """The batched prefill workload resident on one GPU."""
+
+    def __init__(self, dev, seed_offset: int = 0):
+        import torch
+        import kda_state_chunked_gb300 as kda
+        from kda_state_chunked_gb300 import workloads
+        self.kda = kda
+        self.w = w = workloads.WORKLOADS[WORKLOAD]
+        self.dev = dev
+        self.T_tot = w.nseq * w.T
+        self.toks = workloads.make_tokens(self.T_tot, w.H, w.d, w.dtype, w.seed + seed_offset, dev)
+        self.cu = [i * w.T for i in range(w.nseq + 1)]
+        self.start = [0] * w.nseq
+        self.dt = kda.DTYPES[w.dtype]
+        self.pool = kda.Pool(w.page_bytes, 1024, dev)
+        self.P = self.pool.object_pages(w.H, w.d, self.dt)
+        self.active = kda.kda_page_alloc(self.pool, w.nseq * self.P).reshape(w.nseq, self.P)
+        self.o = torch.empty_like(self.toks["q"])
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        n_ck = sum(len(kda.kda_ckpt_positions(0, w.T, w.hash_block, w.stride, w.include_last))
+                   for _ in range(w.nseq))
+        self.n_ckpt = n_ck
+        self.ws = torch.empty(kda.kda_prefill_workspace_bytes(w.nseq, n_ck, self.P),
+                              dtype=torch.uint8, device=dev)
+        self.rec = kda.kda_record_bytes(w.d, self.dt)
+
+    def step(self, toks=None, o=None):
+        kda, w = self.kda, self.w
+        t = toks or self.toks
+        seq, pos, pages = kda.kda_ckpt_plan(self.pool, w.H, w.d, self.dt, self.cu, self.start,
+                                            w.hash_block, w.stride, w.include_last)
+        kda.kda_prefill_varlen(self.pool, self.cu, self.start, [0] * w.nseq, t["q"], t["k"], t["v"],
+                               t["alpha"], t["beta"], t["conv_w"], o if o is not None else self.o,
+                               self.active, seq, pos, pages, self.ws, self.status)
+        kda.kda_page_decref(self.pool, pages.reshape(-1))
+
+    def algorithmic_bytes(self) -> int:
+        w = self.w
+        es = 2 if w.dtype == "bf16" else 4
+        th = self.T_tot * w.H
+        tokens = th * (4 * w.d * es + es + w.d * es)     # q, k, v, alpha, beta in; o out
+        states = (self.n_ckpt + w.nseq) * w.H * self.rec  # checkpoints + final states
+        return tokens + states
+
+    def algorithmic_flops(self) -> int:
+        w = self.w
+        C, d = 64, w.d
+        return self.T_tot * w.H * (6 * d * d + 4 * C * d + C * C // 3)
+
+
+def _time_steps(fn, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev]
+    return start.elapsed_time(end), per
+
+
+def _decode_phase(dev, steps=64, warmup=3):
+    """Decode workload: 256 requests x 32 heads, states in a 4096-page pool of 256 KiB pages
+    addressed through a permuted page table; states come from a 512-token setup prefill."""
+    import torch
+    import kda_state_chunked_gb300 as kda
+    from kda_state_chunked_gb300 import workloads
+    w = workloads.WORKLOADS["decode"]
+    dt = kda.DTYPES[w.dtype]
+    pool = kda.Pool(w.page_bytes, 4096, dev)
+    P = pool.object_pages(w.H, w.d, dt)
+    table = workloads.permuted_page_table(4096, w.nseq, P, w.seed)
+    kda.kda_page_claim(pool, table.reshape(-1))
+    setup_T = 512
+    toks = workloads.make_tokens(w.nseq * setup_T, w.H, w.d, w.dtype, w.seed, dev)
+    cu = [i * setup_T for i in range(w.nseq + 1)]
+    ws = torch.empty(kda.kda_prefill_workspace_bytes(w.nseq, 0, P), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    o = torch.empty_like(toks["q"])
+    kda.kda_prefill_varlen(pool, cu, [0] * w.nseq, [0] * w.nseq, toks["q"], toks["k"], toks["v"],
+                           toks["alpha"], toks["beta"], toks["conv_w"], o, table.numpy(), [], [], None,
+                           ws, st)
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+    del toks, o
+    step_toks = [workloads.decode_step_tokens(w.nseq, w.H, w.d, w.dtype, w.seed, s, dev)
+                 for s in range(steps)]
+    conv_w = workloads.make_tokens(1, w.H, w.d, w.dtype, w.seed, dev)["conv_w"]
+    table_dev = table.to(dev)
+    od = torch.empty_like(step_toks[0]["q"])
+    stream = torch.cuda.current_stream()
+    it = iter(range(10 ** 9))
+
+    def one():
+        t = step_toks[next(it) % steps]
+        kda.kda_decode_step(pool, t["q"], t["k"], t["v"], t["alpha"], t["beta"], conv_w, od,
+                            table_dev, st)
+
+    total, per = _time_steps(one, steps, warmup, stream)
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+    rec = kda.kda_record_bytes(w.d, dt)
+    es = 2
+    bytes_per = w.nseq * w.H * (2 * w.d * w.d * 4 + 2 * 3 * 3 * w.d * es + 4 * w.d * es + es + w.d * es)
+    del rec
+    us = statistics.median(per) * 1e3
+    return {"step_us": us, "mean_step_us": total * 1e3 / steps, "steps": steps, "B": w.nseq, "H": w.H,
+            "bytes_per_step": bytes_per, "achieved_gbs": bytes_per / (us * 1e-6) / 1e9,
+            "l2": "state set 1.1 GB per step > L2"}
+
+
+def _ckpt_io_phase(dev, n=256, reps=5):
+    """Checkpoint write (snapshot) and restore of 256 objects of 32 heads, 64 KiB pages."""
+    import torch
+    import kda_state_chunked_gb300 as kda
+    H, d, dt = 32, 128, kda.KDA_BF16
+    pool = kda.Pool(65536, 3 * n * 34 + 64, dev)
+    P = pool.object_pages(H, d, dt)
+    src = kda.kda_page_alloc(pool, n * P)
+    act = kda.kda_page_alloc(pool, n * P)
+    ws = torch.empty(kda.kda_copy_workspace_bytes(n, P), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    nb = kda.kda_object_bytes(H, d, dt) * n * 2
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name in ("write", "restore"):
+        times = []
+        for r in range(reps + 2):
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            if name == "write":
+                dst = kda.kda_ckpt_write(pool, H, d, dt, src, ws, st)
+            else:
+                kda.kda_ckpt_restore(pool, H, d, dt, src, act, ws, st)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if name == "write":
+                kda.kda_page_decref(pool, dst.reshape(-1))
+            else:
+                kda.kda_ckpt_release(pool, src, P)
+            if r >= 2:
+                times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        res[name] = {"ms": ms, "gbs": nb / (ms * 1e-3) / 1e9}
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+    res["objects"] = n
+    res["bytes_moved"] = nb
+    return res
+
+
+def _oracle_sample(toks_cpu_fn, threads_note=True):
+    """Time the oracle (as it stands) on one sequence of the batched workload."""
+    import oracle
+    from kda_state_chunked_gb300 import workloads
+    w = workloads.WORKLOADS[WORKLOAD]
+    t = toks_cpu_fn()
+    ck = [[p for p in range(2048, w.T + 1, 2048)]]
+    t0 = time.perf_counter()
+    oracle.kda_run(t["q"], t["k"], t["v"], t["alpha"], t["beta"], t["conv_w"], [0, w.T], ckpt_counts=ck)
+    sec = time.perf_counter() - t0
+    return {"value": w.T / sec, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"sequence 0 of the batched workload: {w.T} tokens x {w.H} heads, conv + "
+                      f"fp64 token recurrence + 4 checkpoints ({sec:.2f} s wall)"}
+
+
+# --------------------------------------------------------------------------- arms
+def run_ours(args, rank, world, dev):
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(dev)
+    peaks = _peaks()
+    bench = BatchedPrefill(dev, seed_offset=rank * 1000)
+    stream = torch.cuda.current_stream()
+    w = bench.w
+
+    # device-resident timed region
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        total_ms, per = _time_steps(bench.step, args.steps, args.warmup, stream)
+    rc, bits = bench.kda.kda_sync_status(bench.status)
+    assert rc == bench.kda.KDA_OK, f"device status {bits}"
+    t = torch.tensor([total_ms], dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.barrier()
+    ms_per_step = float(t[0]) / args.steps
+    tokens_per_step = bench.T_tot * world
+    value = tokens_per_step / (ms_per_step * 1e-3)
+    launch_ms = statistics.mean(per)
+    ab = bench.algorithmic_bytes()
+    achieved = ab / (launch_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+            "kernel": "prefill", "algorithmic_bytes_per_launch": ab,
+            "launch_ms": launch_ms,
+            "traffic": _traffic("prefill_batched", ["kernels/prefill_simt.cu"], 1.0),
+            "tensor": {"flops_per_launch": bench.algorithmic_flops(),
+                       "achieved_tflops": bench.algorithmic_flops() / (launch_ms * 1e-3) / 1e12,
+                       "peak_tflops": peaks["bf16_tflops"]}}
+    roof["tensor"]["frac"] = roof["tensor"]["achieved_tflops"] / peaks["bf16_tflops"]
+
+    # end to end through the public API with host buffers
+    host = {k: v.cpu().pin_memory() for k, v in bench.toks.items()}
+    dtoks = {k: torch.empty_like(v) for k, v in bench.toks.items()}
+    o_host = torch.empty(bench.o.shape, dtype=bench.o.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = o_host.numel() * o_host.element_size()
+
+    def e2e_step():
+        for k in host:
+            dtoks[k].copy_(host[k], non_blocking=True)
+        bench.step(dtoks)
+        o_host.copy_(bench.o, non_blocking=True)
+
+    e2e_ms, _ = _time_steps(e2e_step, args.steps, args.warmup, stream)
+    te = torch.tensor([e2e_ms], dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = tokens_per_step / (float(te[0]) / args.steps * 1e-3)
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; q,k unit-norm N(0,1), v N(0,1), beta=sigmoid(N(0,1)), "
+                    "alpha=sigmoid(N(3,1)), conv w N(0,0.5^2))",
+            "config": {"workload": "batched prefill: 4 sequences x 8192 tokens, H=16, d_k=d_v=128, "
+                                   "bf16 inputs, fp32 state, chunk 64, conv width 4, checkpoints at "
+                                   "every 4th 512-token hash-block end, 64 KiB pages",
+                       "nseq": w.nseq, "seq_len": w.T, "H": w.H, "d": w.d, "chunk": 64, "stride": w.stride,
+                       "page_bytes": w.page_bytes, "checkpoints_per_step": bench.n_ckpt,
+                       "l2": f"inputs larger than L2 ({ab / 1e6:.0f} MB per step, no flush)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roof,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "clocks": clk.summary(),
+            "gpu_launches": args.steps}
+    if rank == 0 and not args.no_extras:
+        dec = _decode_phase(dev)
+        dec["roofline"] = {"bound": "hbm", "achieved": dec["achieved_gbs"], "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": dec["achieved_gbs"] / peaks["hbm_gbs"]}
+        line["decode"] = dec
+        io = _ckpt_io_phase(dev)
+        for k in ("write", "restore"):
+            io[k]["frac"] = io[k]["gbs"] / peaks["hbm_gbs"]
+        line["ckpt_io"] = io
+        line["gpu_launches"] = args.steps   # prefill launches in the headline timed region
+    if rank == 0 and world == 1 and not args.no_cpu:
+        def cpu_toks():
+            return {k: (v[:w.T] if k != "conv_w" else v).cpu() for k, v in bench.toks.items()}
+        line["cpu_baseline"] = _oracle_sample(cpu_toks)
+    return line
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, over a bounded sample per step."""
+    if rank != 0:
+        return None
+    import torch
+    from kda_state_chunked_gb300 import workloads
+    w = workloads.WORKLOADS[WORKLOAD]
+    toks = workloads.make_tokens(w.T, w.H, w.d, w.dtype, w.seed, "cpu")
+    samples = []
+    for i in range(args.warmup + args.steps):
+        r = _oracle_sample(lambda: toks)
+        if i >= args.warmup:
+            samples.append(r)
+    sec = statistics.mean(w.T / s["value"] for s in samples)
+    value = w.T / sec
+    cb = dict(samples[-1])
+    cb["value"] = value
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, same distributions as the GPU arm)",
+            "config": {"workload": "batched prefill (one 8192-token sequence x 16 heads per step: "
+                                   "bounded sample of the 4-sequence workload)",
+                       "nseq": 1, "seq_len": w.T, "H": w.H, "d": w.d},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip the decode and copy phases")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    line = run_ours(args, rank, world, f"cuda:{local}")
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * kda.h — C ABI of the KDA state library (libkda.so) for one GB300 GPU (sm_103a).
+ *
+ * The library computes the Kimi Delta Attention (KDA) state path:
+ *   - a chunked varlen prefill that reads q, k, v, alpha, beta, applies the width-4 causal
+ *     depthwise conv to q | k | v, runs the recurrence
+ *         S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,  o_t = S_t^T q_t
+ *     (decay first, then the delta-rule write, then the read: "Lesson 01 · Architecture
+ *     map", §两种 Attention，两种状态), writes o, streams checkpoints of (S, conv window) at
+ *     a sparse subset of 512-token hash-block ends into a paged pool ("Cache de préfixe
+ *     hybride KDA–MLA", §La solution and §Le fonctionnement du prefill) and writes the
+ *     final state to the sequence's private (active) object;
+ *   - resume from any checkpoint: copy it into the private object, then prefill with
+ *     has_init = 1 (same page, §Les checkpoints sont en lecture seule);
+ *   - a batched single-token decode step that gathers each request's state through a page
+ *     table and updates it in place ("KIMI K3 경량 복제에서 본 KDA의 AI 인프라 과제",
+ *     §0x08 8.2.2: conv state and recurrent state handed to a fused decode kernel).
+ *
+ * Conventions
+ * -----------
+ * - Every function returns a kda_status (int); functions that return a count return it as
+ *   a non-negative value and errors as negative kda_status values.
+ * - dtype: KDA_F32 or KDA_BF16; it is the type of q, k, v, alpha, beta, o and of the conv
+ *   window stored in records.  The recurrent state is always fp32.  conv_w is always fp32.
+ * - "device" pointers are CUDA device addresses on the current device; "host" pointers are
+ *   ordinary host memory that is read (or written) before the call returns.
+ * - The caller owns every device buffer (inputs, outputs, the pool base, page tables, the
+ *   workspace and the int32 device status word).  The library owns only the host-side pool
+ *   metadata behind the opaque kda_pool (free set, reference counts) and a few pinned host
+ *   staging buffers that carry call metadata to the workspace.
+ * - GPU work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream).  Buffers handed to a call must stay alive until that work completes.
+ * - Nothing aborts or traps.  Host-side argument errors return KDA_EINVAL / KDA_ENOPAGES /
+ *   KDA_EREF before anything is enqueued.  Kernels check page ids and metadata and, on a bad
+ *   value, skip the access and set a bit in *status_dev; kda_sync_status reports it as
+ *   KDA_EDEVICE.  CUDA launch errors return KDA_ECUDA.
+ * - A kda_pool may be used from one host thread at a time.
+ *
+ * Paged state layout (bit-exact)
+ * ------------------------------
+ * One page byte size for the whole pool.  A head record is S as fp32 row-major [d][d]
+ * (row i = key channel i, column j = value channel j), then the conv window [3][3d] in
+ * dtype (oldest raw token first, channels q | k | v), zero-padded to a multiple of 256
+ * bytes.  An object is the H head records of one sequence, one after another in head order
+ * (heads stored contiguously: "Cache de préfixe hybride KDA–MLA", §La mise en page
+ * unifiée).  Logical byte x of an object lives in page list[x / page_bytes] at byte
+ * x % page_bytes of that page; the page lists are int32 [P] with P = kda_object_pages().
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status_code {
+    KDA_OK = 0,
+    KDA_EINVAL = -1,    /* bad argument, shape, dtype, position or size */
+    KDA_ENOPAGES = -2,  /* pool exhausted: nothing was allocated */
+    KDA_EREF = -3,      /* reference-count misuse (freeing a free page, claiming a used one) */
+    KDA_ECUDA = -4,     /* CUDA launch / runtime error */
+    KDA_EDEVICE = -5    /* a kernel found a bad page id or metadata (see kda_sync_status) */
+} kda_status_code;
+
+typedef enum kda_dtype { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Device status bits set by kernels (reported through kda_sync_status). */
+#define KDA_DEV_BAD_PAGE 1   /* a page id outside [0, num_pages) was met; access skipped */
+#define KDA_DEV_BAD_META 2   /* inconsistent metadata in the workspace; work skipped */
+
+typedef struct kda_pool kda_pool;
+
+/* ---------------------------------------------------------------- sizes --------------- */
+
+/* Bytes of one head record for head dimension d (64 or 128) and dtype; KDA_EINVAL if bad. */
+int64_t kda_record_bytes(int32_t d, int32_t dtype);
+
+/* Bytes of one object (H records).  KDA_EINVAL if bad. */
+int64_t kda_object_bytes(int32_t H, int32_t d, int32_t dtype);
+
+/* Pages per object in this pool: ceil(kda_object_bytes / page_bytes).  KDA_EINVAL if bad. */
+int32_t kda_object_pages(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype);
+
+/* ---------------------------------------------------------------- pool ---------------- */
+/* One refcounted page allocator for every state object ("Cache de préfixe hybride
+ * KDA–MLA", §La mise en page unifiée: one allocation / reference-count / eviction path for
+ * all page kinds).  Device memory for the pages is the caller's: num_pages * page_bytes
+ * bytes at `pool_base`, passed to each GPU call. */
+
+/* page_bytes must be a positive multiple of 256; num_pages > 0.  *out receives the pool. */
+int kda_pool_create(int64_t page_bytes, int32_t num_pages, kda_pool **out);
+int kda_pool_destroy(kda_pool *pool);
+int64_t kda_pool_page_bytes(const kda_pool *pool);
+int32_t kda_pool_num_pages(const kda_pool *pool);
+int32_t kda_pool_free_count(const kda_pool *pool);
+
+/* Allocate n pages, lowest free id first, each with refcount 1; ids written to out_ids[n].
+ * KDA_ENOPAGES (nothing allocated) if fewer than n pages are free. */
+int kda_page_alloc(kda_pool *pool, int32_t n, int32_t *out_ids);
+
+/* Take the n given free pages (refcount 0 -> 1), e.g. to follow a caller's page table.
+ * KDA_EREF if any is in use or repeated, KDA_EINVAL if out of range; all or nothing. */
+int kda_page_claim(kda_pool *pool, int32_t n, const int32_t *ids);
+
+/* Pin (refcount + 1) n pages that are in use; KDA_EREF if one is free.  All or nothing.
+ * Pinning every hit page before any allocation is the first concurrency rule of "Cache de
+ * préfixe hybride KDA–MLA", §La cohérence sous ordonnancement concurrent. */
+int kda_page_incref(kda_pool *pool, int32_t n, const int32_t *ids);
+
+/* Unpin n pages; a page is free again at refcount 0.  KDA_EREF if a count would go below
+ * zero (repeated ids count once per occurrence).  All or nothing. */
+int kda_page_decref(kda_pool *pool, int32_t n, const int32_t *ids);
+
+/* Refcount of page id, or KDA_EINVAL if out of range. */
+int32_t kda_page_refcount(const kda_pool *pool, int32_t id);
+
+/* ---------------------------------------------------------------- policy -------------- */
+
+/* Checkpoint positions of one forward over absolute positions [start, end): every p with
+ * p % (hash_block * stride) == 0 and start < p <= end, plus floor(end / hash_block) *
+ * hash_block when include_last != 0 and it is > start ("Cache de préfixe hybride KDA–MLA",
+ * §La solution: a sparse subset of hash-block ends; §Le fonctionnement du prefill: persist
+ * the last hash-aligned position processed).  Writes up to cap ascending positions to out
+ * and returns the total count (which may exceed cap), or KDA_EINVAL. */
+int32_t kda_ckpt_positions(int64_t start, int64_t end, int32_t hash_block, int32_t stride,
+                           int32_t include_last, int64_t *out, int32_t cap);
+
+/* Plan the checkpoints of one prefill call and allocate their objects.  Sequence s covers
+ * absolute positions [start_pos[s], start_pos[s] + cu_seqlens[s+1] - cu_seqlens[s]).
+ * Checkpoints are listed in (sequence ascending, position ascending) order and each gets P
+ * fresh pages, lowest free first, refcount 1 (new checkpoints go to fresh slots: "Cache de
+ * préfixe hybride KDA–MLA", §Les checkpoints sont en lecture seule).  Outputs (host):
+ * *out_n, out_seq[cap], out_pos[cap], out_pages[cap * P].  KDA_EINVAL if more than cap
+ * checkpoints would result; KDA_ENOPAGES if the pool cannot hold them (nothing allocated).
+ * hash_block must be a positive multiple of 64. */
+int kda_ckpt_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t nseq,
+                  const int32_t *cu_seqlens, const int64_t *start_pos, int32_t hash_block,
+                  int32_t stride, int32_t include_last, int32_t cap, int32_t *out_n,
+                  int32_t *out_seq, int64_t *out_pos, int32_t *out_pages);
+
+/* ---------------------------------------------------------------- prefill ------------- */
+
+/* Workspace bytes kda_prefill_varlen needs for nseq sequences and n_ckpt checkpoints. */
+int64_t kda_prefill_workspace_bytes(int32_t nseq, int32_t n_ckpt, int32_t pages_per_object);
+
+/* Chunked varlen prefill (chunk = 64 tokens, chunks aligned to absolute positions).
+ *   H, d, dtype      heads, head dimension (64 or 128), dtype of the token tensors
+ *   nseq             number of sequences (>= 1)
+ *   cu_seqlens       host int32 [nseq + 1], token offsets into the packed arrays
+ *   start_pos        host int64 [nseq], absolute position of each sequence's first token
+ *   has_init         host uint8 [nseq]; 1 = read the initial (S, window) from the active
+ *                    object, 0 = start from zeros
+ *   q, k, v, alpha   device [T_tot][H][d] dtype (q, k as given: any normalisation is the
+ *                    caller's; the conv runs here)
+ *   beta             device [T_tot][H] dtype
+ *   conv_w           device fp32 [H][3d][4]; tap j multiplies raw token t-3+j
+ *   o                device [T_tot][H][d] dtype, written
+ *   pool_base        device base of the page pool
+ *   active_pages     host int32 [nseq * P]: each sequence's private object (read when
+ *                    has_init, always written with the final state and window)
+ *   n_ckpt, ckpt_seq, ckpt_pos, ckpt_pages   host: the checkpoints to stream (as produced
+ *                    by kda_ckpt_plan): sequence ids ascending, positions ascending within
+ *                    a sequence, each position p with start < p <= end and p % 64 == 0 or
+ *                    p == end; ckpt_pages [n_ckpt * P] must be allocated pages
+ *   workspace        device scratch of at least kda_prefill_workspace_bytes(); the call
+ *                    writes metadata there (one async host-to-device copy)
+ *   status_dev       device int32 status word (bits KDA_DEV_*), OR-ed by the kernel
+ * The state checkpoint at p is S after tokens [0, p) with the raw tokens p-3, p-2, p-1 as
+ * window, in the record layout above. */
+int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t nseq,
+                       const int32_t *cu_seqlens, const int64_t *start_pos,
+                       const uint8_t *has_init, const void *q, const void *k, const void *v,
+                       const void *alpha, const void *beta, const float *conv_w, void *o,
+                       void *pool_base, const int32_t *active_pages, int32_t n_ckpt,
+                       const int32_t *ckpt_seq, const int64_t *ckpt_pos,
+                       const int32_t *ckpt_pages, void *workspace, int64_t ws_bytes,
+                       int32_t *status_dev, void *stream);
+
+/* ---------------------------------------------------------------- decode -------------- */
+
+/* One decode step for B requests, one token each.  q, k, v, alpha device [B][H][d] dtype,
+ * beta device [B][H] dtype, conv_w device fp32 [H][3d][4], o device [B][H][d] dtype.
+ * state_pages device int32 [B * P]: the page table of each request's active object, read
+ * and updated in place (S and the conv window: the window is shifted by one token).
+ * Page ids outside the pool set KDA_DEV_BAD_PAGE and that (request, head) is skipped. */
+int kda_decode_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B,
+                    const void *q, const void *k, const void *v, const void *alpha,
+                    const void *beta, const float *conv_w, void *o, void *pool_base,
+                    const int32_t *state_pages, int32_t *status_dev, void *stream);
+
+/* ---------------------------------------------------------------- checkpoints --------- */
+
+/* Workspace bytes for a checkpoint copy of n objects. */
+int64_t kda_copy_workspace_bytes(int32_t n, int32_t pages_per_object);
+
+/* Snapshot: allocate n fresh objects (lowest free first, refcount 1), copy each source
+ * object (host page lists src_pages [n * P]) into them and return their pages in
+ * dst_pages_out [n * P] (host).  KDA_ENOPAGES if the pool cannot hold them. */
+int kda_ckpt_write(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n,
+                   const int32_t *src_pages, int32_t *dst_pages_out, void *pool_base,
+                   void *workspace, int64_t ws_bytes, int32_t *status_dev, void *stream);
+
+/* Restore (copy-on-write): pin (incref) the checkpoint pages, then copy each checkpoint
+ * object ckpt_pages [n * P] into the private object active_pages [n * P] (both host
+ * lists).  The checkpoint is only read.  Release the pin with kda_ckpt_release once the
+ * copy has completed on the stream. */
+int kda_ckpt_restore(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n,
+                     const int32_t *ckpt_pages, const int32_t *active_pages, void *pool_base,
+                     void *workspace, int64_t ws_bytes, int32_t *status_dev, void *stream);
+
+/* Drop the pin kda_ckpt_restore took: decref the same n * P checkpoint page ids. */
+int kda_ckpt_release(kda_pool *pool, int32_t n, int32_t pages_per_object,
+                     const int32_t *ckpt_pages);
+
+/* ---------------------------------------------------------------- status -------------- */
+
+/* Wait for `stream`, read and clear *status_dev.  Returns KDA_OK, KDA_EDEVICE (bits in
+ * *bits_out if not NULL) or KDA_ECUDA. */
+int kda_sync_status(int32_t *status_dev, void *stream, int32_t *bits_out);
+
+/* Static description of a status code. */
+const char *kda_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

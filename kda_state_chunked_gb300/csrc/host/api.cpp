@@ -1,0 +1,343 @@
+// C ABI of libkda.so: argument validation, checkpoint planning, metadata upload and kernel
+// launches.  Every GPU call is stream-ordered and makes no host synchronisation except
+// when a pinned staging slot is still in use by an earlier copy.
+#include <algorithm>
+#include <cstring>
+#include <unordered_set>
+#include <vector>
+
+#include "kda.h"
+#include "pool.h"
+#include "../kda_internal.h"
+
+namespace {
+
+using kda::CkptMeta;
+using kda::SeqMeta;
+
+bool valid_shape(int32_t H, int32_t d, int32_t dtype) {
+    return H > 0 && H <= 4096 && (d == 64 || d == 128) && (dtype == KDA_F32 || dtype == KDA_BF16);
+}
+
+int64_t elem_size(int32_t dtype) { return dtype == KDA_BF16 ? 2 : 4; }
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+kda::PoolView pool_view(const kda_pool *p, void *base, int32_t H, int32_t d, int32_t dtype) {
+    kda::PoolView v;
+    v.base = static_cast<uint8_t *>(base);
+    v.page_bytes = p->page_bytes;
+    v.num_pages = p->num_pages;
+    v.pages_per_object = kda_object_pages(p, H, d, dtype);
+    v.rec_bytes = kda_record_bytes(d, dtype);
+    return v;
+}
+
+// Pages written by a call must be private to it: allocated, refcount exactly 1, and not
+// repeated (a checkpoint visible to others is never written in place).
+int check_private(const kda_pool *p, const int32_t *ids, int64_t n, std::unordered_set<int32_t> &seen) {
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t id = ids[i];
+        if (id < 0 || id >= p->num_pages) return KDA_EINVAL;
+        if (p->ref[id] != 1 || !seen.insert(id).second) return KDA_EREF;
+    }
+    return KDA_OK;
+}
+
+int check_allocated(const kda_pool *p, const int32_t *ids, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) {
+        if (ids[i] < 0 || ids[i] >= p->num_pages) return KDA_EINVAL;
+        if (p->ref[ids[i]] < 1) return KDA_EREF;
+    }
+    return KDA_OK;
+}
+
+int64_t prefill_ws_bytes(int64_t nseq, int64_t nck, int64_t P) {
+    return align_up(nseq * (int64_t)sizeof(SeqMeta), 256) + align_up(nck * (int64_t)sizeof(CkptMeta), 256) +
+           align_up((nseq + nck) * P * 4, 256);
+}
+
+int copy_objects(kda_pool *p, int32_t H, int32_t d, int32_t dtype, int32_t n, const int32_t *src,
+                 const int32_t *dst, void *pool_base, void *ws, int64_t ws_bytes, int32_t *status,
+                 cudaStream_t stream) {
+    const int32_t P = kda_object_pages(p, H, d, dtype);
+    const int64_t list = (int64_t)n * P * 4;
+    std::vector<int32_t> both((size_t)n * P * 2);
+    std::memcpy(both.data(), src, (size_t)list);
+    std::memcpy(both.data() + (size_t)n * P, dst, (size_t)list);
+    int rc = kda::stage_upload(p, both.data(), (size_t)(2 * list), ws, stream);
+    if (rc != KDA_OK) return rc;
+    kda::CopyArgs a;
+    a.n = n;
+    a.object_bytes = kda_object_bytes(H, d, dtype);
+    a.pool = pool_view(p, pool_base, H, d, dtype);
+    a.src_pages = static_cast<const int32_t *>(ws);
+    a.dst_pages = static_cast<const int32_t *>(ws) + (size_t)n * P;
+    a.status = status;
+    return kda::launch_copy_objects(a, stream) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t kda_record_bytes(int32_t d, int32_t dtype) {
+    if (!valid_shape(1, d, dtype)) return KDA_EINVAL;
+    return align_up((int64_t)d * d * 4 + (int64_t)kda::kWin * 3 * d * elem_size(dtype), 256);
+}
+
+int64_t kda_object_bytes(int32_t H, int32_t d, int32_t dtype) {
+    if (!valid_shape(H, d, dtype)) return KDA_EINVAL;
+    return (int64_t)H * kda_record_bytes(d, dtype);
+}
+
+int32_t kda_object_pages(const kda_pool *p, int32_t H, int32_t d, int32_t dtype) {
+    if (!p || !valid_shape(H, d, dtype)) return KDA_EINVAL;
+    return (int32_t)((kda_object_bytes(H, d, dtype) + p->page_bytes - 1) / p->page_bytes);
+}
+
+int32_t kda_ckpt_positions(int64_t start, int64_t end, int32_t hash_block, int32_t stride,
+                           int32_t include_last, int64_t *out, int32_t cap) {
+    if (start < 0 || end < start || hash_block <= 0 || stride <= 0 || cap < 0 || (cap > 0 && !out))
+        return KDA_EINVAL;
+    const int64_t step = (int64_t)hash_block * stride;
+    int64_t count = 0;
+    int64_t last_emitted = -1;
+    for (int64_t p = (start / step + 1) * step; p <= end; p += step) {
+        if (count < cap) out[count] = p;
+        ++count;
+        last_emitted = p;
+    }
+    if (include_last) {
+        const int64_t last = (end / hash_block) * hash_block;
+        if (last > start && last != last_emitted) {
+            if (count < cap) out[count] = last;   // last >= every stride multiple <= end
+            ++count;
+        }
+    }
+    if (count > INT32_MAX) return KDA_EINVAL;
+    return (int32_t)count;
+}
+
+int kda_ckpt_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t nseq,
+                  const int32_t *cu_seqlens, const int64_t *start_pos, int32_t hash_block,
+                  int32_t stride, int32_t include_last, int32_t cap, int32_t *out_n,
+                  int32_t *out_seq, int64_t *out_pos, int32_t *out_pages) {
+    if (!pool || !valid_shape(H, d, dtype) || nseq < 0 || !cu_seqlens || !start_pos || !out_n ||
+        hash_block <= 0 || hash_block % kda::kChunk != 0 || stride <= 0 || cap < 0)
+        return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype);
+    std::vector<std::pair<int32_t, int64_t>> items;
+    for (int32_t s = 0; s < nseq; ++s) {
+        const int64_t len = (int64_t)cu_seqlens[s + 1] - cu_seqlens[s];
+        if (len < 0 || start_pos[s] < 0) return KDA_EINVAL;
+        const int32_t cnt = kda_ckpt_positions(start_pos[s], start_pos[s] + len, hash_block, stride,
+                                               include_last, nullptr, 0);
+        if (cnt < 0) return cnt;
+        std::vector<int64_t> pos((size_t)cnt);
+        kda_ckpt_positions(start_pos[s], start_pos[s] + len, hash_block, stride, include_last,
+                           pos.data(), cnt);
+        for (int64_t p : pos) items.emplace_back(s, p);
+    }
+    if ((int64_t)items.size() > cap) return KDA_EINVAL;
+    if (!items.empty() && (!out_seq || !out_pos || !out_pages)) return KDA_EINVAL;
+    std::lock_guard<std::mutex> g(pool->mu);
+    if ((int64_t)pool->free_ids.size() < (int64_t)items.size() * P) return KDA_ENOPAGES;
+    for (size_t i = 0; i < items.size(); ++i) {
+        out_seq[i] = items[i].first;
+        out_pos[i] = items[i].second;
+        kda::pool_alloc(pool, P, out_pages + i * (size_t)P);
+    }
+    *out_n = (int32_t)items.size();
+    return KDA_OK;
+}
+
+int64_t kda_prefill_workspace_bytes(int32_t nseq, int32_t n_ckpt, int32_t pages_per_object) {
+    if (nseq < 0 || n_ckpt < 0 || pages_per_object <= 0) return KDA_EINVAL;
+    return prefill_ws_bytes(nseq, n_ckpt, pages_per_object);
+}
+
+int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t nseq,
+                       const int32_t *cu_seqlens, const int64_t *start_pos,
+                       const uint8_t *has_init, const void *q, const void *k, const void *v,
+                       const void *alpha, const void *beta, const float *conv_w, void *o,
+                       void *pool_base, const int32_t *active_pages, int32_t n_ckpt,
+                       const int32_t *ckpt_seq, const int64_t *ckpt_pos,
+                       const int32_t *ckpt_pages, void *workspace, int64_t ws_bytes,
+                       int32_t *status_dev, void *stream) {
+    if (!pool || !valid_shape(H, d, dtype) || nseq < 1 || !cu_seqlens || !start_pos || !has_init ||
+        !conv_w || !pool_base || !active_pages || n_ckpt < 0 || !workspace || !status_dev)
+        return KDA_EINVAL;
+    if (n_ckpt > 0 && (!ckpt_seq || !ckpt_pos || !ckpt_pages)) return KDA_EINVAL;
+    if (cu_seqlens[0] != 0) return KDA_EINVAL;
+    for (int32_t s = 0; s < nseq; ++s)
+        if (cu_seqlens[s + 1] < cu_seqlens[s] || start_pos[s] < 0 || has_init[s] > 1) return KDA_EINVAL;
+    const int64_t T_tot = cu_seqlens[nseq];
+    if ((int64_t)T_tot * H * d > ((int64_t)1 << 40)) return KDA_EINVAL;
+    if (T_tot > 0 && (!q || !k || !v || !alpha || !beta || !o)) return KDA_EINVAL;
+    if ((uintptr_t)workspace % 16 != 0) return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype);
+    if (ws_bytes < prefill_ws_bytes(nseq, n_ckpt, P)) return KDA_EINVAL;
+
+    std::vector<SeqMeta> seqs((size_t)nseq);
+    std::vector<CkptMeta> cks((size_t)n_ckpt);
+    std::vector<int32_t> pages((size_t)(nseq + n_ckpt) * P);
+    {
+        std::lock_guard<std::mutex> g(pool->mu);
+        std::unordered_set<int32_t> seen;
+        int rc = check_private(pool, active_pages, (int64_t)nseq * P, seen);
+        if (rc != KDA_OK) return rc;
+        rc = check_private(pool, ckpt_pages, (int64_t)n_ckpt * P, seen);
+        if (rc != KDA_OK) return rc;
+    }
+    std::memcpy(pages.data(), active_pages, (size_t)nseq * P * 4);
+    if (n_ckpt) std::memcpy(pages.data() + (size_t)nseq * P, ckpt_pages, (size_t)n_ckpt * P * 4);
+    int32_t ci = 0;
+    for (int32_t s = 0; s < nseq; ++s) {
+        SeqMeta &m = seqs[s];
+        m.start_pos = start_pos[s];
+        m.tok_begin = cu_seqlens[s];
+        m.len = cu_seqlens[s + 1] - cu_seqlens[s];
+        m.has_init = has_init[s];
+        m.active_off = s * P;
+        m.ckpt_begin = ci;
+        const int64_t end = m.start_pos + m.len;
+        int64_t prev = m.start_pos;
+        while (ci < n_ckpt && ckpt_seq[ci] == s) {
+            const int64_t p = ckpt_pos[ci];
+            if (p <= prev || p > end || (p % kda::kChunk != 0 && p != end)) return KDA_EINVAL;
+            cks[ci].pos = p;
+            cks[ci].seq = s;
+            cks[ci].pages_off = (nseq + ci) * P;
+            prev = p;
+            ++ci;
+        }
+        m.ckpt_count = ci - m.ckpt_begin;
+    }
+    if (ci != n_ckpt) return KDA_EINVAL;   // sequence ids not ascending or out of range
+
+    // One upload: [SeqMeta][CkptMeta][pages], each part 256-byte aligned.
+    const int64_t o_ck = align_up((int64_t)nseq * sizeof(SeqMeta), 256);
+    const int64_t o_pg = o_ck + align_up((int64_t)n_ckpt * sizeof(CkptMeta), 256);
+    const int64_t total = o_pg + (int64_t)pages.size() * 4;
+    std::vector<uint8_t> blob((size_t)total, 0);
+    std::memcpy(blob.data(), seqs.data(), seqs.size() * sizeof(SeqMeta));
+    if (n_ckpt) std::memcpy(blob.data() + o_ck, cks.data(), cks.size() * sizeof(CkptMeta));
+    std::memcpy(blob.data() + o_pg, pages.data(), pages.size() * 4);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = kda::stage_upload(pool, blob.data(), (size_t)total, workspace, st);
+    if (rc != KDA_OK) return rc;
+
+    kda::PrefillArgs a;
+    a.H = H; a.d = d; a.dtype = dtype; a.nseq = nseq;
+    a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.conv_w = conv_w; a.o = o;
+    a.pool = pool_view(pool, pool_base, H, d, dtype);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.seqs = reinterpret_cast<const SeqMeta *>(ws);
+    a.ckpts = reinterpret_cast<const CkptMeta *>(ws + o_ck);
+    a.pages = reinterpret_cast<const int32_t *>(ws + o_pg);
+    a.status = status_dev;
+    return kda::launch_prefill_simt(a, st) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+
+int kda_decode_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B,
+                    const void *q, const void *k, const void *v, const void *alpha,
+                    const void *beta, const float *conv_w, void *o, void *pool_base,
+                    const int32_t *state_pages, int32_t *status_dev, void *stream) {
+    if (!pool || !valid_shape(H, d, dtype) || B < 0 || (int64_t)B * H > INT32_MAX || !status_dev)
+        return KDA_EINVAL;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !alpha || !beta || !conv_w || !o || !pool_base || !state_pages)
+        return KDA_EINVAL;
+    kda::DecodeArgs a;
+    a.H = H; a.d = d; a.dtype = dtype; a.B = B;
+    a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.conv_w = conv_w; a.o = o;
+    a.pool = pool_view(pool, pool_base, H, d, dtype);
+    a.state_pages = state_pages;
+    a.status = status_dev;
+    return kda::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+
+int64_t kda_copy_workspace_bytes(int32_t n, int32_t pages_per_object) {
+    if (n < 0 || pages_per_object <= 0) return KDA_EINVAL;
+    return align_up((int64_t)n * pages_per_object * 8, 256);
+}
+
+int kda_ckpt_write(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n,
+                   const int32_t *src_pages, int32_t *dst_pages_out, void *pool_base,
+                   void *workspace, int64_t ws_bytes, int32_t *status_dev, void *stream) {
+    if (!pool || !valid_shape(H, d, dtype) || n < 0 || !pool_base || !workspace || !status_dev)
+        return KDA_EINVAL;
+    if (n == 0) return KDA_OK;
+    if (!src_pages || !dst_pages_out) return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype);
+    if (ws_bytes < kda_copy_workspace_bytes(n, P) || (uintptr_t)workspace % 16 != 0) return KDA_EINVAL;
+    std::lock_guard<std::mutex> g(pool->mu);
+    int rc = check_allocated(pool, src_pages, (int64_t)n * P);
+    if (rc != KDA_OK) return rc;
+    rc = kda::pool_alloc(pool, n * P, dst_pages_out);
+    if (rc != KDA_OK) return rc;
+    rc = copy_objects(pool, H, d, dtype, n, src_pages, dst_pages_out, pool_base, workspace, ws_bytes,
+                      status_dev, static_cast<cudaStream_t>(stream));
+    if (rc != KDA_OK) kda::pool_decref(pool, n * P, dst_pages_out);
+    return rc;
+}
+
+int kda_ckpt_restore(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n,
+                     const int32_t *ckpt_pages, const int32_t *active_pages, void *pool_base,
+                     void *workspace, int64_t ws_bytes, int32_t *status_dev, void *stream) {
+    if (!pool || !valid_shape(H, d, dtype) || n < 0 || !pool_base || !workspace || !status_dev)
+        return KDA_EINVAL;
+    if (n == 0) return KDA_OK;
+    if (!ckpt_pages || !active_pages) return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype);
+    if (ws_bytes < kda_copy_workspace_bytes(n, P) || (uintptr_t)workspace % 16 != 0) return KDA_EINVAL;
+    std::lock_guard<std::mutex> g(pool->mu);
+    int rc = check_allocated(pool, ckpt_pages, (int64_t)n * P);
+    if (rc != KDA_OK) return rc;
+    std::unordered_set<int32_t> seen;
+    rc = check_private(pool, active_pages, (int64_t)n * P, seen);
+    if (rc != KDA_OK) return rc;
+    for (int64_t i = 0; i < (int64_t)n * P; ++i)
+        if (seen.count(ckpt_pages[i])) return KDA_EREF;   // never copy onto the source
+    rc = kda::pool_incref(pool, n * P, ckpt_pages);
+    if (rc != KDA_OK) return rc;
+    rc = copy_objects(pool, H, d, dtype, n, ckpt_pages, active_pages, pool_base, workspace, ws_bytes,
+                      status_dev, static_cast<cudaStream_t>(stream));
+    if (rc != KDA_OK) kda::pool_decref(pool, n * P, ckpt_pages);
+    return rc;
+}
+
+int kda_ckpt_release(kda_pool *pool, int32_t n, int32_t pages_per_object, const int32_t *ckpt_pages) {
+    if (!pool || n < 0 || pages_per_object <= 0) return KDA_EINVAL;
+    return kda_page_decref(pool, n * pages_per_object, ckpt_pages);
+}
+
+int kda_sync_status(int32_t *status_dev, void *stream, int32_t *bits_out) {
+    if (!status_dev) return KDA_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t h = 0;
+    if (cudaMemcpyAsync(&h, status_dev, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return KDA_ECUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ECUDA;
+    if (bits_out) *bits_out = h;
+    if (h != 0) {
+        if (cudaMemsetAsync(status_dev, 0, 4, st) != cudaSuccess) return KDA_ECUDA;
+        if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ECUDA;
+        return KDA_EDEVICE;
+    }
+    return KDA_OK;
+}
+
+const char *kda_status_string(int code) {
+    switch (code) {
+        case KDA_OK: return "ok";
+        case KDA_EINVAL: return "invalid argument";
+        case KDA_ENOPAGES: return "page pool exhausted";
+        case KDA_EREF: return "reference-count misuse";
+        case KDA_ECUDA: return "CUDA error";
+        case KDA_EDEVICE: return "device-side check failed";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// Host-side page pool of libkda.so: one page byte size, lowest-free-first allocation,
+// reference counts, and pinned staging buffers that carry call metadata to the device.
+#pragma once
+
+#include <cstdint>
+#include <mutex>
+#include <set>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+struct kda_pool {
+    int64_t page_bytes = 0;
+    int32_t num_pages = 0;
+    std::vector<int32_t> ref;        // reference count per page (0 = free)
+    std::set<int32_t> free_ids;      // ordered: begin() is the lowest free id
+
+    // Pinned host staging slots, reused round-robin; each slot's event marks the end of the
+    // last host-to-device copy that read it.
+    struct Slot {
+        void *host = nullptr;
+        size_t cap = 0;
+        cudaEvent_t done = nullptr;
+        bool pending = false;
+    };
+    static constexpr int kSlots = 4;
+    Slot slots[kSlots];
+    int next_slot = 0;
+    std::mutex mu;
+};
+
+namespace kda {
+
+// Allocator primitives (caller holds pool->mu).  All return a kda_status.
+int pool_alloc(kda_pool *p, int32_t n, int32_t *out);
+int pool_decref(kda_pool *p, int32_t n, const int32_t *ids);
+int pool_incref(kda_pool *p, int32_t n, const int32_t *ids);
+
+// Copy `bytes` of host data to device memory `dst` on `stream` through a pinned slot.
+// The host data may be reused as soon as this returns.
+int stage_upload(kda_pool *p, const void *src, size_t bytes, void *dst, cudaStream_t stream);
+
+}  // namespace kda

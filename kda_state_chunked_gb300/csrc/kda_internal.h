@@ -1,0 +1,81 @@
+// Internal declarations shared by the host library and the CUDA kernels of libkda.so.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int kChunk = 64;   // tokens per chunk; chunks are aligned to absolute positions
+constexpr int kConvW = 4;    // short causal conv width (taps on t-3 .. t)
+constexpr int kWin = kConvW - 1;
+
+// Per-sequence metadata of one prefill call (device copy in the workspace).
+struct SeqMeta {
+    int64_t start_pos;   // absolute position of the first token
+    int32_t tok_begin;   // row of the first token in the packed [T_tot][H][d] arrays
+    int32_t len;         // tokens in this call
+    int32_t has_init;    // 1: read (S, window) from the active object first
+    int32_t ckpt_begin;  // first entry of this sequence in the checkpoint table
+    int32_t ckpt_count;  // number of entries
+    int32_t active_off;  // offset of the active object's page list in the page array
+};
+static_assert(sizeof(SeqMeta) == 32, "SeqMeta layout");
+
+// One checkpoint to stream (device copy in the workspace).
+struct CkptMeta {
+    int64_t pos;         // absolute position p: state after tokens [0, p)
+    int32_t pages_off;   // offset of its page list in the page array
+    int32_t seq;         // owning sequence
+};
+static_assert(sizeof(CkptMeta) == 16, "CkptMeta layout");
+
+// Geometry of the paged pool and of one head record.
+struct PoolView {
+    uint8_t *base;
+    int64_t page_bytes;
+    int32_t num_pages;
+    int32_t pages_per_object;
+    int64_t rec_bytes;   // bytes of one head record (multiple of 256)
+};
+
+struct PrefillArgs {
+    int32_t H, d, dtype, nseq;
+    const void *q, *k, *v, *alpha, *beta;
+    const float *conv_w;
+    void *o;
+    PoolView pool;
+    const SeqMeta *seqs;
+    const CkptMeta *ckpts;
+    const int32_t *pages;
+    int32_t *status;
+};
+
+struct DecodeArgs {
+    int32_t H, d, dtype, B;
+    const void *q, *k, *v, *alpha, *beta;
+    const float *conv_w;
+    void *o;
+    PoolView pool;
+    const int32_t *state_pages;   // [B * P]
+    int32_t *status;
+};
+
+struct CopyArgs {
+    int32_t n;                    // objects
+    int64_t object_bytes;
+    PoolView pool;
+    const int32_t *src_pages;     // [n * P]
+    const int32_t *dst_pages;     // [n * P]
+    int32_t *status;
+};
+
+// Kernel launchers (defined in the .cu files).
+cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_copy_objects(const CopyArgs &a, cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,206 @@
+"""CPU tests of libkda.so's host side: the library loads without a GPU, exports every
+symbol include/kda.h declares, and its allocator / checkpoint policy / sizes agree bit for
+bit with the oracle's independent Python version.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import kda_state_chunked_gb300 as kda
+from kda_state_chunked_gb300 import build as kbuild
+from oracle import policy
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    kbuild.build()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    names = _declared_functions()
+    assert len(names) >= 20
+    L = ctypes.CDLL(kda.library_path())
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    # the binding declares a signature for each of them, under the same name
+    assert sorted(kda._SIGS) == names
+    for n in names:
+        assert callable(getattr(kda, n, None)) or n in ("kda_pool_create", "kda_pool_destroy",
+                                                       "kda_pool_page_bytes", "kda_pool_num_pages",
+                                                       "kda_pool_free_count", "kda_status_string")
+
+
+@pytest.mark.parametrize("H,d,dt", [(16, 128, "bf16"), (32, 128, "bf16"), (2, 64, "f32"),
+                                    (3, 64, "bf16"), (5, 128, "f32")])
+def test_sizes_match_oracle(H, d, dt):
+    assert kda.kda_record_bytes(d, kda.DTYPES[dt]) == policy.record_bytes(d, dt)
+    assert kda.kda_object_bytes(H, d, kda.DTYPES[dt]) == policy.object_bytes(H, d, dt)
+    for pb in (256, 4096, 65536, 262144):
+        pool = kda.Pool(pb, 8)
+        assert pool.object_pages(H, d, kda.DTYPES[dt]) == policy.object_pages(H, d, dt, pb)
+
+
+def test_bad_shapes_rejected():
+    L = kda.lib()
+    assert L.kda_record_bytes(96, 0) == kda.KDA_EINVAL
+    assert L.kda_record_bytes(64, 7) == kda.KDA_EINVAL
+    assert L.kda_object_bytes(0, 64, 0) == kda.KDA_EINVAL
+    h = ctypes.c_void_p()
+    assert L.kda_pool_create(1000, 4, ctypes.byref(h)) == kda.KDA_EINVAL   # not a 256 multiple
+    assert L.kda_pool_create(4096, 0, ctypes.byref(h)) == kda.KDA_EINVAL
+
+
+def test_positions_match_oracle():
+    rng = np.random.default_rng(11)
+    for _ in range(400):
+        start = int(rng.integers(0, 1 << 21))
+        end = start + int(rng.integers(0, 50000))
+        hb = int(rng.choice([64, 128, 512]))
+        stride = int(rng.integers(1, 8))
+        last = bool(rng.integers(0, 2))
+        assert kda.kda_ckpt_positions(start, end, hb, stride, last) == \
+            policy.ckpt_positions(start, end, hb, stride, last)
+    assert kda.kda_ckpt_positions(0, 1048576, 512, 4, True)[-1] == 1048576
+    # truncated output still reports the full count
+    out = np.zeros(2, dtype=np.int64)
+    n = kda.lib().kda_ckpt_positions(0, 8192, 512, 1, 0, out.ctypes.data_as(ctypes.c_void_p), 2)
+    assert n == 16 and list(out) == [512, 1024]
+    assert kda.lib().kda_ckpt_positions(10, 5, 512, 1, 0, None, 0) == kda.KDA_EINVAL
+
+
+def test_allocator_matches_oracle_under_random_traffic():
+    rng = np.random.default_rng(12)
+    N = 64
+    pool = kda.Pool(4096, N)
+    sim = policy.PoolSim(N)
+    for _ in range(3000):
+        op = int(rng.integers(0, 4))
+        if op == 0:
+            n = int(rng.integers(0, 9))
+            try:
+                want = sim.alloc(n)
+            except policy.AllocError:
+                want = None
+            try:
+                got = list(kda.kda_page_alloc(pool, n))
+            except kda.KdaError as e:
+                assert e.code == kda.KDA_ENOPAGES
+                got = None
+            assert got == want
+        else:
+            ids = [int(x) for x in rng.integers(0, N, int(rng.integers(1, 4)))]
+            fn_sim = {1: sim.claim, 2: sim.incref, 3: sim.decref}[op]
+            fn_lib = {1: kda.kda_page_claim, 2: kda.kda_page_incref, 3: kda.kda_page_decref}[op]
+            try:
+                fn_sim(ids)
+                ok_sim = True
+            except policy.AllocError:
+                ok_sim = False
+            try:
+                fn_lib(pool, ids)
+                ok_lib = True
+            except kda.KdaError as e:
+                assert e.code in (kda.KDA_EREF, kda.KDA_EINVAL)
+                ok_lib = False
+            assert ok_lib == ok_sim, (op, ids)
+        assert pool.free_count() == sim.free_count()
+    assert [kda.kda_page_refcount(pool, i) for i in range(N)] == sim.ref
+
+
+def test_allocator_error_codes():
+    pool = kda.Pool(4096, 8)
+    assert list(kda.kda_page_alloc(pool, 3)) == [0, 1, 2]
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_page_alloc(pool, 6)
+    assert e.value.code == kda.KDA_ENOPAGES and pool.free_count() == 5
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_page_decref(pool, [5])
+    assert e.value.code == kda.KDA_EREF
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_page_claim(pool, [1])
+    assert e.value.code == kda.KDA_EREF
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_page_claim(pool, [9])
+    assert e.value.code == kda.KDA_EINVAL
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_page_claim(pool, [4, 4])
+    assert e.value.code == kda.KDA_EREF
+    assert kda.kda_page_refcount(pool, 4) == 0
+
+
+@pytest.mark.parametrize("stride,last", [(1, False), (4, True), (2, False)])
+def test_plan_matches_oracle(stride, last):
+    rng = np.random.default_rng(13 + stride)
+    H, d, dt, PB = 4, 64, "bf16", 8192
+    P = policy.object_pages(H, d, dt, PB)
+    pool = kda.Pool(PB, 4000)
+    sim = policy.PoolSim(4000)
+    lens = [int(x) for x in rng.integers(0, 5000, 6)]
+    starts = [int(512 * x) for x in rng.integers(0, 8, 6)]
+    act = kda.kda_page_alloc(pool, 6 * P)
+    assert list(act) == sim.alloc(6 * P)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    seq, pos, pages = kda.kda_ckpt_plan(pool, H, d, kda.DTYPES[dt], cu, starts, 512, stride, last)
+    want = policy.plan_checkpoints(sim, [(s, s + L) for s, L in zip(starts, lens)], P, 512, stride, last)
+    assert [(int(a), int(b)) for a, b in zip(seq, pos)] == [(s, p) for s, p, _ in want]
+    assert [list(map(int, row)) for row in pages] == [pg for _, _, pg in want]
+    assert pool.free_count() == sim.free_count()
+
+
+def test_plan_all_or_nothing():
+    pool = kda.Pool(65536, 10)
+    P = pool.object_pages(16, 128, kda.KDA_BF16)   # 17 pages: cannot fit
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_ckpt_plan(pool, 16, 128, kda.KDA_BF16, [0, 4096], [0], 512, 4, True)
+    assert e.value.code == kda.KDA_ENOPAGES and pool.free_count() == 10 and P == 17
+
+
+def test_gpu_calls_reject_bad_arguments_before_touching_the_device():
+    """Host validation returns KDA_EINVAL without any CUDA call (safe on a CPU machine)."""
+    L = kda.lib()
+    pool = kda.Pool(65536, 64)
+    fake = ctypes.c_void_p(256)
+    cu = np.array([0, 10], dtype=np.int32)
+    sp = np.array([0], dtype=np.int64)
+    hi = np.array([0], dtype=np.uint8)
+    act = np.arange(2, dtype=np.int32)
+    args = [pool.handle, 2, 64, kda.KDA_F32, 1, kda._ptr(cu), kda._ptr(sp), kda._ptr(hi),
+            fake, fake, fake, fake, fake, fake, fake, fake, kda._ptr(act), 0, None, None, None,
+            fake, 1 << 20, fake, None]
+    # active pages are not allocated -> reference error
+    assert L.kda_prefill_varlen(*args) == kda.KDA_EINVAL or L.kda_prefill_varlen(*args) == kda.KDA_EREF
+    bad = list(args)
+    bad[2] = 96                     # d not supported
+    assert L.kda_prefill_varlen(*bad) == kda.KDA_EINVAL
+    bad = list(args)
+    bad[4] = 0                      # no sequences
+    assert L.kda_prefill_varlen(*bad) == kda.KDA_EINVAL
+    kda.kda_page_alloc(pool, 1)
+    ok = list(args)
+    ok[16] = kda._ptr(np.array([0], dtype=np.int32))
+    ok[22] = 16                     # workspace too small
+    assert L.kda_prefill_varlen(*ok) == kda.KDA_EINVAL
+    # checkpoint position not on a chunk boundary
+    ck = list(ok)
+    ck[22] = 1 << 20
+    kda.kda_page_alloc(pool, 1)
+    ck[17] = 1
+    ck[18] = kda._ptr(np.array([0], dtype=np.int32))
+    ck[19] = kda._ptr(np.array([5], dtype=np.int64))
+    ck[20] = kda._ptr(np.array([1], dtype=np.int32))
+    assert L.kda_prefill_varlen(*ck) == kda.KDA_EINVAL
+    # a shared (refcount 2) page may not be written
+    kda.kda_page_incref(pool, [0])
+    assert L.kda_prefill_varlen(*ok[:22], 1 << 20, *ok[23:]) == kda.KDA_EREF
+    assert L.kda_decode_step(pool.handle, 2, 80, 0, 4, *([fake] * 10), None) == kda.KDA_EINVAL
+    assert L.kda_ckpt_write(pool.handle, 2, 64, 0, 1, None, None, fake, fake, 0, fake, None) == kda.KDA_EINVAL
