@@ -19,7 +19,8 @@ SO = os.path.join(BUILD, "libkda.so")
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-CU_SOURCES = ["kernels/ckpt_copy.cu", "kernels/decode.cu", "kernels/prefill_simt.cu"]
+CU_SOURCES = ["kernels/ckpt_copy.cu", "kernels/decode.cu", "kernels/prefill_simt.cu",
+              "kernels/tc_selftest.cu"]
 CPP_SOURCES = ["host/pool.cpp", "host/api.cpp"]
 
 

@@ -3,7 +3,6 @@
 // when a pinned staging slot is still in use by an earlier copy.
 #include <algorithm>
 #include <cstring>
-#include <unordered_set>
 #include <vector>
 
 #include "kda.h"
@@ -34,12 +33,14 @@ kda::PoolView pool_view(const kda_pool *p, void *base, int32_t H, int32_t d, int
 }
 
 // Pages written by a call must be private to it: allocated, refcount exactly 1, and not
-// repeated (a checkpoint visible to others is never written in place).
-int check_private(const kda_pool *p, const int32_t *ids, int64_t n, std::unordered_set<int32_t> &seen) {
+// repeated (a checkpoint visible to others is never written in place).  `g` is the
+// duplicate-check generation of this call (kda::pool_new_stamp).
+int check_private(kda_pool *p, const int32_t *ids, int64_t n, uint32_t g) {
     for (int64_t i = 0; i < n; ++i) {
         const int32_t id = ids[i];
         if (id < 0 || id >= p->num_pages) return KDA_EINVAL;
-        if (p->ref[id] != 1 || !seen.insert(id).second) return KDA_EREF;
+        if (p->ref[id] != 1 || p->stamp[id] == g) return KDA_EREF;
+        p->stamp[id] = g;
     }
     return KDA_OK;
 }
@@ -142,7 +143,7 @@ int kda_ckpt_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n
     if ((int64_t)items.size() > cap) return KDA_EINVAL;
     if (!items.empty() && (!out_seq || !out_pos || !out_pages)) return KDA_EINVAL;
     std::lock_guard<std::mutex> g(pool->mu);
-    if ((int64_t)pool->free_ids.size() < (int64_t)items.size() * P) return KDA_ENOPAGES;
+    if ((int64_t)pool->free_n < (int64_t)items.size() * P) return KDA_ENOPAGES;
     for (size_t i = 0; i < items.size(); ++i) {
         out_seq[i] = items[i].first;
         out_pos[i] = items[i].second;
@@ -184,10 +185,10 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
     std::vector<int32_t> pages((size_t)(nseq + n_ckpt) * P);
     {
         std::lock_guard<std::mutex> g(pool->mu);
-        std::unordered_set<int32_t> seen;
-        int rc = check_private(pool, active_pages, (int64_t)nseq * P, seen);
+        const uint32_t gen = kda::pool_new_stamp(pool);
+        int rc = check_private(pool, active_pages, (int64_t)nseq * P, gen);
         if (rc != KDA_OK) return rc;
-        rc = check_private(pool, ckpt_pages, (int64_t)n_ckpt * P, seen);
+        rc = check_private(pool, ckpt_pages, (int64_t)n_ckpt * P, gen);
         if (rc != KDA_OK) return rc;
     }
     std::memcpy(pages.data(), active_pages, (size_t)nseq * P * 4);
@@ -295,11 +296,11 @@ int kda_ckpt_restore(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_
     std::lock_guard<std::mutex> g(pool->mu);
     int rc = check_allocated(pool, ckpt_pages, (int64_t)n * P);
     if (rc != KDA_OK) return rc;
-    std::unordered_set<int32_t> seen;
-    rc = check_private(pool, active_pages, (int64_t)n * P, seen);
+    const uint32_t gen = kda::pool_new_stamp(pool);
+    rc = check_private(pool, active_pages, (int64_t)n * P, gen);
     if (rc != KDA_OK) return rc;
     for (int64_t i = 0; i < (int64_t)n * P; ++i)
-        if (seen.count(ckpt_pages[i])) return KDA_EREF;   // never copy onto the source
+        if (pool->stamp[ckpt_pages[i]] == gen) return KDA_EREF;   // never copy onto the source
     rc = kda::pool_incref(pool, n * P, ckpt_pages);
     if (rc != KDA_OK) return rc;
     rc = copy_objects(pool, H, d, dtype, n, ckpt_pages, active_pages, pool_base, workspace, ws_bytes,

@@ -4,7 +4,6 @@
 
 #include <cstdint>
 #include <mutex>
-#include <set>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -13,7 +12,11 @@ struct kda_pool {
     int64_t page_bytes = 0;
     int32_t num_pages = 0;
     std::vector<int32_t> ref;        // reference count per page (0 = free)
-    std::set<int32_t> free_ids;      // ordered: begin() is the lowest free id
+    std::vector<uint64_t> free_bits; // bit i set <=> page i free
+    int32_t free_n = 0;
+    int32_t low_word = 0;            // no free page below word low_word
+    std::vector<uint32_t> stamp;     // per-page marks for duplicate checks within one call
+    uint32_t stamp_gen = 0;
 
     // Pinned host staging slots, reused round-robin; each slot's event marks the end of the
     // last host-to-device copy that read it.
@@ -30,6 +33,11 @@ struct kda_pool {
 };
 
 namespace kda {
+
+void pool_mark_free(kda_pool *p, int32_t id);
+void pool_mark_used(kda_pool *p, int32_t id);
+// Start a new duplicate-check generation; returns the mark value for this call.
+uint32_t pool_new_stamp(kda_pool *p);
 
 // Allocator primitives (caller holds pool->mu).  All return a kda_status.
 int pool_alloc(kda_pool *p, int32_t n, int32_t *out);

@@ -9,17 +9,18 @@
 // (PagedAttention: logical blocks mapped to physical pages through a table).
 //
 // The kernel is HBM-bound (about 0.84 flop per byte): each CTA streams one 64 KiB fp32
-// state (d = 128) in and out once.  Warp w owns D/8 consecutive rows of S; lane l owns
+// state (d = 128) in and out once.  Warp w of 16 owns D/16 consecutive rows of S; lane l owns
 // D/32 consecutive columns, so every row is one coalesced 512-byte (d = 128) access made
 // of 128-bit loads, the state stays in registers between the two passes, the row
 // reductions for S'^T k and S^T q are thread-local and one shared-memory pass combines
-// the eight warps.
+// the sixteen warps.  Sixteen warps per CTA and two CTAs per SM keep 64 KiB of state loads
+// in flight per CTA while the other CTA computes.
 #include "common.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kDecThreads = 256;
+constexpr int kDecThreads = 512;
 constexpr int kDecWarps = kDecThreads / 32;
 
 template <int VEC> struct VecT;

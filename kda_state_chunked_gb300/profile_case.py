@@ -1,0 +1,96 @@
+"""Run one kernel of the library on a named workload a few times (for ncu captures).
+
+python -m kda_state_chunked_gb300.profile_case prefill-batched --launches 2
+python -m kda_state_chunked_gb300.profile_case decode --launches 3
+python -m kda_state_chunked_gb300.profile_case ckpt-restore --launches 2
+python -m kda_state_chunked_gb300.profile_case prefill-long-slice --launches 1
+
+Cases
+  prefill-batched     4 x 8192 tokens, H = 16, d = 128, bf16, checkpoints every 2048
+  prefill-long-slice  one 65536-token slice of the long workload (H = 32), same layout
+  decode              256 requests x 32 heads, 256 KiB pages, permuted page table
+  ckpt-restore        256 objects x 32 heads copied checkpoint -> private, 64 KiB pages
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+import kda_state_chunked_gb300 as kda
+from kda_state_chunked_gb300 import workloads
+
+
+def prefill(T_seq, nseq, H, seed, launches, dev):
+    d, dt = 128, kda.KDA_BF16
+    toks = workloads.make_tokens(nseq * T_seq, H, d, "bf16", seed, dev)
+    pool = kda.Pool(65536, 64 + (nseq * (T_seq // 2048 + 1) + nseq) * 34, dev)
+    P = pool.object_pages(H, d, dt)
+    act = kda.kda_page_alloc(pool, nseq * P).reshape(nseq, P)
+    cu = [i * T_seq for i in range(nseq + 1)]
+    o = torch.empty_like(toks["q"])
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(launches):
+        seq, pos, pages = kda.kda_ckpt_plan(pool, H, d, dt, cu, [0] * nseq, 512, 4, True)
+        ws = torch.empty(kda.kda_prefill_workspace_bytes(nseq, len(seq), P), dtype=torch.uint8, device=dev)
+        kda.kda_prefill_varlen(pool, cu, [0] * nseq, [0] * nseq, toks["q"], toks["k"], toks["v"],
+                               toks["alpha"], toks["beta"], toks["conv_w"], o, act, seq, pos, pages, ws, st)
+        torch.cuda.synchronize()
+        kda.kda_page_decref(pool, pages.reshape(-1))
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+
+
+def decode(launches, dev):
+    w = workloads.WORKLOADS["decode"]
+    dt = kda.DTYPES[w.dtype]
+    pool = kda.Pool(w.page_bytes, 4096, dev)
+    P = pool.object_pages(w.H, w.d, dt)
+    table = workloads.permuted_page_table(4096, w.nseq, P, w.seed)
+    kda.kda_page_claim(pool, table.reshape(-1))
+    conv_w = workloads.make_tokens(1, w.H, w.d, w.dtype, w.seed, dev)["conv_w"]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    td = table.to(dev)
+    for s in range(launches):
+        t = workloads.decode_step_tokens(w.nseq, w.H, w.d, w.dtype, w.seed, s, dev)
+        o = torch.empty_like(t["q"])
+        kda.kda_decode_step(pool, t["q"], t["k"], t["v"], t["alpha"], t["beta"], conv_w, o, td, st)
+    torch.cuda.synchronize()
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+
+
+def ckpt_restore(launches, dev, n=256):
+    H, d, dt = 32, 128, kda.KDA_BF16
+    pool = kda.Pool(65536, 2 * n * 34 + 64, dev)
+    P = pool.object_pages(H, d, dt)
+    src = kda.kda_page_alloc(pool, n * P)
+    act = kda.kda_page_alloc(pool, n * P)
+    ws = torch.empty(kda.kda_copy_workspace_bytes(n, P), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(launches):
+        kda.kda_ckpt_restore(pool, H, d, dt, src, act, ws, st)
+        torch.cuda.synchronize()
+        kda.kda_ckpt_release(pool, src, P)
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["prefill-batched", "prefill-long-slice", "decode", "ckpt-restore"])
+    ap.add_argument("--launches", type=int, default=2)
+    a = ap.parse_args()
+    from kda_state_chunked_gb300.build import build
+    build()
+    dev = "cuda:0"
+    if a.case == "prefill-batched":
+        prefill(8192, 4, 16, 1, a.launches, dev)
+    elif a.case == "prefill-long-slice":
+        prefill(65536, 1, 32, 4, a.launches, dev)
+    elif a.case == "decode":
+        decode(a.launches, dev)
+    else:
+        ckpt_restore(a.launches, dev)
+    print("ok")
+
+
+if __name__ == "__main__":
+    main()
