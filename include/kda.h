@@ -178,6 +178,37 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
                        const int32_t *ckpt_pages, void *workspace, int64_t ws_bytes,
                        int32_t *status_dev, void *stream);
 
+/* Bytes of the fixed device scratch used by kda_prefill_varlen_noalloc. */
+#define KDA_NOALLOC_SCRATCH_BYTES (1 << 20)
+
+/* Allocation-free variant of kda_prefill_varlen.  The source pages have no counterpart:
+ * this is an interface convenience of this library.  It serves callers that cannot
+ * allocate device memory when they call the prefill: a serving runtime that reserved all
+ * of HBM for its own pool at start-up (a cudaMalloc there fails or fragments that pool),
+ * or a latency-critical path where cudaMalloc / cudaFree and the device synchronisation
+ * they can cause are not allowed.  Arguments and results are those of kda_prefill_varlen
+ * without the workspace: the per-call metadata goes to a fixed array of
+ * KDA_NOALLOC_SCRATCH_BYTES bytes inside the library's device image, which every GPU that
+ * loads the library holds until the process exits.
+ *   - Metadata that does not fit (32 bytes per sequence and 16 per checkpoint, each part
+ *     rounded up to 256 bytes, plus 4 * (nseq + n_ckpt) * pages_per_object bytes of page
+ *     lists) returns KDA_EINVAL and enqueues nothing.
+ *   - The first call on each device looks up the array's device address, with that device
+ *     current; make that first call before any stream capture.
+ *   - Every call reuses the one array and overwrites all of the metadata it reads, so no
+ *     state carries over between calls; calls whose GPU work may overlap (different streams
+ *     without ordering between them) race on it.  Calls on one stream are ordered.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine: the metadata is built
+ *     in a static host buffer and sent with one pageable cudaMemcpyAsync. */
+int kda_prefill_varlen_noalloc(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t nseq,
+                               const int32_t *cu_seqlens, const int64_t *start_pos,
+                               const uint8_t *has_init, const void *q, const void *k,
+                               const void *v, const void *alpha, const void *beta,
+                               const float *conv_w, void *o, void *pool_base,
+                               const int32_t *active_pages, int32_t n_ckpt,
+                               const int32_t *ckpt_seq, const int64_t *ckpt_pos,
+                               const int32_t *ckpt_pages, int32_t *status_dev, void *stream);
+
 /* ---------------------------------------------------------------- decode -------------- */
 
 /* One decode step for B requests, one token each.  q, k, v, alpha device [B][H][d] dtype,

@@ -50,6 +50,8 @@ _SIGS = {
     "kda_prefill_workspace_bytes": (_I64, [_I32, _I32, _I32]),
     "kda_prefill_varlen": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                           _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _I64, _P, _P]),
+    "kda_prefill_varlen_noalloc": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
+                                                  _P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P]),
     "kda_decode_step": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                        _P, _P, _P, _P]),
     "kda_copy_workspace_bytes": (_I64, [_I32, _I32]),
@@ -267,6 +269,32 @@ def kda_prefill_varlen(pool: Pool, cu_seqlens, start_pos, has_init, q, k, v, alp
         _dev(workspace), workspace.numel() * workspace.element_size(), _dev(status),
         _stream(stream))
     _check(rc, "kda_prefill_varlen")
+
+
+KDA_NOALLOC_SCRATCH_BYTES = 1 << 20
+
+
+def kda_prefill_varlen_noalloc(pool: Pool, cu_seqlens, start_pos, has_init, q, k, v, alpha, beta,
+                               conv_w, o, active_pages, ckpt_seq=(), ckpt_pos=(), ckpt_pages=None,
+                               status=None, stream=None) -> None:
+    """kda_prefill_varlen without a workspace, for callers that cannot allocate device memory
+    at call time: the per-call metadata lives in a fixed 1 MiB array inside the library
+    (see include/kda.h for the limit and the rules on concurrent calls)."""
+    T_tot, H, d = q.shape
+    cu = _i32(cu_seqlens)
+    sp = _i64(start_pos)
+    hi = np.ascontiguousarray(np.asarray(has_init, dtype=np.uint8).reshape(-1))
+    act = _i32(active_pages)
+    cs = _i32(ckpt_seq)
+    cp = _i64(ckpt_pos)
+    n_ck = len(cs)
+    cpg = _i32(ckpt_pages if ckpt_pages is not None else np.zeros(0, np.int32))
+    rc = lib().kda_prefill_varlen_noalloc(
+        pool.handle, H, d, dtype_of(q), len(cu) - 1, _ptr(cu), _ptr(sp), _ptr(hi), _dev(q), _dev(k),
+        _dev(v), _dev(alpha), _dev(beta), _dev(conv_w), _dev(o), _dev(pool.base), _ptr(act), n_ck,
+        _ptr(cs) if n_ck else None, _ptr(cp) if n_ck else None, _ptr(cpg) if n_ck else None,
+        _dev(status), _stream(stream))
+    _check(rc, "kda_prefill_varlen_noalloc")
 
 
 # ------------------------------------------------------------------------------ decode
