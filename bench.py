@@ -342,7 +342,7 @@ def run_ours(args, rank, world, dev):
             "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
             "kernel": "prefill", "algorithmic_bytes_per_launch": ab,
             "launch_ms": launch_ms,
-            "traffic": _traffic("prefill_batched", ["kernels/prefill_simt.cu"], 1.0),
+            "traffic": _traffic("prefill_batched", ["kernels/prefill_tc.cu"], 1.0),
             "tensor": {"flops_per_launch": bench.algorithmic_flops(),
                        "achieved_tflops": bench.algorithmic_flops() / (launch_ms * 1e-3) / 1e12,
                        "peak_tflops": peaks["bf16_tflops"]}}

@@ -69,6 +69,7 @@ typedef enum kda_dtype { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 /* Device status bits set by kernels (reported through kda_sync_status). */
 #define KDA_DEV_BAD_PAGE 1   /* a page id outside [0, num_pages) was met; access skipped */
 #define KDA_DEV_BAD_META 2   /* inconsistent metadata in the workspace; work skipped */
+#define KDA_DEV_TIMEOUT 4    /* an internal pipeline wait gave up; that sequence is incomplete */
 
 typedef struct kda_pool kda_pool;
 

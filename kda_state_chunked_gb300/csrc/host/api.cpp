@@ -231,6 +231,7 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
 
     kda::PrefillArgs a;
     a.H = H; a.d = d; a.dtype = dtype; a.nseq = nseq;
+    a.T_tot = T_tot;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.conv_w = conv_w; a.o = o;
     a.pool = pool_view(pool, pool_base, H, d, dtype);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -238,7 +239,7 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
     a.ckpts = reinterpret_cast<const CkptMeta *>(ws + o_ck);
     a.pages = reinterpret_cast<const int32_t *>(ws + o_pg);
     a.status = status_dev;
-    return kda::launch_prefill_simt(a, st) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+    return kda::launch_prefill(a, st) == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
 int kda_decode_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B,

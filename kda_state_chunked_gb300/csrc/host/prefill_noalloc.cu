@@ -130,6 +130,7 @@ extern "C" int kda_prefill_varlen_noalloc(kda_pool *pool, int32_t H, int32_t d, 
 
     kda::PrefillArgs a;
     a.H = H; a.d = d; a.dtype = dtype; a.nseq = nseq;
+    a.T_tot = T_tot;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.conv_w = conv_w; a.o = o;
     a.pool.base = static_cast<uint8_t *>(pool_base);
     a.pool.page_bytes = pool->page_bytes;
@@ -141,5 +142,5 @@ extern "C" int kda_prefill_varlen_noalloc(kda_pool *pool, int32_t H, int32_t d, 
     a.ckpts = reinterpret_cast<const CkptMeta *>(ws + o_ck);
     a.pages = reinterpret_cast<const int32_t *>(ws + o_pg);
     a.status = status_dev;
-    return kda::launch_prefill_simt(a, st) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+    return kda::launch_prefill(a, st) == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }

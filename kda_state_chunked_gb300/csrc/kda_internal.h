@@ -44,6 +44,7 @@ struct PoolView {
 
 struct PrefillArgs {
     int32_t H, d, dtype, nseq;
+    int64_t T_tot;                // rows of the packed token arrays
     const void *q, *k, *v, *alpha, *beta;
     const float *conv_w;
     void *o;
@@ -75,6 +76,13 @@ struct CopyArgs {
 
 // Kernel launchers (defined in the .cu files).
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
+bool prefill_tc_supported(const PrefillArgs &a);
+// Prefill dispatch: the tensor-core kernel for bf16 with d = 128, the fp32 CUDA-core kernel
+// otherwise (fp32 inputs need fp32 arithmetic to meet their tolerance).
+inline cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
+    return prefill_tc_supported(a) ? launch_prefill_tc(a, s) : launch_prefill_simt(a, s);
+}
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_copy_objects(const CopyArgs &a, cudaStream_t s);
 

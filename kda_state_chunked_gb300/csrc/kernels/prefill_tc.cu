@@ -1,0 +1,821 @@
+// Chunked varlen KDA prefill on the 5th-generation tensor cores (bf16 inputs, d = 128).
+//
+// What it computes is the token recurrence S_t = (I - beta k k^T) Diag(alpha) S_{t-1} +
+// beta k v^T, o_t = S_t^T q_t with the width-4 causal conv on q | k | v ("Lesson 01 ·
+// Architecture map", §两种 Attention，两种状态), grouped into chunks of 64 tokens that each act
+// on S as one affine map ("KIMI K3 경량 복제에서 본 KDA의 AI 인프라 과제", §0x01 1.3), with
+// checkpoints of (S, conv window) streamed at listed chunk ends and the final state written to
+// the sequence's active object ("Cache de préfixe hybride KDA–MLA", §Le fonctionnement du
+// prefill).
+//
+// Chunk algebra (rows r, s = 0..63 of one chunk, S = state at the chunk start, gamma_r =
+// prod_{u<=r} alpha_u per key channel, gamma_C = gamma_63; padding rows are identity tokens):
+//   Kt' = k gamma_r / gamma_C,  Qt' = q gamma_r / gamma_C,  Kb = k gamma_C / gamma_r
+//   G = Kt' Kb^T = Kt Kh^T,     P = lower_incl(Qt' Kb^T)          (one M = 128 MMA)
+//   T = (I + Diag(beta) strict_lower(G))^{-1} Diag(beta)          (CUDA cores + tf32 mma.sync)
+//   WK'^T = Kt'^T T^T,          U^T = V^T T^T                      (two M = 128 MMAs)
+//   O^T  = (Gamma_C S)^T Qt'^T  + W^T P^T
+//   W^T  = U^T - (Gamma_C S)^T WK'^T
+//   S^T <- (Gamma_C S)^T + W^T Kb
+// The state lives transposed in TMEM (lane = value channel j, column = key channel i), so every
+// state contraction has M = 128; the scaled state (Gamma_C S)^T is also kept as a bf16 operand
+// in shared memory.  Decay is anchored at the chunk end, so no per-element division is needed.
+//
+// Warp roles (12 warps): warp 0 issues TMA loads of the raw q, k, v, alpha tiles; warp 1 issues
+// all tcgen05.mma from one thread; warps 4-7 ("prep") do the conv, the decay scaling and the
+// triangular solve for the chunk ahead; warps 8-11 ("seq") run the state epilogues of the
+// current chunk (checkpoint stores, decay of S, W, outputs).  Every wait is bounded: on a
+// timeout the kernel records KDA_DEV_TIMEOUT, stops issuing work, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace kda {
+
+int encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_rows);
+
+namespace {
+
+constexpr int D = 128;
+constexpr int C = kChunk;            // 64
+constexpr int kThreads = 384;
+constexpr int kPrepWarp0 = 4, kSeqWarp0 = 8;
+constexpr int kBarPrep = 1, kBarSeq = 2;
+
+// Shared-memory map (byte offsets from a 1024-aligned base).
+constexpr uint32_t OFF_KQ = 0;          // [2 slots][2 kb][128 rows: k 0-63 | q 64-127][128 B]
+constexpr uint32_t OFF_KB = 65536;      // [2 slots][2 kb][64 rows][128 B]   Kb
+constexpr uint32_t OFF_V = 98304;       // [2 kb][64 rows][128 B]            raw v -> V
+constexpr uint32_t OFF_AL = 114688;     // [2 kb][64 rows][128 B]            raw alpha
+constexpr uint32_t OFF_P = 131072;      // [2 slots][64 rows][128 B]         P
+constexpr uint32_t OFF_T = 147456;      // [64 rows][128 B]                  T
+constexpr uint32_t OFF_WK = 155648;     // [128 rows][128 B] WK'^T; fp32 64x64 solve scratch
+constexpr uint32_t OFF_SB = 172032;     // [2 kb][128 rows][128 B]           (Gamma S)^T bf16
+constexpr uint32_t OFF_WT = 204800;     // [128 rows][128 B]                 W^T bf16
+constexpr uint32_t OFF_GC = 221184;     // float [2][128]                    gamma_C
+constexpr uint32_t OFF_BS = 222208;     // float [2][64]                     beta
+constexpr uint32_t OFF_RED = 222720;    // float2 [2][64]                    half products of alpha
+constexpr uint32_t OFF_HALO = 223744;   // bf16 [3][384]                     conv window
+constexpr uint32_t OFF_BAR = 226048;    // mbarriers, flags
+constexpr uint32_t OFF_PD = OFF_BAR + 256;   // float [64]  exact diagonal of P
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;   // + alignment slack
+
+// TMEM columns.
+constexpr uint32_t COL_S = 0, COL_O = 128, COL_W = 256, COL_GP = 384, COL_WK = 448;
+
+// mbarrier indices ([2] arrays indexed by local chunk parity).
+enum {
+    B_FULL = 0,      // TMA tiles landed             (tx)
+    B_P1 = 2,        // prep: operands of the chunk written
+    B_GP = 4,        // mma: G|P in TMEM
+    B_T = 6,         // prep: T written
+    B_M2 = 8,        // mma: WK'^T, U^T done
+    B_WK = 10,       // prep: WK'^T operand written
+    B_SB = 12,       // seq: (Gamma S)^T operand written, TMEM S scaled
+    B_W = 14,        // mma: W^T in TMEM (M3 done)
+    B_M3 = 16,       // mma: M3 done (for the solve scratch)
+    B_WT = 18,       // seq: W^T operand written, D_W read
+    B_M4 = 20,       // mma: chunk done (S advanced, O complete)
+    B_DO = 22,       // seq: D_O read
+    NUM_BARS = 24
+};
+
+struct TcParams {
+    PrefillArgs a;
+};
+
+__device__ __forceinline__ uint32_t par(int lc) { return (uint32_t)((lc >> 1) & 1); }
+
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) { return f2_to_bf2(lo, hi); }
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// D = A(16x8, row) * B(8x8, col) + D, tf32 in, fp32 accumulate.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// fp32 64x64 solve scratch, XOR-swizzled so that mma.sync fragment loads avoid conflicts.
+__device__ __forceinline__ int msc_idx(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
+
+// 16x16 block (bi, bj) product accumulate: acc(C-frag, 2 n-tiles) += M[bi,bk] * M[bk,bj].
+__device__ __forceinline__ void blk_mma(float (&acc)[2][4], const float *M, int bi, int bk, int bj, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int kt = 0; kt < 2; ++kt) {
+        uint32_t a[4];
+        const int r0 = bi * 16, c0 = bk * 16 + kt * 8;
+        a[0] = to_tf32(M[msc_idx(r0 + g, c0 + t)]);
+        a[1] = to_tf32(M[msc_idx(r0 + g + 8, c0 + t)]);
+        a[2] = to_tf32(M[msc_idx(r0 + g, c0 + t + 4)]);
+        a[3] = to_tf32(M[msc_idx(r0 + g + 8, c0 + t + 4)]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b[2];
+            const int k0 = bk * 16 + kt * 8, n0 = bj * 16 + nt * 8;
+            b[0] = to_tf32(M[msc_idx(k0 + t, n0 + g)]);
+            b[1] = to_tf32(M[msc_idx(k0 + t + 4, n0 + g)]);
+            mma_tf32(acc[nt], a, b);
+        }
+    }
+}
+
+__device__ __forceinline__ void blk_store(float *M, int bi, int bj, const float (&acc)[2][4], float scale, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int r0 = bi * 16, c0 = bj * 16 + nt * 8 + 2 * t;
+        M[msc_idx(r0 + g, c0)] = scale * acc[nt][0];
+        M[msc_idx(r0 + g, c0 + 1)] = scale * acc[nt][1];
+        M[msc_idx(r0 + g + 8, c0)] = scale * acc[nt][2];
+        M[msc_idx(r0 + g + 8, c0 + 1)] = scale * acc[nt][3];
+    }
+}
+
+struct Shared {
+    uint8_t *base;
+    uint64_t *bar;
+    volatile int *err;
+    uint32_t *tmem;
+};
+
+__device__ __forceinline__ bool wait_bar(const Shared &s, int idx, uint32_t parity) {
+    return ptx::mbar_wait(&s.bar[idx], parity, s.err);
+}
+
+// Warpgroup-uniform wait: thread 0 of the group polls (bounded), a named barrier hands the
+// outcome to all 128 threads, so the whole group continues or stops together.
+__device__ __forceinline__ bool wg_wait(const Shared &s, int idx, uint32_t parity, int wg_tid, int bar_id,
+                                        volatile int *flag) {
+    if (wg_tid == 0) *flag = ptx::mbar_wait(&s.bar[idx], parity, s.err) ? 1 : 0;
+    named_bar(bar_id, 128);
+    const bool ok = *flag != 0;
+    named_bar(bar_id, 128);
+    return ok;
+}
+
+// ------------------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Shared S;
+    S.base = sm;
+    S.bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
+    S.err = reinterpret_cast<volatile int *>(sm + OFF_BAR + NUM_BARS * 8);
+    S.tmem = reinterpret_cast<uint32_t *>(sm + OFF_BAR + NUM_BARS * 8 + 16);
+    volatile int *wg_flag = reinterpret_cast<volatile int *>(sm + OFF_BAR + NUM_BARS * 8 + 32);
+    float *gC = reinterpret_cast<float *>(sm + OFF_GC);
+    float *bs = reinterpret_cast<float *>(sm + OFF_BS);
+    float2 *red = reinterpret_cast<float2 *>(sm + OFF_RED);
+    __nv_bfloat16 *halo = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_HALO);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x % a.H, sq = blockIdx.x / a.H;
+    const SeqMeta m = a.seqs[sq];
+    const int H = a.H;
+    const uint64_t rec = (uint64_t)h * (uint64_t)a.pool.rec_bytes;
+    const int32_t *act_pages = a.pages + m.active_off;
+    const int64_t start = m.start_pos, end = m.start_pos + m.len;
+    const int64_t c_first = start / C;
+    const int nchunks = m.len > 0 ? (int)((end - 1) / C - c_first + 1) : 0;
+
+    if (tid == 0) {
+        for (int i = 0; i < NUM_BARS; ++i) ptx::mbar_init(&S.bar[i], 1);
+        *S.err = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(S.tmem, 512);
+        ptx::tmem_relinquish();
+    }
+    // Initial conv window (raw tokens, bf16) from the active object, or zeros.
+    for (int e = tid; e < 3 * 3 * D; e += kThreads) {
+        __nv_bfloat16 x = __float2bfloat16_rn(0.f);
+        if (m.has_init) {
+            const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(
+                obj_addr(a.pool, act_pages, rec + (uint64_t)D * D * 4 + (uint64_t)e * 2, a.status));
+            if (p) x = *p;
+        }
+        halo[e] = x;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tbase = *S.tmem;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0 && nchunks > 0) {
+            ptx::prefetch_tmap(&tm_q);
+            ptx::prefetch_tmap(&tm_k);
+            ptx::prefetch_tmap(&tm_v);
+            ptx::prefetch_tmap(&tm_a);
+            for (int lc = 0; lc < nchunks && !*S.err; ++lc) {
+                const int b = lc & 1;
+                if (lc >= 1) {
+                    if (!wait_bar(S, B_P1 + ((lc - 1) & 1), par(lc - 1))) break;   // alpha consumed
+                    if (!wait_bar(S, B_M2 + ((lc - 1) & 1), par(lc - 1))) break;   // V consumed
+                }
+                if (lc >= 2 && !wait_bar(S, B_M4 + b, par(lc - 2))) break;         // KQ slot free
+                const int64_t abs0 = (c_first + lc) * C;
+                const int32_t y = (int32_t)((int64_t)m.tok_begin + (abs0 - start));
+                uint64_t *fb = &S.bar[B_FULL + b];
+                ptx::mbar_arrive_expect_tx(fb, 4 * 2 * 64 * 128);
+                uint8_t *kq = sm + OFF_KQ + b * 32768;
+                for (int kb = 0; kb < 2; ++kb) {
+                    const int32_t x = h * D + kb * 64;
+                    ptx::tma_load_2d(kq + kb * 16384, &tm_k, fb, x, y);
+                    ptx::tma_load_2d(kq + kb * 16384 + 8192, &tm_q, fb, x, y);
+                    ptx::tma_load_2d(sm + OFF_V + kb * 8192, &tm_v, fb, x, y);
+                    ptx::tma_load_2d(sm + OFF_AL + kb * 8192, &tm_a, fb, x, y);
+                }
+            }
+            // Do not leave while copies may still be landing in shared memory.
+            if (*S.err)
+                for (int lc = 0; lc < nchunks; ++lc) {
+                    uint32_t n = 0;
+                    while (!ptx::mbar_try_wait(&S.bar[B_FULL + (lc & 1)], par(lc)) && n < ptx::kSpinLimit) ++n;
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0 && nchunks > 0) {
+            const uint32_t id_gp = ptx::idesc_bf16(128, 64, 0, 0);
+            const uint32_t id_m2 = ptx::idesc_bf16(128, 64, 1, 0);
+            const uint32_t id_o = ptx::idesc_bf16(128, 64, 0, 0);
+            const uint32_t id_w = ptx::idesc_bf16(128, 64, 0, 1, 1);
+            const uint32_t id_s = ptx::idesc_bf16(128, 128, 0, 1);
+            const uint32_t id_op = ptx::idesc_bf16(128, 64, 0, 0);
+            const uint32_t sbase = ptx::smem_u32(sm);
+            int n1 = 0, n2 = 0, n3 = 0, n4 = 0;
+            uint32_t spins = 0;
+            while (n4 < nchunks && !*S.err) {
+                bool did = false;
+                // M3: O^T = SB Qt'^T ; W^T += -SB WK'^T
+                if (n3 == n4 && n3 < nchunks) {
+                    const int b = n3 & 1;
+                    if (ptx::mbar_try_wait(&S.bar[B_SB + b], par(n3)) &&
+                        ptx::mbar_try_wait(&S.bar[B_WK + b], par(n3)) &&
+                        (n3 < 2 || ptx::mbar_try_wait(&S.bar[B_DO + b], par(n3 - 2)))) {
+                        ptx::tc_fence_after();
+                        const uint32_t sb = sbase + OFF_SB, kq = sbase + OFF_KQ + b * 32768, wk = sbase + OFF_WK;
+                        for (int s = 0; s < 8; ++s) {
+                            const uint64_t ad = ptx::sdesc_sw128(sb + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+                            const uint64_t bq = ptx::sdesc_sw128(kq + 8192 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+                            ptx::mma_bf16(tbase + COL_O + b * 64, ad, bq, id_o, s > 0 ? 1u : 0u);
+                        }
+                        for (int s = 0; s < 8; ++s) {
+                            const uint64_t ad = ptx::sdesc_sw128(sb + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+                            const uint64_t bw = ptx::sdesc_sw128(wk + s * 2048, 8192, 1024);
+                            ptx::mma_bf16(tbase + COL_W + b * 64, ad, bw, id_w, 1u);
+                        }
+                        ptx::mma_commit(&S.bar[B_W + b]);
+                        ptx::mma_commit(&S.bar[B_M3 + b]);
+                        ++n3;
+                        did = true;
+                    }
+                }
+                // M4: S^T += W^T Kb ; O^T += W^T P^T
+                if (n4 < n3) {
+                    const int b = n4 & 1;
+                    if (ptx::mbar_try_wait(&S.bar[B_WT + b], par(n4))) {
+                        ptx::tc_fence_after();
+                        const uint32_t wt = sbase + OFF_WT, kb = sbase + OFF_KB + b * 16384, pb = sbase + OFF_P + b * 8192;
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
+                            const uint64_t bd = ptx::sdesc_sw128(kb + s * 2048, 8192, 1024);
+                            ptx::mma_bf16(tbase + COL_S, ad, bd, id_s, 1u);
+                        }
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
+                            const uint64_t bd = ptx::sdesc_sw128(pb + s * 32, 16, 1024);
+                            ptx::mma_bf16(tbase + COL_O + b * 64, ad, bd, id_op, 1u);
+                        }
+                        ptx::mma_commit(&S.bar[B_M4 + b]);
+                        ++n4;
+                        did = true;
+                    }
+                }
+                // M1: [Kt'; Qt'] Kb^T -> G | P
+                if (n1 < nchunks) {
+                    const int b = n1 & 1;
+                    if (ptx::mbar_try_wait(&S.bar[B_P1 + b], par(n1))) {
+                        ptx::tc_fence_after();
+                        const uint32_t kq = sbase + OFF_KQ + b * 32768, kb = sbase + OFF_KB + b * 16384;
+                        for (int s = 0; s < 8; ++s) {
+                            const uint64_t ad = ptx::sdesc_sw128(kq + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+                            const uint64_t bd = ptx::sdesc_sw128(kb + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024);
+                            ptx::mma_bf16(tbase + COL_GP, ad, bd, id_gp, s > 0 ? 1u : 0u);
+                        }
+                        ptx::mma_commit(&S.bar[B_GP + b]);
+                        ++n1;
+                        did = true;
+                    }
+                }
+                // M2: WK'^T = Kt'^T T^T ; U^T = V^T T^T
+                if (n2 < n1) {
+                    const int b = n2 & 1;
+                    if (ptx::mbar_try_wait(&S.bar[B_T + b], par(n2)) &&
+                        (n2 < 2 || ptx::mbar_try_wait(&S.bar[B_WT + b], par(n2 - 2)))) {
+                        ptx::tc_fence_after();
+                        const uint32_t kq = sbase + OFF_KQ + b * 32768, v = sbase + OFF_V, t = sbase + OFF_T;
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t bd = ptx::sdesc_sw128(t + s * 32, 16, 1024);
+                            ptx::mma_bf16(tbase + COL_WK, ptx::sdesc_sw128(kq + s * 2048, 16384, 1024), bd, id_m2,
+                                          s > 0 ? 1u : 0u);
+                            ptx::mma_bf16(tbase + COL_W + b * 64, ptx::sdesc_sw128(v + s * 2048, 8192, 1024), bd,
+                                          id_m2, s > 0 ? 1u : 0u);
+                        }
+                        ptx::mma_commit(&S.bar[B_M2 + b]);
+                        ++n2;
+                        did = true;
+                    }
+                }
+                if (did) spins = 0;
+                else if (++spins > ptx::kSpinLimit) *S.err = 1;
+            }
+        }
+    } else if (warp >= kPrepWarp0 && warp < kSeqWarp0) {
+        // ------------------------------------------------------------------ prep warpgroup
+        const int t = tid - kPrepWarp0 * 32;          // 0..127, TMEM lane
+        const int p = t & 63, hf = t >> 6;            // channel pair (2p, 2p+1), row half
+        const int c0 = 2 * p, kb = c0 >> 6, cb = (c0 & 63) * 2;   // tile block and column byte
+        float wq[2][4], wk[2][4], wv[2][4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                wq[e][j] = a.conv_w[((int64_t)h * 3 * D + c0 + e) * 4 + j];
+                wk[e][j] = a.conv_w[((int64_t)h * 3 * D + D + c0 + e) * 4 + j];
+                wv[e][j] = a.conv_w[((int64_t)h * 3 * D + 2 * D + c0 + e) * 4 + j];
+            }
+        const __nv_bfloat16 *betag = static_cast<const __nv_bfloat16 *>(a.beta);
+        float *Msc = reinterpret_cast<float *>(sm + OFF_WK);
+        int nck = 0;   // next checkpoint index of this sequence (window part)
+        volatile int *pflag = wg_flag;
+        for (int lc = 0; lc < nchunks; ++lc) {
+            const int b = lc & 1;
+            const int64_t abs0 = (c_first + lc) * C;
+            const int r_first = start > abs0 ? (int)(start - abs0) : 0;
+            const int r_end = end - abs0 < C ? (int)(end - abs0) : C;
+            const int64_t row0 = (int64_t)m.tok_begin + (abs0 - start);
+            // ---------------- P1: conv, decay, scaled operands
+            if (!wg_wait(S, B_FULL + b, par(lc), t, kBarPrep, pflag)) break;
+            if (lc >= 2 && !wg_wait(S, B_M4 + b, par(lc - 2), t, kBarPrep, pflag)) break;   // Kb / P slot free
+            uint8_t *kq = sm + OFF_KQ + b * 32768;
+            uint8_t *kbt = sm + OFF_KB + b * 16384;
+            // window carried in from the previous chunk (halo), for both halves
+            float2 wqv[3], wkv[3], wvv[3];
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+                wqv[u] = make_float2(__bfloat162float(halo[u * 384 + c0]), __bfloat162float(halo[u * 384 + c0 + 1]));
+                wkv[u] = make_float2(__bfloat162float(halo[u * 384 + D + c0]), __bfloat162float(halo[u * 384 + D + c0 + 1]));
+                wvv[u] = make_float2(__bfloat162float(halo[u * 384 + 2 * D + c0]),
+                                     __bfloat162float(halo[u * 384 + 2 * D + c0 + 1]));
+            }
+            // the second half starts after the last (up to three) valid rows below row 32:
+            // shift those raw rows into its window
+            if (hf == 1) {
+                const int hi = r_end < 32 ? r_end : 32;
+                const int lo = (hi - 3) > r_first ? (hi - 3) : r_first;
+                for (int r = lo; r < hi; ++r) {
+                    const uint32_t off = kb * 16384 + ptx::sw128_off(r, cb);
+                    const float2 xq = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + off + 8192));
+                    const float2 xk = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + off));
+                    const float2 xv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_V + kb * 8192 + ptx::sw128_off(r, cb)));
+                    wqv[0] = wqv[1]; wqv[1] = wqv[2]; wqv[2] = xq;
+                    wkv[0] = wkv[1]; wkv[1] = wkv[2]; wkv[2] = xk;
+                    wvv[0] = wvv[1]; wvv[1] = wvv[2]; wvv[2] = xv;
+                }
+            }
+            // alpha product over this half's rows
+            float2 ap = make_float2(1.f, 1.f);
+            for (int r = hf * 32; r < hf * 32 + 32; ++r) {
+                if (r < r_first || r >= r_end) continue;
+                const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_AL + kb * 8192 + ptx::sw128_off(r, cb)));
+                ap.x *= al.x;
+                ap.y *= al.y;
+            }
+            red[hf * 64 + p] = ap;
+            if (t < C) bs[b * 64 + t] = (t >= r_first && t < r_end) ? __bfloat162float(betag[(row0 + t) * H + h]) : 0.f;
+            named_bar(kBarPrep, 128);
+            const float2 h0 = red[p], h1 = red[64 + p];
+            const float gCx = h0.x * h1.x, gCy = h0.y * h1.y;
+            const float icx = 1.f / gCx, icy = 1.f / gCy;
+            if (hf == 0) {
+                gC[b * 128 + c0] = gCx;
+                gC[b * 128 + c0 + 1] = gCy;
+            }
+            float gx = hf ? h0.x : 1.f, gy = hf ? h0.y : 1.f;
+            for (int r = hf * 32; r < hf * 32 + 32; ++r) {
+                const uint32_t offk = kb * 16384 + ptx::sw128_off(r, cb);
+                const uint32_t offv = kb * 8192 + ptx::sw128_off(r, cb);
+                uint32_t oq = 0, ok = 0, okb = 0, ov = 0;
+                if (r >= r_first && r < r_end) {
+                    const float2 xq = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + offk + 8192));
+                    const float2 xk = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + offk));
+                    const float2 xv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_V + offv));
+                    const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_AL + offv));
+                    float qb0 = wq[0][0] * wqv[0].x + wq[0][1] * wqv[1].x + wq[0][2] * wqv[2].x + wq[0][3] * xq.x;
+                    float qb1 = wq[1][0] * wqv[0].y + wq[1][1] * wqv[1].y + wq[1][2] * wqv[2].y + wq[1][3] * xq.y;
+                    float kb0 = wk[0][0] * wkv[0].x + wk[0][1] * wkv[1].x + wk[0][2] * wkv[2].x + wk[0][3] * xk.x;
+                    float kb1 = wk[1][0] * wkv[0].y + wk[1][1] * wkv[1].y + wk[1][2] * wkv[2].y + wk[1][3] * xk.y;
+                    float vb0 = wv[0][0] * wvv[0].x + wv[0][1] * wvv[1].x + wv[0][2] * wvv[2].x + wv[0][3] * xv.x;
+                    float vb1 = wv[1][0] * wvv[0].y + wv[1][1] * wvv[1].y + wv[1][2] * wvv[2].y + wv[1][3] * xv.y;
+                    wqv[0] = wqv[1]; wqv[1] = wqv[2]; wqv[2] = xq;
+                    wkv[0] = wkv[1]; wkv[1] = wkv[2]; wkv[2] = xk;
+                    wvv[0] = wvv[1]; wvv[1] = wvv[2]; wvv[2] = xv;
+                    gx *= al.x;
+                    gy *= al.y;
+                    // this pair's share of the diagonal P[r][r] = qbar_r . kbar_r (the decay
+                    // cancels), kept in fp32 in the alpha slot just read
+                    *reinterpret_cast<float *>(sm + OFF_AL + offv) = qb0 * kb0 + qb1 * kb1;
+                    const float sx = gx * icx, sy = gy * icy;      // gamma_r / gamma_C
+                    oq = pack_bf16x2(qb0 * sx, qb1 * sy);
+                    ok = pack_bf16x2(kb0 * sx, kb1 * sy);
+                    okb = pack_bf16x2(kb0 * rcp_approx(sx), kb1 * rcp_approx(sy));
+                    ov = pack_bf16x2(vb0, vb1);
+                }
+                else {
+                    *reinterpret_cast<float *>(sm + OFF_AL + offv) = 0.f;
+                }
+                *reinterpret_cast<uint32_t *>(kq + offk + 8192) = oq;
+                *reinterpret_cast<uint32_t *>(kq + offk) = ok;
+                *reinterpret_cast<uint32_t *>(kbt + offv) = okb;
+                *reinterpret_cast<uint32_t *>(sm + OFF_V + offv) = ov;
+            }
+            named_bar(kBarPrep, 128);
+            if (t < C) {
+                float acc = 0.f;
+                for (int pp = 0; pp < 64; ++pp)
+                    acc += *reinterpret_cast<const float *>(sm + OFF_AL + (pp >> 5) * 8192 +
+                                                            ptx::sw128_off(t, (pp & 31) * 4));
+                reinterpret_cast<float *>(sm + OFF_PD)[t] = acc;
+            }
+            ptx::fence_proxy_async_smem();
+            named_bar(kBarPrep, 128);
+            if (t == 0) ptx::mbar_arrive(&S.bar[B_P1 + b]);
+            // conv window after this chunk (second half holds it): keep for the next chunk and
+            // store it into a checkpoint that ends here, or into the active object at the end.
+            if (hf == 1) {
+#pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    halo[u * 384 + c0] = __float2bfloat16_rn(wqv[u].x);
+                    halo[u * 384 + c0 + 1] = __float2bfloat16_rn(wqv[u].y);
+                    halo[u * 384 + D + c0] = __float2bfloat16_rn(wkv[u].x);
+                    halo[u * 384 + D + c0 + 1] = __float2bfloat16_rn(wkv[u].y);
+                    halo[u * 384 + 2 * D + c0] = __float2bfloat16_rn(wvv[u].x);
+                    halo[u * 384 + 2 * D + c0 + 1] = __float2bfloat16_rn(wvv[u].y);
+                }
+            }
+            named_bar(kBarPrep, 128);
+            {
+                const int64_t cend = abs0 + r_end;
+                while (nck < m.ckpt_count) {
+                    const CkptMeta ck = a.ckpts[m.ckpt_begin + nck];
+                    if (ck.pos > cend) break;
+                    if (ck.pos == cend) {
+                        const int32_t *pg = a.pages + ck.pages_off;
+                        for (int e = t; e < 9 * D; e += 128) {
+                            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(
+                                obj_addr(a.pool, pg, rec + (uint64_t)D * D * 4 + (uint64_t)e * 2, a.status));
+                            if (dst) *dst = halo[e];
+                        }
+                    }
+                    ++nck;
+                }
+            }
+            // ---------------- P2: G | P from TMEM, T = (I + A)^{-1} Diag(beta)
+            if (!wg_wait(S, B_GP + b, par(lc), t, kBarPrep, pflag)) break;
+            if (lc >= 1 && !wg_wait(S, B_M3 + ((lc - 1) & 1), par(lc - 1), t, kBarPrep, pflag)) break;   // scratch free
+            ptx::tc_fence_after();
+            {
+                float g[64];
+                const uint32_t ta = tbase + ((uint32_t)((warp - kPrepWarp0) * 32) << 16) + COL_GP;
+                ptx::tmem_ld32(ta, *reinterpret_cast<float(*)[32]>(&g[0]));
+                ptx::tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&g[32]));
+                ptx::tmem_wait_ld();
+                if (t < C) {
+                    const int r = t;
+                    const float br = bs[b * 64 + r];
+#pragma unroll
+                    for (int s = 0; s < 64; ++s) Msc[msc_idx(r, s)] = s < r ? br * g[s] : 0.f;
+                } else {
+                    const int r = t - C;
+                    uint8_t *pr = sm + OFF_P + b * 8192;
+                    const float pd = reinterpret_cast<const float *>(sm + OFF_PD)[r];
+#pragma unroll
+                    for (int s2 = 0; s2 < 64; ++s2)
+                        if (s2 == r) g[s2] = pd;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint4 v;
+                        uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            const int s0 = ch * 8 + q2 * 2;
+                            vv[q2] = pack_bf16x2(s0 <= r ? g[s0] : 0.f, s0 + 1 <= r ? g[s0 + 1] : 0.f);
+                        }
+                        *reinterpret_cast<uint4 *>(pr + ptx::sw128_off(r, ch * 16)) = v;
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            named_bar(kBarPrep, 128);
+            // level 0: invert the four 16x16 diagonal blocks, one row per thread
+            if (t < C) {
+                const int r = t, bb = r >> 4, rr = r & 15;
+                float x[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) x[c] = c == rr ? 1.f : 0.f;
+#pragma unroll
+                for (int c = 14; c >= 0; --c) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int mm = c + 1; mm < 16; ++mm) acc = fmaf(x[mm], Msc[msc_idx(bb * 16 + mm, bb * 16 + c)], acc);
+                    if (c < rr) x[c] = -acc;
+                }
+                named_bar(kBarPrep + 2, 64);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) Msc[msc_idx(r, bb * 16 + c)] = x[c];
+            }
+            named_bar(kBarPrep, 128);
+            // block rows 1..3: Inv_ij = -Inv_ii sum_{m=j}^{i-1} A_im Inv_mj, one warp per block
+            const int pw = warp - kPrepWarp0;
+            for (int i = 1; i < 4; ++i) {
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if (pw < i)
+                    for (int mm = pw; mm < i; ++mm) blk_mma(acc, Msc, i, mm, pw, lane);
+                named_bar(kBarPrep, 128);
+                if (pw < i) {
+                    blk_store(Msc, i, pw, acc, 1.f, lane);
+                    __syncwarp();
+                    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    blk_mma(acc2, Msc, i, i, pw, lane);
+                    __syncwarp();
+                    blk_store(Msc, i, pw, acc2, -1.f, lane);
+                }
+                named_bar(kBarPrep, 128);
+            }
+            // T = Inv Diag(beta) -> bf16 operand [r][s]
+            if (t < C) {
+                const int r = t;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 v;
+                    uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        const int s0 = ch * 8 + q2 * 2;
+                        const float x0 = s0 <= r ? Msc[msc_idx(r, s0)] * bs[b * 64 + s0] : 0.f;
+                        const float x1 = s0 + 1 <= r ? Msc[msc_idx(r, s0 + 1)] * bs[b * 64 + s0 + 1] : 0.f;
+                        vv[q2] = pack_bf16x2(x0, x1);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + OFF_T + ptx::sw128_off(r, ch * 16)) = v;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            named_bar(kBarPrep, 128);
+            if (t == 0) ptx::mbar_arrive(&S.bar[B_T + b]);
+            // ---------------- P3: WK'^T from TMEM -> bf16 operand rows (row = key channel)
+            if (!wg_wait(S, B_M2 + b, par(lc), t, kBarPrep, pflag)) break;
+            ptx::tc_fence_after();
+            {
+                float w[64];
+                const uint32_t ta = tbase + ((uint32_t)((warp - kPrepWarp0) * 32) << 16) + COL_WK;
+                ptx::tmem_ld32(ta, *reinterpret_cast<float(*)[32]>(&w[0]));
+                ptx::tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&w[32]));
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 v;
+                    uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) vv[q2] = pack_bf16x2(w[ch * 8 + 2 * q2], w[ch * 8 + 2 * q2 + 1]);
+                    *reinterpret_cast<uint4 *>(sm + OFF_WK + ptx::sw128_off(t, ch * 16)) = v;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            named_bar(kBarPrep, 128);
+            if (t == 0) ptx::mbar_arrive(&S.bar[B_WK + b]);
+        }
+        // final conv window into the active object
+        for (int e = t; e < 9 * D; e += 128) {
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(
+                obj_addr(a.pool, act_pages, rec + (uint64_t)D * D * 4 + (uint64_t)e * 2, a.status));
+            if (dst) *dst = halo[e];
+        }
+    } else if (warp >= kSeqWarp0) {
+        // ------------------------------------------------------------------ seq warpgroup
+        const int j = tid - kSeqWarp0 * 32;           // value channel = TMEM lane
+        const uint32_t lanes = (uint32_t)((warp - kSeqWarp0) * 32) << 16;
+        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(a.o);
+        // initial state (S^T row j = column j of S)
+        for (int i0 = 0; i0 < D; i0 += 32) {
+            float v[32];
+#pragma unroll
+            for (int ii = 0; ii < 32; ++ii) {
+                float x = 0.f;
+                if (m.has_init) {
+                    const float *p = reinterpret_cast<const float *>(
+                        obj_addr(a.pool, act_pages, rec + ((uint64_t)(i0 + ii) * D + j) * 4, a.status));
+                    if (p) x = *p;
+                }
+                v[ii] = x;
+            }
+            ptx::tmem_st32(tbase + lanes + COL_S + i0, v);
+        }
+        ptx::tmem_wait_st();
+        int nck = 0;
+        auto write_state_ckpts = [&](int64_t cend, bool final_state) {
+            // S (fp32, from TMEM) into the checkpoints ending at cend, and the active object
+            bool any = final_state;
+            int k = nck;
+            while (k < m.ckpt_count && a.ckpts[m.ckpt_begin + k].pos <= cend) {
+                if (a.ckpts[m.ckpt_begin + k].pos == cend) any = true;
+                ++k;
+            }
+            if (!any) {
+                nck = k;
+                return;
+            }
+            for (int i0 = 0; i0 < D; i0 += 32) {
+                float v[32];
+                ptx::tmem_ld32(tbase + lanes + COL_S + i0, v);
+                ptx::tmem_wait_ld();
+                for (int kk = nck; kk < k; ++kk) {
+                    const CkptMeta ck = a.ckpts[m.ckpt_begin + kk];
+                    if (ck.pos != cend) continue;
+                    const int32_t *pg = a.pages + ck.pages_off;
+#pragma unroll 4
+                    for (int ii = 0; ii < 32; ++ii) {
+                        float *dst = reinterpret_cast<float *>(
+                            obj_addr(a.pool, pg, rec + ((uint64_t)(i0 + ii) * D + j) * 4, a.status));
+                        if (dst) *dst = v[ii];
+                    }
+                }
+                if (final_state) {
+#pragma unroll 4
+                    for (int ii = 0; ii < 32; ++ii) {
+                        float *dst = reinterpret_cast<float *>(
+                            obj_addr(a.pool, act_pages, rec + ((uint64_t)(i0 + ii) * D + j) * 4, a.status));
+                        if (dst) *dst = v[ii];
+                    }
+                }
+            }
+            nck = k;
+        };
+        auto store_outputs = [&](int lc) {
+            const int b = lc & 1;
+            const int64_t abs0 = (c_first + lc) * C;
+            const int r_first = start > abs0 ? (int)(start - abs0) : 0;
+            const int r_end = end - abs0 < C ? (int)(end - abs0) : C;
+            const int64_t row0 = (int64_t)m.tok_begin + (abs0 - start);
+            for (int r0 = 0; r0 < C; r0 += 32) {
+                float v[32];
+                ptx::tmem_ld32(tbase + lanes + COL_O + b * 64 + r0, v);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int r = r0 + rr;
+                    if (r >= r_first && r < r_end) og[((row0 + r) * H + h) * D + j] = __float2bfloat16_rn(v[rr]);
+                }
+            }
+            ptx::tc_fence_before();
+            named_bar(kBarSeq, 128);
+            if (j == 0) ptx::mbar_arrive(&S.bar[B_DO + b]);
+        };
+        volatile int *sflag = wg_flag + 1;
+        bool ok = true;
+        for (int lc = 0; lc < nchunks; ++lc) {
+            const int b = lc & 1;
+            // ---------------- E1: checkpoint S, decay S by gamma_C in TMEM, bf16 operand
+            if (lc >= 1) {
+                if (!(ok = wg_wait(S, B_M4 + ((lc - 1) & 1), par(lc - 1), j, kBarSeq, sflag))) break;
+                ptx::tc_fence_after();
+                write_state_ckpts((c_first + lc) * C, false);
+            }
+            if (!(ok = wg_wait(S, B_P1 + b, par(lc), j, kBarSeq, sflag))) break;
+            const float *gcb = gC + b * 128;
+            for (int i0 = 0; i0 < D; i0 += 32) {
+                float v[32];
+                ptx::tmem_ld32(tbase + lanes + COL_S + i0, v);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int ii = 0; ii < 32; ++ii) v[ii] *= gcb[i0 + ii];
+                ptx::tmem_st32(tbase + lanes + COL_S + i0, v);
+                // bf16 row j of (Gamma S)^T: columns i0..i0+31 = 64 bytes
+                uint8_t *row = sm + OFF_SB + (i0 >> 6) * 16384;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint4 pk;
+                    uint32_t *pp = reinterpret_cast<uint32_t *>(&pk);
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) pp[q2] = pack_bf16x2(v[ch * 8 + 2 * q2], v[ch * 8 + 2 * q2 + 1]);
+                    *reinterpret_cast<uint4 *>(row + ptx::sw128_off(j, ((i0 & 63) * 2) + ch * 16)) = pk;
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            named_bar(kBarSeq, 128);
+            if (j == 0) ptx::mbar_arrive(&S.bar[B_SB + b]);
+            // ---------------- E3 of the previous chunk (off the critical path)
+            if (lc >= 1) store_outputs(lc - 1);
+            // ---------------- E2: W^T -> bf16 operand
+            if (!(ok = wg_wait(S, B_W + b, par(lc), j, kBarSeq, sflag))) break;
+            ptx::tc_fence_after();
+            for (int r0 = 0; r0 < C; r0 += 32) {
+                float v[32];
+                ptx::tmem_ld32(tbase + lanes + COL_W + b * 64 + r0, v);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint4 pk;
+                    uint32_t *pp = reinterpret_cast<uint32_t *>(&pk);
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) pp[q2] = pack_bf16x2(v[ch * 8 + 2 * q2], v[ch * 8 + 2 * q2 + 1]);
+                    *reinterpret_cast<uint4 *>(sm + OFF_WT + ptx::sw128_off(j, r0 * 2 + ch * 16)) = pk;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            named_bar(kBarSeq, 128);
+            if (j == 0) ptx::mbar_arrive(&S.bar[B_WT + b]);
+        }
+        if (nchunks > 0 && ok && wg_wait(S, B_M4 + ((nchunks - 1) & 1), par(nchunks - 1), j, kBarSeq, sflag)) {
+            ptx::tc_fence_after();
+            write_state_ckpts(end, true);
+            store_outputs(nchunks - 1);
+        } else if (nchunks == 0) {
+            write_state_ckpts(end, true);
+        }
+    }
+    // ---------------------------------------------------------------------- teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (*S.err && tid == 0) flag_status(a.status, KDA_DEV_TIMEOUT);
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tbase, 512);
+    }
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PrefillArgs &a) { return a.dtype == KDA_BF16 && a.d == 128; }
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
+    const int64_t T_tot = a.T_tot;
+    CUtensorMap tm[4];
+    const void *src[4] = {a.q, a.k, a.v, a.alpha};
+    for (int i = 0; i < 4; ++i) {
+        std::memset(&tm[i], 0, sizeof(CUtensorMap));
+        const uint64_t rows = T_tot > 0 ? (uint64_t)T_tot : 1;
+        if (encode_tmap_bf16_2d(&tm[i], src[i], (uint64_t)a.H * D, rows, (uint64_t)a.H * D * 2, 64, 64) != 0)
+            return cudaErrorInvalidValue;
+    }
+    auto kern = prefill_tc_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)(a.nseq * a.H), kThreads, SMEM_BYTES, s>>>(a, tm[0], tm[1], tm[2], tm[3]);
+    return cudaGetLastError();
+}
+
+}  // namespace kda
