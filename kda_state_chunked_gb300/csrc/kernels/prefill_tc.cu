@@ -442,42 +442,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 gC[b * 128 + c0 + 1] = gCy;
             }
             float gx = hf ? h0.x : 1.f, gy = hf ? h0.y : 1.f;
-            for (int r = hf * 32; r < hf * 32 + 32; ++r) {
+            // One row: conv of q | k | v, running decay, scaled bf16 operands written in place
+            // (q, k, v tiles) and to Kb; rows outside the sequence become zeros.
+            auto row_step = [&](int r, bool valid) {
                 const uint32_t offk = kb * 16384 + ptx::sw128_off(r, cb);
                 const uint32_t offv = kb * 8192 + ptx::sw128_off(r, cb);
+                const float2 xq = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + offk + 8192));
+                const float2 xk = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + offk));
+                const float2 xv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_V + offv));
+                const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_AL + offv));
                 uint32_t oq = 0, ok = 0, okb = 0, ov = 0;
-                if (r >= r_first && r < r_end) {
-                    const float2 xq = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + offk + 8192));
-                    const float2 xk = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + offk));
-                    const float2 xv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_V + offv));
-                    const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_AL + offv));
-                    float qb0 = wq[0][0] * wqv[0].x + wq[0][1] * wqv[1].x + wq[0][2] * wqv[2].x + wq[0][3] * xq.x;
-                    float qb1 = wq[1][0] * wqv[0].y + wq[1][1] * wqv[1].y + wq[1][2] * wqv[2].y + wq[1][3] * xq.y;
-                    float kb0 = wk[0][0] * wkv[0].x + wk[0][1] * wkv[1].x + wk[0][2] * wkv[2].x + wk[0][3] * xk.x;
-                    float kb1 = wk[1][0] * wkv[0].y + wk[1][1] * wkv[1].y + wk[1][2] * wkv[2].y + wk[1][3] * xk.y;
-                    float vb0 = wv[0][0] * wvv[0].x + wv[0][1] * wvv[1].x + wv[0][2] * wvv[2].x + wv[0][3] * xv.x;
-                    float vb1 = wv[1][0] * wvv[0].y + wv[1][1] * wvv[1].y + wv[1][2] * wvv[2].y + wv[1][3] * xv.y;
+                float dpart = 0.f;
+                if (valid) {
+                    const float qb0 = wq[0][0] * wqv[0].x + wq[0][1] * wqv[1].x + wq[0][2] * wqv[2].x + wq[0][3] * xq.x;
+                    const float qb1 = wq[1][0] * wqv[0].y + wq[1][1] * wqv[1].y + wq[1][2] * wqv[2].y + wq[1][3] * xq.y;
+                    const float kb0 = wk[0][0] * wkv[0].x + wk[0][1] * wkv[1].x + wk[0][2] * wkv[2].x + wk[0][3] * xk.x;
+                    const float kb1 = wk[1][0] * wkv[0].y + wk[1][1] * wkv[1].y + wk[1][2] * wkv[2].y + wk[1][3] * xk.y;
+                    const float vb0 = wv[0][0] * wvv[0].x + wv[0][1] * wvv[1].x + wv[0][2] * wvv[2].x + wv[0][3] * xv.x;
+                    const float vb1 = wv[1][0] * wvv[0].y + wv[1][1] * wvv[1].y + wv[1][2] * wvv[2].y + wv[1][3] * xv.y;
                     wqv[0] = wqv[1]; wqv[1] = wqv[2]; wqv[2] = xq;
                     wkv[0] = wkv[1]; wkv[1] = wkv[2]; wkv[2] = xk;
                     wvv[0] = wvv[1]; wvv[1] = wvv[2]; wvv[2] = xv;
                     gx *= al.x;
                     gy *= al.y;
-                    // this pair's share of the diagonal P[r][r] = qbar_r . kbar_r (the decay
-                    // cancels), kept in fp32 in the alpha slot just read
-                    *reinterpret_cast<float *>(sm + OFF_AL + offv) = qb0 * kb0 + qb1 * kb1;
+                    // this pair's share of the diagonal P[r][r] = qbar_r . kbar_r (the decay cancels)
+                    dpart = qb0 * kb0 + qb1 * kb1;
                     const float sx = gx * icx, sy = gy * icy;      // gamma_r / gamma_C
                     oq = pack_bf16x2(qb0 * sx, qb1 * sy);
                     ok = pack_bf16x2(kb0 * sx, kb1 * sy);
                     okb = pack_bf16x2(kb0 * rcp_approx(sx), kb1 * rcp_approx(sy));
                     ov = pack_bf16x2(vb0, vb1);
                 }
-                else {
-                    *reinterpret_cast<float *>(sm + OFF_AL + offv) = 0.f;
-                }
+                *reinterpret_cast<float *>(sm + OFF_AL + offv) = dpart;   // alpha slot, just read
                 *reinterpret_cast<uint32_t *>(kq + offk + 8192) = oq;
                 *reinterpret_cast<uint32_t *>(kq + offk) = ok;
                 *reinterpret_cast<uint32_t *>(kbt + offv) = okb;
                 *reinterpret_cast<uint32_t *>(sm + OFF_V + offv) = ov;
+            };
+            if (r_first == 0 && r_end == C) {
+#pragma unroll 4
+                for (int rr = 0; rr < 32; ++rr) row_step(hf * 32 + rr, true);
+            } else {
+#pragma unroll 2
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int r = hf * 32 + rr;
+                    row_step(r, r >= r_first && r < r_end);
+                }
             }
             named_bar(kBarPrep, 128);
             if (t < C) {
@@ -525,23 +535,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lc >= 1 && !wg_wait(S, B_M3 + ((lc - 1) & 1), par(lc - 1), t, kBarPrep, pflag)) break;   // scratch free
             ptx::tc_fence_after();
             {
-                float g[64];
+                float g0[32], g1[32];
                 const uint32_t ta = tbase + ((uint32_t)((warp - kPrepWarp0) * 32) << 16) + COL_GP;
-                ptx::tmem_ld32(ta, *reinterpret_cast<float(*)[32]>(&g[0]));
-                ptx::tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&g[32]));
+                ptx::tmem_ld32(ta, g0);
+                ptx::tmem_ld32(ta + 32, g1);
                 ptx::tmem_wait_ld();
                 if (t < C) {
+                    // A row r = beta_r * strict_lower(G) (fp32 scratch, swizzled float4 groups)
                     const int r = t;
                     const float br = bs[b * 64 + r];
+                    float4 *row = reinterpret_cast<float4 *>(Msc + r * 64);
 #pragma unroll
-                    for (int s = 0; s < 64; ++s) Msc[msc_idx(r, s)] = s < r ? br * g[s] : 0.f;
+                    for (int c4 = 0; c4 < 16; ++c4) {
+                        float e[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int s2 = c4 * 4 + u;
+                            const float gv = s2 < 32 ? g0[s2 & 31] : g1[s2 & 31];
+                            e[u] = s2 < r ? br * gv : 0.f;
+                        }
+                        row[c4 ^ (r & 7)] = make_float4(e[0], e[1], e[2], e[3]);
+                    }
                 } else {
+                    // P row r = lower_incl(Qt' Kb^T), with the exact fp32 diagonal
                     const int r = t - C;
                     uint8_t *pr = sm + OFF_P + b * 8192;
                     const float pd = reinterpret_cast<const float *>(sm + OFF_PD)[r];
-#pragma unroll
-                    for (int s2 = 0; s2 < 64; ++s2)
-                        if (s2 == r) g[s2] = pd;
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
                         uint4 v;
@@ -549,7 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int q2 = 0; q2 < 4; ++q2) {
                             const int s0 = ch * 8 + q2 * 2;
-                            vv[q2] = pack_bf16x2(s0 <= r ? g[s0] : 0.f, s0 + 1 <= r ? g[s0 + 1] : 0.f);
+                            const float ga = s0 < 32 ? g0[s0 & 31] : g1[s0 & 31];
+                            const float gb = s0 + 1 < 32 ? g0[(s0 + 1) & 31] : g1[(s0 + 1) & 31];
+                            vv[q2] = pack_bf16x2(s0 < r ? ga : (s0 == r ? pd : 0.f),
+                                                 s0 + 1 < r ? gb : (s0 + 1 == r ? pd : 0.f));
                         }
                         *reinterpret_cast<uint4 *>(pr + ptx::sw128_off(r, ch * 16)) = v;
                     }
@@ -557,22 +579,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tc_fence_before();
             named_bar(kBarPrep, 128);
-            // level 0: invert the four 16x16 diagonal blocks, one row per thread
+            // level 0: invert the four 16x16 diagonal blocks, one row per thread.  Row x of the
+            // inverse solves x (I + A_bb) = e_r; eliminating from the last row upward needs only
+            // rows of A_bb, which every thread of the block reads (broadcast), and no predicate:
+            // x[m] is still zero for m above the thread's own row.
             if (t < C) {
                 const int r = t, bb = r >> 4, rr = r & 15;
                 float x[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) x[c] = c == rr ? 1.f : 0.f;
 #pragma unroll
-                for (int c = 14; c >= 0; --c) {
-                    float acc = 0.f;
+                for (int mm = 15; mm >= 1; --mm) {
+                    const int ar = bb * 16 + mm;
+                    const float4 *arow = reinterpret_cast<const float4 *>(Msc + ar * 64);
+                    float av[16];
 #pragma unroll
-                    for (int mm = c + 1; mm < 16; ++mm) acc = fmaf(x[mm], Msc[msc_idx(bb * 16 + mm, bb * 16 + c)], acc);
-                    if (c < rr) x[c] = -acc;
+                    for (int q = 0; q < 4; ++q) {
+                        if (q * 4 < mm) {
+                            const float4 v4 = arow[(bb * 4 + q) ^ (ar & 7)];
+                            av[q * 4] = v4.x; av[q * 4 + 1] = v4.y; av[q * 4 + 2] = v4.z; av[q * 4 + 3] = v4.w;
+                        }
+                    }
+                    const float xm = x[mm];
+#pragma unroll
+                    for (int c = 0; c < mm; ++c) x[c] = fmaf(-xm, av[c], x[c]);
                 }
                 named_bar(kBarPrep + 2, 64);
+                float4 *row = reinterpret_cast<float4 *>(Msc + r * 64);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) Msc[msc_idx(r, bb * 16 + c)] = x[c];
+                for (int q = 0; q < 4; ++q)
+                    row[(bb * 4 + q) ^ (r & 7)] = make_float4(x[q * 4], x[q * 4 + 1], x[q * 4 + 2], x[q * 4 + 3]);
             }
             named_bar(kBarPrep, 128);
             // block rows 1..3: Inv_ij = -Inv_ii sum_{m=j}^{i-1} A_im Inv_mj, one warp per block
@@ -595,17 +631,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             // T = Inv Diag(beta) -> bf16 operand [r][s]
             if (t < C) {
                 const int r = t;
+                const float4 *row = reinterpret_cast<const float4 *>(Msc + r * 64);
+                const float4 *b4 = reinterpret_cast<const float4 *>(bs + b * 64);
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
-                    uint4 v;
-                    uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
+                    float e[8];
 #pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        const int s0 = ch * 8 + q2 * 2;
-                        const float x0 = s0 <= r ? Msc[msc_idx(r, s0)] * bs[b * 64 + s0] : 0.f;
-                        const float x1 = s0 + 1 <= r ? Msc[msc_idx(r, s0 + 1)] * bs[b * 64 + s0 + 1] : 0.f;
-                        vv[q2] = pack_bf16x2(x0, x1);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int c4 = ch * 2 + h2;
+                        const float4 mv = row[c4 ^ (r & 7)];
+                        const float4 bv = b4[c4];
+                        e[h2 * 4 + 0] = c4 * 4 + 0 <= r ? mv.x * bv.x : 0.f;
+                        e[h2 * 4 + 1] = c4 * 4 + 1 <= r ? mv.y * bv.y : 0.f;
+                        e[h2 * 4 + 2] = c4 * 4 + 2 <= r ? mv.z * bv.z : 0.f;
+                        e[h2 * 4 + 3] = c4 * 4 + 3 <= r ? mv.w * bv.w : 0.f;
                     }
+                    uint4 v;
+                    v.x = pack_bf16x2(e[0], e[1]);
+                    v.y = pack_bf16x2(e[2], e[3]);
+                    v.z = pack_bf16x2(e[4], e[5]);
+                    v.w = pack_bf16x2(e[6], e[7]);
                     *reinterpret_cast<uint4 *>(sm + OFF_T + ptx::sw128_off(r, ch * 16)) = v;
                 }
             }
@@ -616,17 +661,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wg_wait(S, B_M2 + b, par(lc), t, kBarPrep, pflag)) break;
             ptx::tc_fence_after();
             {
-                float w[64];
+                float w0[32], w1[32];
                 const uint32_t ta = tbase + ((uint32_t)((warp - kPrepWarp0) * 32) << 16) + COL_WK;
-                ptx::tmem_ld32(ta, *reinterpret_cast<float(*)[32]>(&w[0]));
-                ptx::tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&w[32]));
+                ptx::tmem_ld32(ta, w0);
+                ptx::tmem_ld32(ta + 32, w1);
                 ptx::tmem_wait_ld();
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     uint4 v;
                     uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
 #pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) vv[q2] = pack_bf16x2(w[ch * 8 + 2 * q2], w[ch * 8 + 2 * q2 + 1]);
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        const int c = ch * 8 + 2 * q2;
+                        vv[q2] = c < 32 ? pack_bf16x2(w0[c & 31], w0[(c + 1) & 31])
+                                        : pack_bf16x2(w1[c & 31], w1[(c + 1) & 31]);
+                    }
                     *reinterpret_cast<uint4 *>(sm + OFF_WK + ptx::sw128_off(t, ch * 16)) = v;
                 }
             }
