@@ -289,9 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // M3: O^T = SB Qt'^T ; W^T += -SB WK'^T
                 if (n3 == n4 && n3 < nchunks) {
                     const int b = n3 & 1;
-                    if (ptx::mbar_try_wait(&S.bar[B_SB + b], par(n3)) &&
-                        ptx::mbar_try_wait(&S.bar[B_WK + b], par(n3)) &&
-                        (n3 < 2 || ptx::mbar_try_wait(&S.bar[B_DO + b], par(n3 - 2)))) {
+                    if (ptx::mbar_test(&S.bar[B_SB + b], par(n3)) &&
+                        ptx::mbar_test(&S.bar[B_WK + b], par(n3)) &&
+                        (n3 < 2 || ptx::mbar_test(&S.bar[B_DO + b], par(n3 - 2)))) {
                         ptx::tc_fence_after();
                         const uint32_t sb = sbase + OFF_SB, kq = sbase + OFF_KQ + b * 32768, wk = sbase + OFF_WK;
                         for (int s = 0; s < 8; ++s) {
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // M4: S^T += W^T Kb ; O^T += W^T P^T
                 if (n4 < n3) {
                     const int b = n4 & 1;
-                    if (ptx::mbar_try_wait(&S.bar[B_WT + b], par(n4))) {
+                    if (ptx::mbar_test(&S.bar[B_WT + b], par(n4))) {
                         ptx::tc_fence_after();
                         const uint32_t wt = sbase + OFF_WT, kb = sbase + OFF_KB + b * 16384, pb = sbase + OFF_P + b * 8192;
                         for (int s = 0; s < 4; ++s) {
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // M1: [Kt'; Qt'] Kb^T -> G | P
                 if (n1 < nchunks) {
                     const int b = n1 & 1;
-                    if (ptx::mbar_try_wait(&S.bar[B_P1 + b], par(n1))) {
+                    if (ptx::mbar_test(&S.bar[B_P1 + b], par(n1))) {
                         ptx::tc_fence_after();
                         const uint32_t kq = sbase + OFF_KQ + b * 32768, kb = sbase + OFF_KB + b * 16384;
                         for (int s = 0; s < 8; ++s) {
@@ -350,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // M2: WK'^T = Kt'^T T^T ; U^T = V^T T^T
                 if (n2 < n1) {
                     const int b = n2 & 1;
-                    if (ptx::mbar_try_wait(&S.bar[B_T + b], par(n2)) &&
-                        (n2 < 2 || ptx::mbar_try_wait(&S.bar[B_WT + b], par(n2 - 2)))) {
+                    if (ptx::mbar_test(&S.bar[B_T + b], par(n2)) &&
+                        (n2 < 2 || ptx::mbar_test(&S.bar[B_WT + b], par(n2 - 2)))) {
                         ptx::tc_fence_after();
                         const uint32_t kq = sbase + OFF_KQ + b * 32768, v = sbase + OFF_V, t = sbase + OFF_T;
                         for (int s = 0; s < 4; ++s) {
@@ -388,12 +388,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *Msc = reinterpret_cast<float *>(sm + OFF_WK);
         int nck = 0;   // next checkpoint index of this sequence (window part)
         volatile int *pflag = wg_flag;
+        // beta of chunk lc for this thread's row t (t < 64); 0 outside the sequence
+        auto load_beta = [&](int lc2) {
+            const int64_t a0 = (c_first + lc2) * C;
+            const int64_t pos = a0 + t;
+            if (pos < start || pos >= end) return 0.f;
+            return __bfloat162float(betag[((int64_t)m.tok_begin + (pos - start)) * H + h]);
+        };
+        float beta_next = (t < C && nchunks > 0) ? load_beta(0) : 0.f;
         for (int lc = 0; lc < nchunks; ++lc) {
             const int b = lc & 1;
             const int64_t abs0 = (c_first + lc) * C;
             const int r_first = start > abs0 ? (int)(start - abs0) : 0;
             const int r_end = end - abs0 < C ? (int)(end - abs0) : C;
-            const int64_t row0 = (int64_t)m.tok_begin + (abs0 - start);
             // ---------------- P1: conv, decay, scaled operands
             if (!wg_wait(S, B_FULL + b, par(lc), t, kBarPrep, pflag)) break;
             if (lc >= 2 && !wg_wait(S, B_M4 + b, par(lc - 2), t, kBarPrep, pflag)) break;   // Kb / P slot free
@@ -423,17 +430,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wvv[0] = wvv[1]; wvv[1] = wvv[2]; wvv[2] = xv;
                 }
             }
-            // alpha product over this half's rows
-            float2 ap = make_float2(1.f, 1.f);
-            for (int r = hf * 32; r < hf * 32 + 32; ++r) {
-                if (r < r_first || r >= r_end) continue;
+            // alpha product over this half's rows (four independent partial products)
+            float2 ap[4] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f), make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
+#pragma unroll 8
+            for (int rr = 0; rr < 32; ++rr) {
+                const int r = hf * 32 + rr;
                 const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_AL + kb * 8192 + ptx::sw128_off(r, cb)));
-                ap.x *= al.x;
-                ap.y *= al.y;
+                const bool valid = r >= r_first && r < r_end;
+                ap[rr & 3].x *= valid ? al.x : 1.f;
+                ap[rr & 3].y *= valid ? al.y : 1.f;
             }
-            red[hf * 64 + p] = ap;
-            if (t < C) bs[b * 64 + t] = (t >= r_first && t < r_end) ? __bfloat162float(betag[(row0 + t) * H + h]) : 0.f;
+            red[hf * 64 + p] = make_float2((ap[0].x * ap[1].x) * (ap[2].x * ap[3].x), (ap[0].y * ap[1].y) * (ap[2].y * ap[3].y));
+            if (t < C) bs[b * 64 + t] = beta_next;
             named_bar(kBarPrep, 128);
+            // fetch the next chunk's beta now; it is needed only one chunk later
+            if (t < C && lc + 1 < nchunks) beta_next = load_beta(lc + 1);
             const float2 h0 = red[p], h1 = red[64 + p];
             const float gCx = h0.x * h1.x, gCy = h0.y * h1.y;
             const float icx = 1.f / gCx, icy = 1.f / gCy;
@@ -443,14 +454,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float gx = hf ? h0.x : 1.f, gy = hf ? h0.y : 1.f;
             // One row: conv of q | k | v, running decay, scaled bf16 operands written in place
-            // (q, k, v tiles) and to Kb; rows outside the sequence become zeros.
-            auto row_step = [&](int r, bool valid) {
-                const uint32_t offk = kb * 16384 + ptx::sw128_off(r, cb);
-                const uint32_t offv = kb * 8192 + ptx::sw128_off(r, cb);
-                const float2 xq = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + offk + 8192));
-                const float2 xk = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + offk));
-                const float2 xv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_V + offv));
-                const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_AL + offv));
+            // (q, k, v tiles) and to Kb; rows outside the sequence become zeros.  The 128-byte
+            // swizzle of a row depends only on r mod 8, so the eight in-row offsets of this
+            // thread's channel pair are computed once; full chunks take a branch-free path of
+            // eight rows at a time with all loads issued before the in-place stores.
+            uint32_t swz[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) swz[u] = ptx::sw128_off(u, cb);
+            uint8_t *const qrow = kq + kb * 16384 + 8192, *const krow = kq + kb * 16384;
+            uint8_t *const vrow = sm + OFF_V + kb * 8192, *const arow = sm + OFF_AL + kb * 8192;
+            uint8_t *const kbrow = kbt + kb * 8192;
+            auto row_proc = [&](uint32_t off, float2 xq, float2 xk, float2 xv, float2 al, bool valid) {
                 uint32_t oq = 0, ok = 0, okb = 0, ov = 0;
                 float dpart = 0.f;
                 if (valid) {
@@ -473,20 +487,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     okb = pack_bf16x2(kb0 * rcp_approx(sx), kb1 * rcp_approx(sy));
                     ov = pack_bf16x2(vb0, vb1);
                 }
-                *reinterpret_cast<float *>(sm + OFF_AL + offv) = dpart;   // alpha slot, just read
-                *reinterpret_cast<uint32_t *>(kq + offk + 8192) = oq;
-                *reinterpret_cast<uint32_t *>(kq + offk) = ok;
-                *reinterpret_cast<uint32_t *>(kbt + offv) = okb;
-                *reinterpret_cast<uint32_t *>(sm + OFF_V + offv) = ov;
+                *reinterpret_cast<float *>(arow + off) = dpart;   // alpha slot, already read
+                *reinterpret_cast<uint32_t *>(qrow + off) = oq;
+                *reinterpret_cast<uint32_t *>(krow + off) = ok;
+                *reinterpret_cast<uint32_t *>(kbrow + off) = okb;
+                *reinterpret_cast<uint32_t *>(vrow + off) = ov;
             };
             if (r_first == 0 && r_end == C) {
-#pragma unroll 4
-                for (int rr = 0; rr < 32; ++rr) row_step(hf * 32 + rr, true);
+#pragma unroll 1
+                for (int r0 = hf * 32; r0 < hf * 32 + 32; r0 += 8) {
+                    float2 xq[8], xk[8], xv[8], al[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t off = (uint32_t)(r0 + u) * 128u + (swz[u] & 127u);
+                        xq[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qrow + off));
+                        xk[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(krow + off));
+                        xv[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(vrow + off));
+                        al[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(arow + off));
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        row_proc((uint32_t)(r0 + u) * 128u + (swz[u] & 127u), xq[u], xk[u], xv[u], al[u], true);
+                }
             } else {
-#pragma unroll 2
-                for (int rr = 0; rr < 32; ++rr) {
-                    const int r = hf * 32 + rr;
-                    row_step(r, r >= r_first && r < r_end);
+#pragma unroll 1
+                for (int r = hf * 32; r < hf * 32 + 32; ++r) {
+                    const uint32_t off = ptx::sw128_off((uint32_t)r, cb);
+                    const float2 xq = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qrow + off));
+                    const float2 xk = bf2_to_f2(*reinterpret_cast<const uint32_t *>(krow + off));
+                    const float2 xv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(vrow + off));
+                    const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(arow + off));
+                    row_proc(off, xq, xk, xv, al, r >= r_first && r < r_end);
                 }
             }
             named_bar(kBarPrep, 128);
@@ -611,23 +642,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                     row[(bb * 4 + q) ^ (r & 7)] = make_float4(x[q * 4], x[q * 4 + 1], x[q * 4 + 2], x[q * 4 + 3]);
             }
             named_bar(kBarPrep, 128);
-            // block rows 1..3: Inv_ij = -Inv_ii sum_{m=j}^{i-1} A_im Inv_mj, one warp per block
-            const int pw = warp - kPrepWarp0;
-            for (int i = 1; i < 4; ++i) {
-                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                if (pw < i)
-                    for (int mm = pw; mm < i; ++mm) blk_mma(acc, Msc, i, mm, pw, lane);
-                named_bar(kBarPrep, 128);
-                if (pw < i) {
-                    blk_store(Msc, i, pw, acc, 1.f, lane);
+            // Off-diagonal blocks of Inv = (I + A)^{-1}, in 32 x 32 halves (tf32 mma.sync, one
+            // warp per 16 x 16 block).  With J0, J1 the inverses of the two diagonal 32 x 32 blocks
+            // and B the lower-left 32 x 32 block of A:
+            //   J0 = [[I00, 0], [-I11 A10 I00, I11]],  J1 likewise from blocks 2, 3,
+            //   lower-left of Inv = -J1 (B J0).
+            {
+                const int pw = warp - kPrepWarp0;
+                const float zero4[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                // step A: X10 = -I11 (A10 I00) on warp 0, X32 = -I33 (A32 I22) on warp 1
+                if (pw < 2) {
+                    const int i = pw == 0 ? 1 : 3, j = i - 1;
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    blk_mma(acc, Msc, i, j, j, lane);
+                    __syncwarp();
+                    blk_store(Msc, i, j, acc, 1.f, lane);
                     __syncwarp();
                     float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    blk_mma(acc2, Msc, i, i, pw, lane);
+                    blk_mma(acc2, Msc, i, i, j, lane);
                     __syncwarp();
-                    blk_store(Msc, i, pw, acc2, -1.f, lane);
+                    blk_store(Msc, i, j, acc2, -1.f, lane);
                 }
                 named_bar(kBarPrep, 128);
+                // step B1: Y = B J0, block (bi, bj) = (2 + pw / 2, pw % 2) per warp
+                const int bi = 2 + (pw >> 1), bj = pw & 1;
+                float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if (bj == 0) {
+                    blk_mma(y, Msc, bi, 0, 0, lane);     // A_i0 I00
+                    blk_mma(y, Msc, bi, 1, 0, lane);     // A_i1 X10
+                } else {
+                    blk_mma(y, Msc, bi, 1, 1, lane);     // A_i1 I11
+                }
+                named_bar(kBarPrep, 128);
+                blk_store(Msc, bi, bj, y, 1.f, lane);
+                named_bar(kBarPrep, 128);
+                // step B2: Z = -J1 Y
+                float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if (bi == 2) {
+                    blk_mma(z, Msc, 2, 2, bj, lane);     // I22 Y2j
+                } else {
+                    blk_mma(z, Msc, 3, 2, bj, lane);     // X32 Y2j
+                    blk_mma(z, Msc, 3, 3, bj, lane);     // I33 Y3j
+                }
+                named_bar(kBarPrep, 128);
+                blk_store(Msc, bi, bj, z, -1.f, lane);
+                (void)zero4;
             }
+            named_bar(kBarPrep, 128);
             // T = Inv Diag(beta) -> bf16 operand [r][s]
             if (t < C) {
                 const int r = t;
