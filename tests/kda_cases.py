@@ -69,13 +69,19 @@ class Prefill:
     """One prefill call through the binding, with its checkpoint plan."""
 
     def __init__(self, pool, toks, cu, start_pos, has_init, active_pages, stride=1,
-                 include_last=True, hash_block=512):
+                 include_last=True, hash_block=512, checkpoints=True):
         q = toks["q"]
         T_tot, H, d = q.shape
         dt = kda.dtype_of(q)
         self.H, self.d = H, d
-        self.seq, self.pos, self.pages = kda.kda_ckpt_plan(pool, H, d, dt, cu, start_pos, hash_block,
-                                                           stride, include_last)
+        if checkpoints:
+            self.seq, self.pos, self.pages = kda.kda_ckpt_plan(pool, H, d, dt, cu, start_pos, hash_block,
+                                                               stride, include_last)
+        else:
+            P0 = pool.object_pages(H, d, dt)
+            self.seq = np.zeros(0, np.int32)
+            self.pos = np.zeros(0, np.int64)
+            self.pages = np.zeros((0, P0), np.int32)
         P = pool.object_pages(H, d, dt)
         ws = torch.empty(kda.kda_prefill_workspace_bytes(len(cu) - 1, len(self.seq), P),
                          dtype=torch.uint8, device=q.device)
