@@ -18,8 +18,9 @@
 //   W^T  = U^T - (Gamma_C S)^T WK'^T
 //   S^T <- (Gamma_C S)^T + W^T Kb
 // The state lives transposed in TMEM (lane = value channel j, column = key channel i), so every
-// state contraction has M = 128; the scaled state (Gamma_C S)^T is also kept as a bf16 operand
-// in shared memory.  Decay is anchored at the chunk end, so no per-element division is needed.
+// state contraction has M = 128; the scaled state (Gamma_C S)^T is also kept in TMEM as the bf16
+// A operand of the next contraction.  Decay is anchored at the chunk end, so no per-element
+// division is needed.
 //
 // Warp roles (12 warps): warp 0 issues TMA loads of the raw q, k, v, alpha tiles; warp 1 issues
 // all tcgen05.mma from one thread; warps 4-7 ("prep") do the conv, the decay scaling and the
@@ -43,30 +44,30 @@ namespace {
 
 constexpr int D = 128;
 constexpr int C = kChunk;            // 64
-constexpr int kThreads = 384;
-constexpr int kPrepWarp0 = 4, kSeqWarp0 = 8;
-constexpr int kBarPrep = 1, kBarSeq = 2;
+constexpr int kThreads = 512;
+constexpr int kPrepWarp0 = 4, kSolveWarp0 = 8, kSeqWarp0 = 12;
+constexpr int kBarPrep = 1, kBarSeq = 2, kBarSolve = 3, kBarSolveHalf = 4;
 
 // Shared-memory map (byte offsets from a 1024-aligned base).
 constexpr uint32_t OFF_KQ = 0;          // [2 slots][2 kb][128 rows: k 0-63 | q 64-127][128 B]
 constexpr uint32_t OFF_KB = 65536;      // [2 slots][2 kb][64 rows][128 B]   Kb
-constexpr uint32_t OFF_V = 98304;       // [2 kb][64 rows][128 B]            raw v -> V
-constexpr uint32_t OFF_AL = 114688;     // [2 kb][64 rows][128 B]            raw alpha
-constexpr uint32_t OFF_P = 131072;      // [2 slots][64 rows][128 B]         P
-constexpr uint32_t OFF_T = 147456;      // [64 rows][128 B]                  T
-constexpr uint32_t OFF_WK = 155648;     // [128 rows][128 B] WK'^T; fp32 64x64 solve scratch
-constexpr uint32_t OFF_SB = 172032;     // [2 kb][128 rows][128 B]           (Gamma S)^T bf16
+constexpr uint32_t OFF_V = 98304;       // [2 slots][2 kb][64 rows][128 B]   raw v -> V
+constexpr uint32_t OFF_AL = 131072;     // [2 slots][2 kb][64 rows][128 B]   raw alpha
+constexpr uint32_t OFF_P = 163840;      // [2 slots][64 rows][128 B]         P
+constexpr uint32_t OFF_T = 180224;      // [64 rows][128 B]                  T
+constexpr uint32_t OFF_WK = 188416;     // [128 rows][128 B] WK'^T; fp32 64x64 solve scratch
 constexpr uint32_t OFF_WT = 204800;     // [128 rows][128 B]                 W^T bf16
 constexpr uint32_t OFF_GC = 221184;     // float [2][128]                    gamma_C
 constexpr uint32_t OFF_BS = 222208;     // float [2][64]                     beta
 constexpr uint32_t OFF_RED = 222720;    // float2 [2][64]                    half products of alpha
 constexpr uint32_t OFF_HALO = 223744;   // bf16 [3][384]                     conv window
 constexpr uint32_t OFF_BAR = 226048;    // mbarriers, flags
-constexpr uint32_t OFF_PD = OFF_BAR + 256;   // float [64]  exact diagonal of P
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 512 + 1024;   // + alignment slack
+constexpr uint32_t OFF_PD = OFF_BAR + 256;   // float [2][64]  exact diagonal of P
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 768 + 1024;   // + alignment slack
 
-// TMEM columns.
-constexpr uint32_t COL_S = 0, COL_O = 128, COL_W = 256, COL_GP = 384, COL_WK = 448;
+// TMEM columns.  G|P and WK'^T share columns (their lifetimes do not overlap); the bf16
+// operand (Gamma S)^T of M3 lives in the last 64 columns (two values per column).
+constexpr uint32_t COL_S = 0, COL_O = 128, COL_W = 256, COL_GP = 384, COL_WK = 384, COL_SA = 448;
 
 // mbarrier indices ([2] arrays indexed by local chunk parity).
 enum {
@@ -82,7 +83,8 @@ enum {
     B_WT = 18,       // seq: W^T operand written, D_W read
     B_M4 = 20,       // mma: chunk done (S advanced, O complete)
     B_DO = 22,       // seq: D_O read
-    NUM_BARS = 24
+    B_GPF = 24,      // solve: G|P read from TMEM (the next M1 may overwrite it)
+    NUM_BARS = 26
 };
 
 struct TcParams {
@@ -247,11 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::prefetch_tmap(&tm_a);
             for (int lc = 0; lc < nchunks && !*S.err; ++lc) {
                 const int b = lc & 1;
-                if (lc >= 1) {
-                    if (!wait_bar(S, B_P1 + ((lc - 1) & 1), par(lc - 1))) break;   // alpha consumed
-                    if (!wait_bar(S, B_M2 + ((lc - 1) & 1), par(lc - 1))) break;   // V consumed
+                if (lc >= 2) {
+                    if (!wait_bar(S, B_P1 + b, par(lc - 2))) break;   // alpha slot consumed
+                    if (!wait_bar(S, B_M2 + b, par(lc - 2))) break;   // V slot consumed
+                    if (!wait_bar(S, B_M4 + b, par(lc - 2))) break;   // KQ slot free
                 }
-                if (lc >= 2 && !wait_bar(S, B_M4 + b, par(lc - 2))) break;         // KQ slot free
                 const int64_t abs0 = (c_first + lc) * C;
                 const int32_t y = (int32_t)((int64_t)m.tok_begin + (abs0 - start));
                 uint64_t *fb = &S.bar[B_FULL + b];
@@ -261,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t x = h * D + kb * 64;
                     ptx::tma_load_2d(kq + kb * 16384, &tm_k, fb, x, y);
                     ptx::tma_load_2d(kq + kb * 16384 + 8192, &tm_q, fb, x, y);
-                    ptx::tma_load_2d(sm + OFF_V + kb * 8192, &tm_v, fb, x, y);
-                    ptx::tma_load_2d(sm + OFF_AL + kb * 8192, &tm_a, fb, x, y);
+                    ptx::tma_load_2d(sm + OFF_V + b * 16384 + kb * 8192, &tm_v, fb, x, y);
+                    ptx::tma_load_2d(sm + OFF_AL + b * 16384 + kb * 8192, &tm_a, fb, x, y);
                 }
             }
             // Do not leave while copies may still be landing in shared memory.
@@ -293,16 +295,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mbar_test(&S.bar[B_WK + b], par(n3)) &&
                         (n3 < 2 || ptx::mbar_test(&S.bar[B_DO + b], par(n3 - 2)))) {
                         ptx::tc_fence_after();
-                        const uint32_t sb = sbase + OFF_SB, kq = sbase + OFF_KQ + b * 32768, wk = sbase + OFF_WK;
+                        const uint32_t kq = sbase + OFF_KQ + b * 32768, wk = sbase + OFF_WK;
                         for (int s = 0; s < 8; ++s) {
-                            const uint64_t ad = ptx::sdesc_sw128(sb + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
                             const uint64_t bq = ptx::sdesc_sw128(kq + 8192 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-                            ptx::mma_bf16(tbase + COL_O + b * 64, ad, bq, id_o, s > 0 ? 1u : 0u);
+                            ptx::mma_bf16_ta(tbase + COL_O + b * 64, tbase + COL_SA + s * 8, bq, id_o, s > 0 ? 1u : 0u);
                         }
                         for (int s = 0; s < 8; ++s) {
-                            const uint64_t ad = ptx::sdesc_sw128(sb + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
                             const uint64_t bw = ptx::sdesc_sw128(wk + s * 2048, 8192, 1024);
-                            ptx::mma_bf16(tbase + COL_W + b * 64, ad, bw, id_w, 1u);
+                            ptx::mma_bf16_ta(tbase + COL_W + b * 64, tbase + COL_SA + s * 8, bw, id_w, 1u);
                         }
                         ptx::mma_commit(&S.bar[B_W + b]);
                         ptx::mma_commit(&S.bar[B_M3 + b]);
@@ -334,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // M1: [Kt'; Qt'] Kb^T -> G | P
                 if (n1 < nchunks) {
                     const int b = n1 & 1;
-                    if (ptx::mbar_test(&S.bar[B_P1 + b], par(n1))) {
+                    if (ptx::mbar_test(&S.bar[B_P1 + b], par(n1)) &&
+                        (n1 == 0 || ptx::mbar_test(&S.bar[B_WK + ((n1 - 1) & 1)], par(n1 - 1)))) {
                         ptx::tc_fence_after();
                         const uint32_t kq = sbase + OFF_KQ + b * 32768, kb = sbase + OFF_KB + b * 16384;
                         for (int s = 0; s < 8; ++s) {
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ptx::mbar_test(&S.bar[B_T + b], par(n2)) &&
                         (n2 < 2 || ptx::mbar_test(&S.bar[B_WT + b], par(n2 - 2)))) {
                         ptx::tc_fence_after();
-                        const uint32_t kq = sbase + OFF_KQ + b * 32768, v = sbase + OFF_V, t = sbase + OFF_T;
+                        const uint32_t kq = sbase + OFF_KQ + b * 32768, v = sbase + OFF_V + b * 16384, t = sbase + OFF_T;
                         for (int s = 0; s < 4; ++s) {
                             const uint64_t bd = ptx::sdesc_sw128(t + s * 32, 16, 1024);
                             ptx::mma_bf16(tbase + COL_WK, ptx::sdesc_sw128(kq + s * 2048, 16384, 1024), bd, id_m2,
@@ -370,8 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else if (++spins > ptx::kSpinLimit) *S.err = 1;
             }
         }
-    } else if (warp >= kPrepWarp0 && warp < kSeqWarp0) {
-        // ------------------------------------------------------------------ prep warpgroup
+    } else if (warp >= kPrepWarp0 && warp < kSolveWarp0) {
+        // ------------------------------------------------------------------ conv warpgroup
         const int t = tid - kPrepWarp0 * 32;          // 0..127, TMEM lane
         const int p = t & 63, hf = t >> 6;            // channel pair (2p, 2p+1), row half
         const int c0 = 2 * p, kb = c0 >> 6, cb = (c0 & 63) * 2;   // tile block and column byte
@@ -385,7 +386,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wv[e][j] = a.conv_w[((int64_t)h * 3 * D + 2 * D + c0 + e) * 4 + j];
             }
         const __nv_bfloat16 *betag = static_cast<const __nv_bfloat16 *>(a.beta);
-        float *Msc = reinterpret_cast<float *>(sm + OFF_WK);
         int nck = 0;   // next checkpoint index of this sequence (window part)
         volatile int *pflag = wg_flag;
         // beta of chunk lc for this thread's row t (t < 64); 0 outside the sequence
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t off = kb * 16384 + ptx::sw128_off(r, cb);
                     const float2 xq = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + off + 8192));
                     const float2 xk = bf2_to_f2(*reinterpret_cast<const uint32_t *>(kq + off));
-                    const float2 xv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_V + kb * 8192 + ptx::sw128_off(r, cb)));
+                    const float2 xv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_V + b * 16384 + kb * 8192 + ptx::sw128_off(r, cb)));
                     wqv[0] = wqv[1]; wqv[1] = wqv[2]; wqv[2] = xq;
                     wkv[0] = wkv[1]; wkv[1] = wkv[2]; wkv[2] = xk;
                     wvv[0] = wvv[1]; wvv[1] = wvv[2]; wvv[2] = xv;
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 8
             for (int rr = 0; rr < 32; ++rr) {
                 const int r = hf * 32 + rr;
-                const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_AL + kb * 8192 + ptx::sw128_off(r, cb)));
+                const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(sm + OFF_AL + b * 16384 + kb * 8192 + ptx::sw128_off(r, cb)));
                 const bool valid = r >= r_first && r < r_end;
                 ap[rr & 3].x *= valid ? al.x : 1.f;
                 ap[rr & 3].y *= valid ? al.y : 1.f;
@@ -462,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 8; ++u) swz[u] = ptx::sw128_off(u, cb);
             uint8_t *const qrow = kq + kb * 16384 + 8192, *const krow = kq + kb * 16384;
-            uint8_t *const vrow = sm + OFF_V + kb * 8192, *const arow = sm + OFF_AL + kb * 8192;
+            uint8_t *const vrow = sm + OFF_V + b * 16384 + kb * 8192, *const arow = sm + OFF_AL + b * 16384 + kb * 8192;
             uint8_t *const kbrow = kbt + kb * 8192;
             auto row_proc = [&](uint32_t off, float2 xq, float2 xk, float2 xv, float2 al, bool valid) {
                 uint32_t oq = 0, ok = 0, okb = 0, ov = 0;
@@ -496,18 +496,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (r_first == 0 && r_end == C) {
 #pragma unroll 1
                 for (int r0 = hf * 32; r0 < hf * 32 + 32; r0 += 8) {
-                    float2 xq[8], xk[8], xv[8], al[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint32_t off = (uint32_t)(r0 + u) * 128u + (swz[u] & 127u);
-                        xq[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qrow + off));
-                        xk[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(krow + off));
-                        xv[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(vrow + off));
-                        al[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(arow + off));
+                    for (int h4 = 0; h4 < 8; h4 += 4) {
+                        float2 xq[4], xk[4], xv[4], al[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t off = (uint32_t)(r0 + h4 + u) * 128u + (swz[h4 + u] & 127u);
+                            xq[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qrow + off));
+                            xk[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(krow + off));
+                            xv[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(vrow + off));
+                            al[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(arow + off));
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            row_proc((uint32_t)(r0 + h4 + u) * 128u + (swz[h4 + u] & 127u), xq[u], xk[u], xv[u],
+                                     al[u], true);
                     }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        row_proc((uint32_t)(r0 + u) * 128u + (swz[u] & 127u), xq[u], xk[u], xv[u], al[u], true);
                 }
             } else {
 #pragma unroll 1
@@ -524,9 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t < C) {
                 float acc = 0.f;
                 for (int pp = 0; pp < 64; ++pp)
-                    acc += *reinterpret_cast<const float *>(sm + OFF_AL + (pp >> 5) * 8192 +
+                    acc += *reinterpret_cast<const float *>(sm + OFF_AL + b * 16384 + (pp >> 5) * 8192 +
                                                             ptx::sw128_off(t, (pp & 31) * 4));
-                reinterpret_cast<float *>(sm + OFF_PD)[t] = acc;
+                reinterpret_cast<float *>(sm + OFF_PD)[b * 64 + t] = acc;
             }
             ptx::fence_proxy_async_smem();
             named_bar(kBarPrep, 128);
@@ -561,13 +565,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++nck;
                 }
             }
+        }
+        // final conv window into the active object
+        for (int e = t; e < 9 * D; e += 128) {
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(
+                obj_addr(a.pool, act_pages, rec + (uint64_t)D * D * 4 + (uint64_t)e * 2, a.status));
+            if (dst) *dst = halo[e];
+        }
+    } else if (warp >= kSolveWarp0 && warp < kSeqWarp0) {
+        // ------------------------------------------------------------------ solve warpgroup
+        // T of chunk lc (G | P from TMEM, triangular solve) and the WK'^T operand, while the conv
+        // warpgroup already prepares chunk lc + 1.
+        const int t = tid - kSolveWarp0 * 32;         // 0..127, TMEM lane
+        float *Msc = reinterpret_cast<float *>(sm + OFF_WK);
+        volatile int *pflag = wg_flag + 2;
+        for (int lc = 0; lc < nchunks; ++lc) {
+            const int b = lc & 1;
             // ---------------- P2: G | P from TMEM, T = (I + A)^{-1} Diag(beta)
-            if (!wg_wait(S, B_GP + b, par(lc), t, kBarPrep, pflag)) break;
-            if (lc >= 1 && !wg_wait(S, B_M3 + ((lc - 1) & 1), par(lc - 1), t, kBarPrep, pflag)) break;   // scratch free
+            if (!wg_wait(S, B_GP + b, par(lc), t, kBarSolve, pflag)) break;
+            if (!wg_wait(S, B_P1 + b, par(lc), t, kBarSolve, pflag)) break;              // beta, diag of P
+            if (lc >= 1 && !wg_wait(S, B_M3 + ((lc - 1) & 1), par(lc - 1), t, kBarSolve, pflag)) break;   // scratch free
+            if (lc >= 2 && !wg_wait(S, B_M4 + b, par(lc - 2), t, kBarSolve, pflag)) break;   // P slot free
             ptx::tc_fence_after();
             {
                 float g0[32], g1[32];
-                const uint32_t ta = tbase + ((uint32_t)((warp - kPrepWarp0) * 32) << 16) + COL_GP;
+                const uint32_t ta = tbase + ((uint32_t)((warp - kSolveWarp0) * 32) << 16) + COL_GP;
                 ptx::tmem_ld32(ta, g0);
                 ptx::tmem_ld32(ta + 32, g1);
                 ptx::tmem_wait_ld();
@@ -591,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // P row r = lower_incl(Qt' Kb^T), with the exact fp32 diagonal
                     const int r = t - C;
                     uint8_t *pr = sm + OFF_P + b * 8192;
-                    const float pd = reinterpret_cast<const float *>(sm + OFF_PD)[r];
+                    const float pd = reinterpret_cast<const float *>(sm + OFF_PD)[b * 64 + r];
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
                         uint4 v;
@@ -609,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             ptx::tc_fence_before();
-            named_bar(kBarPrep, 128);
+            named_bar(kBarSolve, 128);
             // level 0: invert the four 16x16 diagonal blocks, one row per thread.  Row x of the
             // inverse solves x (I + A_bb) = e_r; eliminating from the last row upward needs only
             // rows of A_bb, which every thread of the block reads (broadcast), and no predicate:
@@ -635,20 +657,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < mm; ++c) x[c] = fmaf(-xm, av[c], x[c]);
                 }
-                named_bar(kBarPrep + 2, 64);
+                named_bar(kBarSolveHalf, 64);
                 float4 *row = reinterpret_cast<float4 *>(Msc + r * 64);
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     row[(bb * 4 + q) ^ (r & 7)] = make_float4(x[q * 4], x[q * 4 + 1], x[q * 4 + 2], x[q * 4 + 3]);
             }
-            named_bar(kBarPrep, 128);
+            named_bar(kBarSolve, 128);
             // Off-diagonal blocks of Inv = (I + A)^{-1}, in 32 x 32 halves (tf32 mma.sync, one
             // warp per 16 x 16 block).  With J0, J1 the inverses of the two diagonal 32 x 32 blocks
             // and B the lower-left 32 x 32 block of A:
             //   J0 = [[I00, 0], [-I11 A10 I00, I11]],  J1 likewise from blocks 2, 3,
             //   lower-left of Inv = -J1 (B J0).
             {
-                const int pw = warp - kPrepWarp0;
+                const int pw = warp - kSolveWarp0;
                 const float zero4[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 // step A: X10 = -I11 (A10 I00) on warp 0, X32 = -I33 (A32 I22) on warp 1
                 if (pw < 2) {
@@ -663,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     blk_store(Msc, i, j, acc2, -1.f, lane);
                 }
-                named_bar(kBarPrep, 128);
+                named_bar(kBarSolve, 128);
                 // step B1: Y = B J0, block (bi, bj) = (2 + pw / 2, pw % 2) per warp
                 const int bi = 2 + (pw >> 1), bj = pw & 1;
                 float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -673,9 +695,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     blk_mma(y, Msc, bi, 1, 1, lane);     // A_i1 I11
                 }
-                named_bar(kBarPrep, 128);
+                named_bar(kBarSolve, 128);
                 blk_store(Msc, bi, bj, y, 1.f, lane);
-                named_bar(kBarPrep, 128);
+                named_bar(kBarSolve, 128);
                 // step B2: Z = -J1 Y
                 float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 if (bi == 2) {
@@ -684,11 +706,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     blk_mma(z, Msc, 3, 2, bj, lane);     // X32 Y2j
                     blk_mma(z, Msc, 3, 3, bj, lane);     // I33 Y3j
                 }
-                named_bar(kBarPrep, 128);
+                named_bar(kBarSolve, 128);
                 blk_store(Msc, bi, bj, z, -1.f, lane);
                 (void)zero4;
             }
-            named_bar(kBarPrep, 128);
+            named_bar(kBarSolve, 128);
             // T = Inv Diag(beta) -> bf16 operand [r][s]
             if (t < C) {
                 const int r = t;
@@ -716,14 +738,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             ptx::fence_proxy_async_smem();
-            named_bar(kBarPrep, 128);
+            named_bar(kBarSolve, 128);
             if (t == 0) ptx::mbar_arrive(&S.bar[B_T + b]);
             // ---------------- P3: WK'^T from TMEM -> bf16 operand rows (row = key channel)
-            if (!wg_wait(S, B_M2 + b, par(lc), t, kBarPrep, pflag)) break;
+            if (!wg_wait(S, B_M2 + b, par(lc), t, kBarSolve, pflag)) break;
             ptx::tc_fence_after();
             {
                 float w0[32], w1[32];
-                const uint32_t ta = tbase + ((uint32_t)((warp - kPrepWarp0) * 32) << 16) + COL_WK;
+                const uint32_t ta = tbase + ((uint32_t)((warp - kSolveWarp0) * 32) << 16) + COL_WK;
                 ptx::tmem_ld32(ta, w0);
                 ptx::tmem_ld32(ta + 32, w1);
                 ptx::tmem_wait_ld();
@@ -742,14 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            named_bar(kBarPrep, 128);
+            named_bar(kBarSolve, 128);
             if (t == 0) ptx::mbar_arrive(&S.bar[B_WK + b]);
-        }
-        // final conv window into the active object
-        for (int e = t; e < 9 * D; e += 128) {
-            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(
-                obj_addr(a.pool, act_pages, rec + (uint64_t)D * D * 4 + (uint64_t)e * 2, a.status));
-            if (dst) *dst = halo[e];
         }
     } else if (warp >= kSeqWarp0) {
         // ------------------------------------------------------------------ seq warpgroup
@@ -843,26 +859,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!(ok = wg_wait(S, B_P1 + b, par(lc), j, kBarSeq, sflag))) break;
             const float *gcb = gC + b * 128;
-            for (int i0 = 0; i0 < D; i0 += 32) {
-                float v[32];
+            for (int i0 = 0; i0 < D; i0 += 64) {
+                float v[32], w[32], pk[32];
                 ptx::tmem_ld32(tbase + lanes + COL_S + i0, v);
+                ptx::tmem_ld32(tbase + lanes + COL_S + i0 + 32, w);
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int ii = 0; ii < 32; ++ii) v[ii] *= gcb[i0 + ii];
-                ptx::tmem_st32(tbase + lanes + COL_S + i0, v);
-                // bf16 row j of (Gamma S)^T: columns i0..i0+31 = 64 bytes
-                uint8_t *row = sm + OFF_SB + (i0 >> 6) * 16384;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint4 pk;
-                    uint32_t *pp = reinterpret_cast<uint32_t *>(&pk);
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) pp[q2] = pack_bf16x2(v[ch * 8 + 2 * q2], v[ch * 8 + 2 * q2 + 1]);
-                    *reinterpret_cast<uint4 *>(row + ptx::sw128_off(j, ((i0 & 63) * 2) + ch * 16)) = pk;
+                for (int ii = 0; ii < 32; ++ii) {
+                    v[ii] *= gcb[i0 + ii];
+                    w[ii] *= gcb[i0 + 32 + ii];
                 }
+                ptx::tmem_st32(tbase + lanes + COL_S + i0, v);
+                ptx::tmem_st32(tbase + lanes + COL_S + i0 + 32, w);
+                // bf16 row j of (Gamma S)^T, two values per TMEM column: columns i0/2 .. i0/2 + 31
+#pragma unroll
+                for (int q2 = 0; q2 < 16; ++q2) {
+                    pk[q2] = __uint_as_float(pack_bf16x2(v[2 * q2], v[2 * q2 + 1]));
+                    pk[16 + q2] = __uint_as_float(pack_bf16x2(w[2 * q2], w[2 * q2 + 1]));
+                }
+                ptx::tmem_st32(tbase + lanes + COL_SA + (i0 >> 1), pk);
             }
             ptx::tmem_wait_st();
-            ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             named_bar(kBarSeq, 128);
             if (j == 0) ptx::mbar_arrive(&S.bar[B_SB + b]);

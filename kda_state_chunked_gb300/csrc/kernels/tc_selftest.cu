@@ -21,7 +21,7 @@ struct SelftestArgs {
     const __nv_bfloat16 *A;   // [128][K]
     const __nv_bfloat16 *B;   // [K][N]
     float *D;                 // [128][N]
-    int K, N, a_mn, b_mn, neg, use_tma;
+    int K, N, a_mn, b_mn, neg, use_tma, a_tmem;
     int *err;
 };
 
@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(128, 1) mma_selftest_kernel(SelftestArgs a, co
         err_s = 0;
     }
     if (warp == 0) {
-        ptx::tmem_alloc(&tmem_base, 128);
+        ptx::tmem_alloc(&tmem_base, 256);
         ptx::tmem_relinquish();
     }
     __syncthreads();
@@ -69,6 +69,24 @@ __global__ void __launch_bounds__(128, 1) mma_selftest_kernel(SelftestArgs a, co
         else off = (k / 64) * (N * 128) + ptx::sw128_off(n, (k % 64) * 2);
         *reinterpret_cast<__nv_bfloat16 *>(sB + off) = a.B[e];
     }
+    if (a.a_tmem) {
+        // A into TMEM columns 128.. : thread m holds row m, bf16 pairs packed along K.
+        __syncthreads();
+        const int m = warp * 32 + (tid & 31);
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        for (int c0 = 0; c0 < K / 2; c0 += 32) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int k = 2 * (c0 + i);
+                __nv_bfloat162 pr = __halves2bfloat162(a.A[(int64_t)m * K + k], a.A[(int64_t)m * K + k + 1]);
+                v[i] = __uint_as_float(*reinterpret_cast<uint32_t *>(&pr));
+            }
+            if (c0 < K / 2) ptx::tmem_st32(tmem_base + lane_base + 128 + c0, v);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+    }
     ptx::fence_proxy_async_smem();
     __syncthreads();
     if (a.use_tma && !ptx::mbar_wait(&bar_tma, 0, &err_s)) {
@@ -85,7 +103,8 @@ __global__ void __launch_bounds__(128, 1) mma_selftest_kernel(SelftestArgs a, co
                 else ad = ptx::sdesc_sw128(aBase + (s / 4) * (kM * 128) + (s % 4) * 32, 16, 1024);
                 if (a.b_mn) bd = ptx::sdesc_sw128(bBase + s * 2048, K * 128, 1024);
                 else bd = ptx::sdesc_sw128(bBase + (s / 4) * (N * 128) + (s % 4) * 32, 16, 1024);
-                ptx::mma_bf16(tmem_base, ad, bd, idesc, (pass > 0 || s > 0) ? 1u : 0u);
+                if (a.a_tmem) ptx::mma_bf16_ta(tmem_base, tmem_base + 128 + s * 8, bd, idesc, (pass > 0 || s > 0) ? 1u : 0u);
+                else ptx::mma_bf16(tmem_base, ad, bd, idesc, (pass > 0 || s > 0) ? 1u : 0u);
             }
         }
         ptx::mma_commit(&bar_mma);
@@ -109,7 +128,7 @@ __global__ void __launch_bounds__(128, 1) mma_selftest_kernel(SelftestArgs a, co
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 0) ptx::tmem_dealloc(tmem_base, 128);
+    if (warp == 0) ptx::tmem_dealloc(tmem_base, 256);
 }
 
 }  // namespace
@@ -144,13 +163,16 @@ int encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint
 extern "C" int kda_internal_mma_selftest(const void *A, const void *B, float *D, int K, int N, int a_mn, int b_mn,
                                          int neg, int use_tma, int *err_dev, void *stream) {
     using namespace kda;
+    // use_tma == 2 selects an A operand read from TMEM instead of shared memory
+    const int a_tmem = use_tma == 2 ? 1 : 0;
+    if (a_tmem) use_tma = 0;
     if ((K != 64 && K != 128) || (N != 64 && N != 128) || !A || !B || !D || !err_dev) return -1;
-    if (use_tma && a_mn) return -1;
+    if ((use_tma || a_tmem) && a_mn) return -1;
     CUtensorMap tm;
     std::memset(&tm, 0, sizeof(tm));
     if (use_tma && encode_tmap_bf16_2d(&tm, A, (uint64_t)K, 128, (uint64_t)K * 2, 64, 128) != 0) return -3;
     SelftestArgs a{static_cast<const __nv_bfloat16 *>(A), static_cast<const __nv_bfloat16 *>(B), D, K, N, a_mn,
-                   b_mn, neg, use_tma, err_dev};
+                   b_mn, neg, use_tma, a_tmem, err_dev};
     const int smem = 65536 + 1024;
     auto kern = mma_selftest_kernel;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -4;

@@ -46,3 +46,9 @@ def test_mma_negate_a(a_mn, b_mn):
 @pytest.mark.parametrize("K,N", [(64, 64), (128, 128)])
 def test_mma_tma_loaded_operand(K, N):
     assert _run(K, N, 0, 0, 0, 1) < 1e-5
+
+
+@pytest.mark.parametrize("K,N,b_mn,neg", [(64, 64, 0, 0), (128, 64, 1, 1), (128, 128, 0, 0), (64, 128, 1, 0)])
+def test_mma_a_operand_from_tmem(K, N, b_mn, neg):
+    """A read from tensor memory (bf16 pairs packed along K per 32-bit column)."""
+    assert _run(K, N, 0, b_mn, neg, 2) < 1e-5
