@@ -29,6 +29,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "KDA prefill tokens/s and decode step µs at B=256; % of tensor/HBM roofline"
 WORKLOAD = "batched"
+# sources of the dominant (prefill) kernel, for matching committed ncu traffic to the code
+PREFILL_SOURCES = ["kernels/prefill_tc.cu", "kernels/tc_common.cuh", "kernels/sm100_ptx.cuh",
+                   "kernels/common.cuh", "kda_internal.h"]
 
 
 # --------------------------------------------------------------------------- helpers
@@ -45,10 +48,17 @@ def _peaks():
 
 
 def _kernel_source_hash(files):
+    """Hash of the kernel's sources with comments and blank lines removed (a comment edit
+    does not change the kernel the counters were taken on)."""
+    import re
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "kda_state_chunked_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "kda_state_chunked_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+        h.update("\n".join(lines).encode())
     return h.hexdigest()[:16]
 
 
@@ -310,6 +320,24 @@ def _oracle_sample(toks_cpu_fn, threads_note=True):
                       f"fp64 token recurrence + 4 checkpoints ({sec:.2f} s wall)"}
 
 
+# --------------------------------------------------------------------------- replicas
+def _max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """Max of a per-rank number over all ranks (NCCL wants the tensor on the GPU)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0].item())
+
+
+def _aggregate(units_per_rank_step: int, steps: int, total_ms_max: float, world: int):
+    """Whole-job throughput: all ranks' units over the slowest rank's time (weak scaling)."""
+    ms = total_ms_max / steps
+    return ms, units_per_rank_step * world / (ms * 1e-3)
+
+
 # --------------------------------------------------------------------------- arms
 def run_ours(args, rank, world, dev):
     import torch
@@ -328,13 +356,10 @@ def run_ours(args, rank, world, dev):
         total_ms, per = _time_steps(bench.step, args.steps, args.warmup, stream, min_warm_s=1.0)
     rc, bits = bench.kda.kda_sync_status(bench.status)
     assert rc == bench.kda.KDA_OK, f"device status {bits}"
-    t = torch.tensor([total_ms], dtype=torch.float64)
+    total_ms = _max_over_ranks(total_ms, world, dev)
     if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
         dist.barrier()
-    ms_per_step = float(t[0]) / args.steps
-    tokens_per_step = bench.T_tot * world
-    value = tokens_per_step / (ms_per_step * 1e-3)
+    ms_per_step, value = _aggregate(bench.T_tot, args.steps, total_ms, world)
     launch_ms = statistics.mean(per)
     ab = bench.algorithmic_bytes()
     achieved = ab / (launch_ms * 1e-3) / 1e9
@@ -342,7 +367,7 @@ def run_ours(args, rank, world, dev):
             "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
             "kernel": "prefill", "algorithmic_bytes_per_launch": ab,
             "launch_ms": launch_ms,
-            "traffic": _traffic("prefill_batched", ["kernels/prefill_tc.cu"], 1.0),
+            "traffic": _traffic("prefill_batched", PREFILL_SOURCES, 1.0),
             "tensor": {"flops_per_launch": bench.algorithmic_flops(),
                        "achieved_tflops": bench.algorithmic_flops() / (launch_ms * 1e-3) / 1e12,
                        "peak_tflops": peaks["bf16_tflops"]}}
@@ -361,11 +386,10 @@ def run_ours(args, rank, world, dev):
         bench.step(dtoks)
         o_host.copy_(bench.o, non_blocking=True)
 
-    e2e_ms, _ = _time_steps(e2e_step, args.steps, args.warmup, stream)
-    te = torch.tensor([e2e_ms], dtype=torch.float64)
     if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = tokens_per_step / (float(te[0]) / args.steps * 1e-3)
+        dist.barrier()
+    e2e_ms, _ = _time_steps(e2e_step, args.steps, args.warmup, stream)
+    _, e2e_value = _aggregate(bench.T_tot, args.steps, _max_over_ranks(e2e_ms, world, dev), world)
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

@@ -22,10 +22,11 @@
 // A operand of the next contraction.  Decay is anchored at the chunk end, so no per-element
 // division is needed.
 //
-// Warp roles (12 warps): warp 0 issues TMA loads of the raw q, k, v, alpha tiles; warp 1 issues
-// all tcgen05.mma from one thread; warps 4-7 ("prep") do the conv, the decay scaling and the
-// triangular solve for the chunk ahead; warps 8-11 ("seq") run the state epilogues of the
-// current chunk (checkpoint stores, decay of S, W, outputs).  Every wait is bounded: on a
+// Warp roles (16 warps): warp 0 issues TMA loads of the raw q, k, v, alpha tiles; warp 1 issues
+// all tcgen05.mma from one thread; warps 4-7 ("conv") do the conv and the decay scaling of the
+// chunk ahead; warps 8-11 ("solve") do the triangular solve and the WK'^T operand; warps 12-15
+// ("seq") run the state epilogues of the current chunk (checkpoint stores, decay of S, W,
+// outputs).  The three warpgroups work on three consecutive chunks at once.  Every wait is bounded: on a
 // timeout the kernel records KDA_DEV_TIMEOUT, stops issuing work, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
