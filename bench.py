@@ -158,8 +158,7 @@ class BatchedPrefill:
         n_ck = sum(len(kda.kda_ckpt_positions(0, w.T, w.hash_block, w.stride, w.include_last))
                    for _ in range(w.nseq))
         self.n_ckpt = n_ck
-        self.ws = torch.empty(kda.kda_prefill_workspace_bytes(w.nseq, n_ck, self.P),
-                              dtype=torch.uint8, device=dev)
+        self.ws = kda.prefill_workspace(self.toks["q"], self.cu, self.start, n_ck, self.P)
         self.rec = kda.kda_record_bytes(w.d, self.dt)
 
     def step(self, toks=None, o=None):
@@ -228,7 +227,7 @@ def _decode_phase(dev, steps=64, warmup=3):
     setup_T = 512
     toks = workloads.make_tokens(w.nseq * setup_T, w.H, w.d, w.dtype, w.seed, dev)
     cu = [i * setup_T for i in range(w.nseq + 1)]
-    ws = torch.empty(kda.kda_prefill_workspace_bytes(w.nseq, 0, P), dtype=torch.uint8, device=dev)
+    ws = kda.prefill_workspace(toks["q"], cu, [0] * w.nseq, 0, P)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     o = torch.empty_like(toks["q"])
     kda.kda_prefill_varlen(pool, cu, [0] * w.nseq, [0] * w.nseq, toks["q"], toks["k"], toks["v"],

@@ -143,8 +143,19 @@ int kda_ckpt_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n
 
 /* ---------------------------------------------------------------- prefill ------------- */
 
-/* Workspace bytes kda_prefill_varlen needs for nseq sequences and n_ckpt checkpoints. */
-int64_t kda_prefill_workspace_bytes(int32_t nseq, int32_t n_ckpt, int32_t pages_per_object);
+/* Workspace bytes kda_prefill_varlen needs for this batch (the same arguments as that call):
+ *   H, d, dtype            heads, head dimension, token dtype
+ *   nseq, cu_seqlens, start_pos   host arrays as in kda_prefill_varlen (they may be NULL when
+ *                          the path for this shape needs metadata only: fp32 or d = 64)
+ *   n_ckpt, pages_per_object      the checkpoint count of the call and kda_object_pages()
+ * For bf16 with d = 128 the workspace also holds the chunk-operand images of the split
+ * tensor-core prefill: two slots of at most ~48 MiB of images each (one image of 90,624 B per
+ * (chunk, head) of a wave of chunks), plus the state handed between waves (64 KiB per
+ * (sequence, head), when there is more than one wave) and the final conv windows.  Returns
+ * the byte count, or KDA_EINVAL for a bad shape or inconsistent arrays. */
+int64_t kda_prefill_workspace_bytes(int32_t H, int32_t d, int32_t dtype, int32_t nseq,
+                                    const int32_t *cu_seqlens, const int64_t *start_pos,
+                                    int32_t n_ckpt, int32_t pages_per_object);
 
 /* Chunked varlen prefill (chunk = 64 tokens, chunks aligned to absolute positions).
  *   H, d, dtype      heads, head dimension (64 or 128), dtype of the token tensors
@@ -165,7 +176,8 @@ int64_t kda_prefill_workspace_bytes(int32_t nseq, int32_t n_ckpt, int32_t pages_
  *                    by kda_ckpt_plan): sequence ids ascending, positions ascending within
  *                    a sequence, each position p with start < p <= end and p % 64 == 0 or
  *                    p == end; ckpt_pages [n_ckpt * P] must be allocated pages
- *   workspace        device scratch of at least kda_prefill_workspace_bytes(); the call
+ *   workspace        device scratch (16-byte aligned) of at least
+ *                    kda_prefill_workspace_bytes() for the same batch; the call
  *                    writes metadata there (one async host-to-device copy)
  *   status_dev       device int32 status word (bits KDA_DEV_*), OR-ed by the kernel
  * The state checkpoint at p is S after tokens [0, p) with the raw tokens p-3, p-2, p-1 as

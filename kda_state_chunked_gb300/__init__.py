@@ -47,7 +47,7 @@ _SIGS = {
     "kda_ckpt_positions": (_I32, [_I64, _I64, _I32, _I32, _I32, _P, _I32]),
     "kda_ckpt_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _I32, _I32, _I32, _I32,
                                      _P, _P, _P, _P]),
-    "kda_prefill_workspace_bytes": (_I64, [_I32, _I32, _I32]),
+    "kda_prefill_workspace_bytes": (_I64, [_I32, _I32, _I32, _I32, _P, _P, _I32, _I32]),
     "kda_prefill_varlen": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                           _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _I64, _P, _P]),
     "kda_prefill_varlen_noalloc": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
@@ -242,9 +242,21 @@ def kda_ckpt_plan(pool: Pool, H: int, d: int, dtype: int, cu_seqlens, start_pos,
 
 
 # ------------------------------------------------------------------------------ prefill
-def kda_prefill_workspace_bytes(nseq: int, n_ckpt: int, pages_per_object: int) -> int:
-    return _check(lib().kda_prefill_workspace_bytes(nseq, n_ckpt, pages_per_object),
-                  "kda_prefill_workspace_bytes")
+def kda_prefill_workspace_bytes(H: int, d: int, dtype: int, cu_seqlens, start_pos, n_ckpt: int,
+                                pages_per_object: int) -> int:
+    """Workspace bytes of kda_prefill_varlen for this batch (host cu_seqlens / start_pos)."""
+    cu = _i32(cu_seqlens)
+    sp = _i64(start_pos)
+    return _check(lib().kda_prefill_workspace_bytes(H, d, dtype, len(cu) - 1, _ptr(cu), _ptr(sp), n_ckpt,
+                                                    pages_per_object), "kda_prefill_workspace_bytes")
+
+
+def prefill_workspace(q, cu_seqlens, start_pos, n_ckpt: int, pages_per_object: int):
+    """A device byte tensor sized for kda_prefill_varlen on this batch."""
+    import torch
+    T_tot, H, d = q.shape
+    nb = kda_prefill_workspace_bytes(H, d, dtype_of(q), cu_seqlens, start_pos, n_ckpt, pages_per_object)
+    return torch.empty(nb, dtype=torch.uint8, device=q.device)
 
 
 def kda_prefill_varlen(pool: Pool, cu_seqlens, start_pos, has_init, q, k, v, alpha, beta, conv_w,

@@ -53,10 +53,76 @@ int check_allocated(const kda_pool *p, const int32_t *ids, int64_t n) {
     return KDA_OK;
 }
 
-int64_t prefill_ws_bytes(int64_t nseq, int64_t nck, int64_t P) {
-    return align_up(nseq * (int64_t)sizeof(SeqMeta), 256) + align_up(nck * (int64_t)sizeof(CkptMeta), 256) +
-           align_up((nseq + nck) * P * 4, 256);
+// The split tensor-core prefill serves bf16 with d = 128; other shapes use one launch of the
+// fused (fp32: CUDA-core) kernel and need metadata only.
+bool split_applies(int32_t d, int32_t dtype) { return dtype == KDA_BF16 && d == 128; }
+
+int32_t chunks_of(int64_t start, int64_t len) {
+    return len > 0 ? (int32_t)((start + len - 1) / kda::kChunk - start / kda::kChunk + 1) : 0;
 }
+
+// Waves of `cw` chunks per chain: one slot of operand images (all chains' items of a wave)
+// stays near 48 MiB so that two slots fit in L2, with at least 8 chunks per wave to amortise
+// a chain launch.
+void make_split_plan(int32_t H, int32_t nseq, const int32_t *cu, const int64_t *start, kda::SplitPlan &pl) {
+    std::vector<int32_t> nch((size_t)nseq);
+    int32_t maxc = 0, nact = 0;
+    for (int32_t s = 0; s < nseq; ++s) {
+        nch[s] = chunks_of(start[s], (int64_t)cu[s + 1] - cu[s]);
+        maxc = std::max(maxc, nch[s]);
+        nact += nch[s] > 0;
+    }
+    pl = kda::SplitPlan();
+    if (maxc == 0) return;
+    const int64_t per_chunk = (int64_t)nact * H * kda::kImageBytes;
+    int64_t cw = ((int64_t)48 << 20) / per_chunk;
+    cw = std::max<int64_t>(cw, 8);
+    cw = std::min<int64_t>(cw, maxc);
+    pl.cw = (int32_t)cw;
+    pl.nwaves = (int32_t)((maxc + cw - 1) / cw);
+    pl.wave_seq_off.assign((size_t)pl.nwaves * nseq, -1);
+    for (int32_t w = 0; w < pl.nwaves; ++w) {
+        const int32_t b = (int32_t)pl.items.size();
+        pl.wave_begin.push_back(b);
+        for (int32_t s = 0; s < nseq; ++s) {
+            const int32_t l0 = w * pl.cw, l1 = std::min(nch[s], l0 + pl.cw);
+            if (l0 >= l1) continue;
+            pl.wave_seq_off[(size_t)w * nseq + s] = (int32_t)pl.items.size() - b;
+            for (int32_t lc = l0; lc < l1; ++lc) pl.items.push_back(kda::SplitItem{s, lc});
+        }
+        pl.slot_items = std::max<int64_t>(pl.slot_items, (int64_t)pl.items.size() - b);
+    }
+    pl.wave_begin.push_back((int32_t)pl.items.size());
+}
+
+// Workspace: [SeqMeta][CkptMeta][pages][split items][wave offsets] (the uploaded metadata),
+// then for the split path [operand images: 2 slots][wave state scratch][final windows].
+struct WsLayout {
+    int64_t o_ck = 0, o_pg = 0, o_items = 0, o_wso = 0, meta = 0;
+    int64_t o_img = 0, o_state = 0, o_win = 0, total = 0;
+};
+
+WsLayout ws_layout(int64_t H, int64_t nseq, int64_t nck, int64_t P, const kda::SplitPlan *pl) {
+    WsLayout L;
+    L.o_ck = align_up(nseq * (int64_t)sizeof(SeqMeta), 256);
+    L.o_pg = L.o_ck + align_up(nck * (int64_t)sizeof(CkptMeta), 256);
+    L.o_items = L.o_pg + align_up((nseq + nck) * P * 4, 256);
+    const int64_t nit = pl ? (int64_t)pl->items.size() : 0;
+    L.o_wso = L.o_items + align_up(nit * (int64_t)sizeof(kda::SplitItem), 256);
+    L.meta = L.o_wso + (pl ? (int64_t)pl->wave_seq_off.size() * 4 : 0);
+    L.total = L.meta;
+    if (pl) {
+        L.o_img = align_up(L.meta, 1024);
+        L.o_state = L.o_img + 2 * pl->slot_items * H * kda::kImageBytes;
+        const int64_t state = pl->nwaves > 1 ? nseq * H * 128 * 128 * 4 : 0;
+        L.o_win = L.o_state + state;
+        L.total = L.o_win + nseq * H * 9 * 128 * 2;
+    }
+    return L;
+}
+
+// Metadata-only workspace of the fused kernels (also the layout the allocation-free path uses).
+int64_t prefill_ws_bytes(int64_t nseq, int64_t nck, int64_t P) { return ws_layout(1, nseq, nck, P, nullptr).total; }
 
 int copy_objects(kda_pool *p, int32_t H, int32_t d, int32_t dtype, int32_t n, const int32_t *src,
                  const int32_t *dst, void *pool_base, void *ws, int64_t ws_bytes, int32_t *status,
@@ -153,9 +219,16 @@ int kda_ckpt_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n
     return KDA_OK;
 }
 
-int64_t kda_prefill_workspace_bytes(int32_t nseq, int32_t n_ckpt, int32_t pages_per_object) {
-    if (nseq < 0 || n_ckpt < 0 || pages_per_object <= 0) return KDA_EINVAL;
-    return prefill_ws_bytes(nseq, n_ckpt, pages_per_object);
+int64_t kda_prefill_workspace_bytes(int32_t H, int32_t d, int32_t dtype, int32_t nseq, const int32_t *cu_seqlens,
+                                    const int64_t *start_pos, int32_t n_ckpt, int32_t pages_per_object) {
+    if (!valid_shape(H, d, dtype) || nseq < 0 || n_ckpt < 0 || pages_per_object <= 0) return KDA_EINVAL;
+    if (!split_applies(d, dtype)) return prefill_ws_bytes(nseq, n_ckpt, pages_per_object);
+    if (nseq > 0 && (!cu_seqlens || !start_pos)) return KDA_EINVAL;
+    for (int32_t s = 0; s < nseq; ++s)
+        if (cu_seqlens[s + 1] < cu_seqlens[s] || start_pos[s] < 0) return KDA_EINVAL;
+    kda::SplitPlan pl;
+    make_split_plan(H, nseq, cu_seqlens, start_pos, pl);
+    return ws_layout(H, nseq, n_ckpt, pages_per_object, &pl).total;
 }
 
 int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t nseq,
@@ -178,7 +251,11 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
     if (T_tot > 0 && (!q || !k || !v || !alpha || !beta || !o)) return KDA_EINVAL;
     if ((uintptr_t)workspace % 16 != 0) return KDA_EINVAL;
     const int32_t P = kda_object_pages(pool, H, d, dtype);
-    if (ws_bytes < prefill_ws_bytes(nseq, n_ckpt, P)) return KDA_EINVAL;
+    const bool split = split_applies(d, dtype);
+    kda::SplitPlan plan;
+    if (split) make_split_plan(H, nseq, cu_seqlens, start_pos, plan);
+    const WsLayout L = ws_layout(H, nseq, n_ckpt, P, split ? &plan : nullptr);
+    if (ws_bytes < L.total) return KDA_EINVAL;
 
     std::vector<SeqMeta> seqs((size_t)nseq);
     std::vector<CkptMeta> cks((size_t)n_ckpt);
@@ -217,16 +294,19 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
     }
     if (ci != n_ckpt) return KDA_EINVAL;   // sequence ids not ascending or out of range
 
-    // One upload: [SeqMeta][CkptMeta][pages], each part 256-byte aligned.
-    const int64_t o_ck = align_up((int64_t)nseq * sizeof(SeqMeta), 256);
-    const int64_t o_pg = o_ck + align_up((int64_t)n_ckpt * sizeof(CkptMeta), 256);
-    const int64_t total = o_pg + (int64_t)pages.size() * 4;
-    std::vector<uint8_t> blob((size_t)total, 0);
+    // One upload of the metadata part of the workspace layout.
+    std::vector<uint8_t> blob((size_t)L.meta, 0);
     std::memcpy(blob.data(), seqs.data(), seqs.size() * sizeof(SeqMeta));
-    if (n_ckpt) std::memcpy(blob.data() + o_ck, cks.data(), cks.size() * sizeof(CkptMeta));
-    std::memcpy(blob.data() + o_pg, pages.data(), pages.size() * 4);
+    if (n_ckpt) std::memcpy(blob.data() + L.o_ck, cks.data(), cks.size() * sizeof(CkptMeta));
+    std::memcpy(blob.data() + L.o_pg, pages.data(), pages.size() * 4);
+    if (split) {
+        if (!plan.items.empty())
+            std::memcpy(blob.data() + L.o_items, plan.items.data(), plan.items.size() * sizeof(kda::SplitItem));
+        if (!plan.wave_seq_off.empty())
+            std::memcpy(blob.data() + L.o_wso, plan.wave_seq_off.data(), plan.wave_seq_off.size() * 4);
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int rc = kda::stage_upload(pool, blob.data(), (size_t)total, workspace, st);
+    int rc = kda::stage_upload(pool, blob.data(), (size_t)L.meta, workspace, st);
     if (rc != KDA_OK) return rc;
 
     kda::PrefillArgs a;
@@ -236,10 +316,21 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
     a.pool = pool_view(pool, pool_base, H, d, dtype);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     a.seqs = reinterpret_cast<const SeqMeta *>(ws);
-    a.ckpts = reinterpret_cast<const CkptMeta *>(ws + o_ck);
-    a.pages = reinterpret_cast<const int32_t *>(ws + o_pg);
+    a.ckpts = reinterpret_cast<const CkptMeta *>(ws + L.o_ck);
+    a.pages = reinterpret_cast<const int32_t *>(ws + L.o_pg);
     a.status = status_dev;
-    return kda::launch_prefill(a, st) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+    if (!split) return kda::launch_prefill(a, st) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+    kda::SplitArgs sa;
+    sa.p = a;
+    sa.items = reinterpret_cast<const kda::SplitItem *>(ws + L.o_items);
+    sa.wave_seq_off = reinterpret_cast<const int32_t *>(ws + L.o_wso);
+    sa.images = ws + L.o_img;
+    sa.slot_items = plan.slot_items;
+    sa.state_scr = reinterpret_cast<float *>(ws + L.o_state);
+    sa.win_scr = ws + L.o_win;
+    sa.cw = plan.cw;
+    sa.nwaves = plan.nwaves;
+    return kda::launch_prefill_split(sa, plan, st) == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
 int kda_decode_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B,

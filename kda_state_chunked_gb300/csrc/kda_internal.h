@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -55,6 +56,37 @@ struct PrefillArgs {
     int32_t *status;
 };
 
+// Split prefill (bf16, d = 128): a parallel chunk-preparation kernel writes one operand image
+// per (chunk, head) item, a sequential chain kernel consumes the images in chunk order.  The
+// chunks of every chain are processed in waves of `cw` local chunks; wave w's images live in
+// slot w % 2 of the image buffer.
+constexpr int64_t kImageBytes = 90624;   // Qt' 16 KiB | Kb 16 KiB | P 8 KiB | WK'^T 16 KiB | U 32 KiB | gamma_C 512 B
+
+struct SplitItem {
+    int32_t seq;   // sequence
+    int32_t lc;    // chunk index within the sequence's chain
+};
+
+struct SplitArgs {
+    PrefillArgs p;
+    const SplitItem *items;        // every wave's items, wave after wave
+    const int32_t *wave_seq_off;   // [nwaves][nseq]: index in its wave of item (s, w * cw), -1 if none
+    uint8_t *images;               // [2 slots][slot_items][H][kImageBytes]
+    int64_t slot_items;            // items one slot holds
+    float *state_scr;              // [nseq][H][d][d] state handed from one wave to the next
+    uint8_t *win_scr;              // [nseq][H][3][3d] bf16 final conv window
+    int32_t cw, nwaves;
+};
+
+// Host-side wave plan of a split prefill call.
+struct SplitPlan {
+    int32_t cw = 1, nwaves = 0;
+    int64_t slot_items = 0;
+    std::vector<SplitItem> items;
+    std::vector<int32_t> wave_begin;     // [nwaves + 1] offsets into items
+    std::vector<int32_t> wave_seq_off;   // [nwaves * nseq]
+};
+
 struct DecodeArgs {
     int32_t H, d, dtype, B;
     const void *q, *k, *v, *alpha, *beta;
@@ -75,6 +107,7 @@ struct CopyArgs {
 };
 
 // Kernel launchers (defined in the .cu files).
+cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_supported(const PrefillArgs &a);

@@ -1,0 +1,943 @@
+// Split chunked prefill on the 5th-generation tensor cores (bf16 inputs, d = 128).
+//
+// It computes the same result as the fused kernel: the token recurrence
+// S_t = (I - beta k k^T) Diag(alpha) S_{t-1} + beta k v^T, o_t = S_t^T q_t after the width-4
+// causal conv on q | k | v ("Lesson 01 · Architecture map", §两种 Attention，两种状态), grouped
+// into chunks of 64 tokens that each act on S as one affine map ("KIMI K3 경량 복제에서 본 KDA의
+// AI 인프라 과제", §0x01 1.3), with checkpoints of (S, conv window) written at listed chunk ends
+// ("Cache de préfixe hybride KDA–MLA", §Le fonctionnement du prefill).
+//
+// Everything of a chunk that does not depend on the state runs in parallel over all
+// (chunk, head) items; only the state contractions remain sequential per chain:
+//
+//   chunk_prep_kernel (one CTA per item, 160 threads, 2 CTAs per SM)
+//     conv, decay factors, Kt' = k gamma_r/gamma_C, Qt' = q gamma_r/gamma_C, Kb = k gamma_C/gamma_r,
+//     G | P = [Kt'; Qt'] Kb^T (tcgen05), T = (I + Diag(beta) strict_lower(G))^{-1} Diag(beta)
+//     (CUDA cores + tf32 mma.sync), WK'^T = Kt'^T T^T and U^T = V^T T^T (tcgen05), and writes one
+//     operand image per item: Qt', Kb, P, WK'^T (bf16, 128-byte swizzled, as the chain kernel's
+//     MMAs read them), U (fp32) and gamma_C.  Conv windows of checkpoints are written here.
+//
+//   chain_kernel (one CTA per (sequence, head), 256 threads)
+//     S^T resident in TMEM; per chunk: S <- Gamma_C S (+ bf16 copy as the next A operand),
+//     O^T = (Gamma_C S)^T Qt'^T + W^T P^T, W^T = U^T - (Gamma_C S)^T WK'^T, S^T += W^T Kb,
+//     checkpoint states and outputs.  Images arrive by bulk copies, double-buffered.
+//
+// The chunks of every chain are processed in waves of `cw` chunks; a wave's images use one of
+// two slots, so the prep of wave w + 1 may run while the chains consume wave w.  The state is
+// handed from one wave to the next through a small fp32 scratch.  Every wait is bounded: on a
+// timeout a kernel records KDA_DEV_TIMEOUT, stops issuing work, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+#include "tc_common.cuh"
+
+namespace kda {
+
+int encode_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_rows);
+
+namespace {
+
+using namespace tcx;
+
+constexpr int D = 128;
+constexpr int C = kChunk;   // 64
+
+// Operand image of one (chunk, head) item (byte offsets; every operand 1024-byte aligned).
+constexpr uint32_t IMG_Q = 0;        // Qt'   [2 kb][64 rows][128 B]   K-major B operand
+constexpr uint32_t IMG_KB = 16384;   // Kb    [2 kb][64 rows][128 B]   MN-major B operand
+constexpr uint32_t IMG_P = 32768;    // P     [64 rows][128 B]         K-major B operand
+constexpr uint32_t IMG_WK = 40960;   // WK'^T [128 rows][128 B]        MN-major B operand
+constexpr uint32_t IMG_U = 57344;    // U     fp32 [64 chunk rows][128 value channels]
+constexpr uint32_t IMG_GC = 90112;   // gamma_C fp32 [128]
+static_assert(IMG_GC + 512 == kImageBytes, "image layout");
+
+__device__ __forceinline__ uint8_t *image_addr(const SplitArgs &a, int wave, int64_t idx_in_wave, int h) {
+    const int64_t slot = wave & 1;
+    return a.images + ((slot * a.slot_items + idx_in_wave) * a.p.H + h) * kImageBytes;
+}
+
+// Index of the checkpoint of sequence m at absolute position pos, or -1 (positions ascend).
+__device__ __forceinline__ int find_ckpt(const PrefillArgs &a, const SeqMeta &m, int64_t pos) {
+    int lo = 0, hi = m.ckpt_count;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a.ckpts[m.ckpt_begin + mid].pos < pos) lo = mid + 1;
+        else hi = mid;
+    }
+    return (lo < m.ckpt_count && a.ckpts[m.ckpt_begin + lo].pos == pos) ? m.ckpt_begin + lo : -1;
+}
+
+// ============================================================================ chunk prep
+constexpr int kAThreads = 160;   // warps 0-3 compute, warp 4 TMA + MMA + bulk stores
+
+constexpr uint32_t A_KQ = 0;        // [2 kb][128 rows: k 0-63 | q 64-127][128 B] -> Kt' | Qt'
+constexpr uint32_t A_V = 32768;     // [2 kb][64][128 B]  raw v -> V
+constexpr uint32_t A_AL = 49152;    // [2 kb][64][128 B]  raw alpha -> Kb -> fp32 solve scratch -> WK'^T
+constexpr uint32_t A_P = 65536;     // [64][128 B]        P
+constexpr uint32_t A_T = 73728;     // fp32 [64][32] diagonal partials, then T [64][128 B]
+constexpr uint32_t A_GC = 81920;    // float [128]  gamma_C
+constexpr uint32_t A_BS = 82432;    // float [64]   beta
+constexpr uint32_t A_PD = 82688;    // float [64]   exact diagonal of P
+constexpr uint32_t A_RED = 82944;   // float2 [2][64] half products of alpha
+constexpr uint32_t A_HALO = 83968;  // bf16 [3][384] conv window
+constexpr uint32_t A_BAR = 86272;   // mbarriers, flags
+constexpr uint32_t A_SMEM = A_BAR + 128 + 1024;
+constexpr int kAWg = 1, kAHalf = 2;   // named barriers (128 and 64 threads)
+
+enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_T, AB_M2, AB_WK, A_NBARS };
+
+__global__ void __launch_bounds__(kAThreads, 2)
+    chunk_prep_kernel(const SplitArgs a, int wave, int item0, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Shared S;
+    S.base = sm;
+    S.bar = reinterpret_cast<uint64_t *>(sm + A_BAR);
+    S.err = reinterpret_cast<volatile int *>(sm + A_BAR + 64);
+    S.tmem = reinterpret_cast<uint32_t *>(sm + A_BAR + 80);
+    volatile int *wflag = reinterpret_cast<volatile int *>(sm + A_BAR + 96);
+    float *gC = reinterpret_cast<float *>(sm + A_GC);
+    float *bs = reinterpret_cast<float *>(sm + A_BS);
+    float *pd = reinterpret_cast<float *>(sm + A_PD);
+    float2 *red = reinterpret_cast<float2 *>(sm + A_RED);
+    float *diag = reinterpret_cast<float *>(sm + A_T);
+    __nv_bfloat16 *halo = reinterpret_cast<__nv_bfloat16 *>(sm + A_HALO);
+
+    const PrefillArgs &pa = a.p;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = pa.H;
+    const int e = blockIdx.x / H, h = blockIdx.x % H;
+    const SplitItem it = a.items[item0 + e];
+    const SeqMeta m = pa.seqs[it.seq];
+    const int64_t start = m.start_pos, end = m.start_pos + m.len;
+    const int64_t c_first = start / C;
+    const int nchunks = (int)((end - 1) / C - c_first + 1);
+    const int64_t abs0 = (c_first + it.lc) * C;
+    const int r_first = start > abs0 ? (int)(start - abs0) : 0;
+    const int r_end = end - abs0 < C ? (int)(end - abs0) : C;
+    const uint64_t rec = (uint64_t)h * (uint64_t)pa.pool.rec_bytes;
+    const int32_t *act_pages = pa.pages + m.active_off;
+    uint8_t *img = image_addr(a, wave, e, h);
+    const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(pa.q);
+    const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(pa.k);
+    const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(pa.v);
+    const __nv_bfloat16 *betag = static_cast<const __nv_bfloat16 *>(pa.beta);
+
+    if (tid == 128) {
+        for (int i = 0; i < A_NBARS; ++i) ptx::mbar_init(&S.bar[i], 1);
+        *S.err = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 4) {
+        ptx::tmem_alloc(S.tmem, 128);
+        ptx::tmem_relinquish();
+    }
+    // Conv window before the first valid row: raw tokens from the input, or from the active
+    // object's window (positions before this call's start), or zeros.
+    const int64_t fv = abs0 + r_first;
+    for (int x = tid; x < 3 * 3 * D; x += kAThreads) {
+        const int u = x / (3 * D), c = x - u * 3 * D;
+        const int64_t pos = fv - 3 + u;
+        __nv_bfloat16 val = __float2bfloat16_rn(0.f);
+        if (pos >= start) {
+            const int64_t row = (int64_t)m.tok_begin + (pos - start);
+            const __nv_bfloat16 *src = c < D ? qg : (c < 2 * D ? kg : vg);
+            val = src[(row * H + h) * D + (c & (D - 1))];
+        } else if (m.has_init) {
+            const int slot = (int)(pos - start + 3);
+            const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(obj_addr(
+                pa.pool, act_pages, rec + (uint64_t)D * D * 4 + ((uint64_t)slot * 3 * D + c) * 2, pa.status));
+            if (p) val = *p;
+        }
+        halo[x] = val;
+    }
+    if (tid < C) {
+        const int64_t pos = abs0 + tid;
+        bs[tid] = (pos >= start && pos < end)
+                      ? __bfloat162float(betag[((int64_t)m.tok_begin + (pos - start)) * H + h])
+                      : 0.f;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tbase = *S.tmem;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------------ TMA / MMA / stores
+        if (lane == 0) {
+            bool m1 = false, m2 = false;
+            ptx::prefetch_tmap(&tm_q);
+            ptx::prefetch_tmap(&tm_k);
+            ptx::prefetch_tmap(&tm_v);
+            ptx::prefetch_tmap(&tm_a);
+            {
+                const int32_t y = (int32_t)((int64_t)m.tok_begin + (abs0 - start));
+                uint64_t *fb = &S.bar[AB_FULL];
+                ptx::mbar_arrive_expect_tx(fb, 4 * 2 * 64 * 128);
+                for (int kb = 0; kb < 2; ++kb) {
+                    const int32_t x = h * D + kb * 64;
+                    ptx::tma_load_2d(sm + A_KQ + kb * 16384, &tm_k, fb, x, y);
+                    ptx::tma_load_2d(sm + A_KQ + kb * 16384 + 8192, &tm_q, fb, x, y);
+                    ptx::tma_load_2d(sm + A_V + kb * 8192, &tm_v, fb, x, y);
+                    ptx::tma_load_2d(sm + A_AL + kb * 8192, &tm_a, fb, x, y);
+                }
+            }
+            const uint32_t sbase = ptx::smem_u32(sm);
+            if (wait_bar(S, AB_P1, 0)) {
+                // M1: G | P = [Kt'; Qt'] Kb^T
+                ptx::tc_fence_after();
+                const uint32_t id_gp = ptx::idesc_bf16(128, 64, 0, 0);
+                for (int s = 0; s < 8; ++s) {
+                    const uint64_t ad = ptx::sdesc_sw128(sbase + A_KQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+                    const uint64_t bd = ptx::sdesc_sw128(sbase + A_AL + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024);
+                    ptx::mma_bf16(tbase, ad, bd, id_gp, s > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&S.bar[AB_GP]);
+                m1 = true;
+                // Qt' and Kb to the image; the Kb tile is reused once M1 and this copy have read it
+                ptx::bulk_store(img + IMG_Q, sm + A_KQ + 8192, 8192);
+                ptx::bulk_store(img + IMG_Q + 8192, sm + A_KQ + 16384 + 8192, 8192);
+                ptx::bulk_store(img + IMG_KB, sm + A_AL, 16384);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read0();
+                if (wait_bar(S, AB_GP, 0)) ptx::mbar_arrive(&S.bar[AB_KBF]);
+            }
+            if (!*S.err && wait_bar(S, AB_T, 0)) {
+                // M2: WK'^T = Kt'^T T^T (columns 0-63), U^T = V^T T^T (columns 64-127)
+                ptx::tc_fence_after();
+                const uint32_t id_m2 = ptx::idesc_bf16(128, 64, 1, 0);
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t bd = ptx::sdesc_sw128(sbase + A_T + s * 32, 16, 1024);
+                    ptx::mma_bf16(tbase, ptx::sdesc_sw128(sbase + A_KQ + s * 2048, 16384, 1024), bd, id_m2,
+                                  s > 0 ? 1u : 0u);
+                    ptx::mma_bf16(tbase + 64, ptx::sdesc_sw128(sbase + A_V + s * 2048, 8192, 1024), bd, id_m2,
+                                  s > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&S.bar[AB_M2]);
+                m2 = true;
+                ptx::bulk_store(img + IMG_P, sm + A_P, 8192);
+                ptx::bulk_commit();
+            }
+            if (!*S.err && wait_bar(S, AB_WK, 0)) {
+                ptx::bulk_store(img + IMG_WK, sm + A_AL, 16384);
+                ptx::bulk_commit();
+            }
+            ptx::bulk_wait0();
+            if (*S.err) {
+                // leave nothing in flight: the tile loads and any issued MMA
+                uint32_t n = 0;
+                while (!ptx::mbar_try_wait(&S.bar[AB_FULL], 0) && n < ptx::kSpinLimit) ++n;
+                n = 0;
+                while (m1 && !ptx::mbar_try_wait(&S.bar[AB_GP], 0) && n < ptx::kSpinLimit) ++n;
+                n = 0;
+                while (m2 && !ptx::mbar_try_wait(&S.bar[AB_M2], 0) && n < ptx::kSpinLimit) ++n;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ compute warpgroup
+        const int t = tid;                              // 0..127, TMEM lane
+        const int p = t & 63, hf = t >> 6;              // channel pair (2p, 2p+1), row half
+        const int c0 = 2 * p, kb = c0 >> 6, cb = (c0 & 63) * 2;
+        const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+        do {
+            float wq[2][4], wk[2][4], wv[2][4];
+#pragma unroll
+            for (int ee = 0; ee < 2; ++ee)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    wq[ee][j] = pa.conv_w[((int64_t)h * 3 * D + c0 + ee) * 4 + j];
+                    wk[ee][j] = pa.conv_w[((int64_t)h * 3 * D + D + c0 + ee) * 4 + j];
+                    wv[ee][j] = pa.conv_w[((int64_t)h * 3 * D + 2 * D + c0 + ee) * 4 + j];
+                }
+            if (!wg_wait(S, AB_FULL, 0, t, kAWg, wflag)) break;
+            // ---------------- conv, decay, scaled operands (in place)
+            uint8_t *const qrow = sm + A_KQ + kb * 16384 + 8192, *const krow = sm + A_KQ + kb * 16384;
+            uint8_t *const vrow = sm + A_V + kb * 8192, *const arow = sm + A_AL + kb * 8192;
+            float2 wqv[3], wkv[3], wvv[3];
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+                wqv[u] = make_float2(__bfloat162float(halo[u * 384 + c0]), __bfloat162float(halo[u * 384 + c0 + 1]));
+                wkv[u] = make_float2(__bfloat162float(halo[u * 384 + D + c0]), __bfloat162float(halo[u * 384 + D + c0 + 1]));
+                wvv[u] = make_float2(__bfloat162float(halo[u * 384 + 2 * D + c0]),
+                                     __bfloat162float(halo[u * 384 + 2 * D + c0 + 1]));
+            }
+            // the second half starts after the last (up to three) valid rows below row 32
+            if (hf == 1) {
+                const int hi = r_end < 32 ? r_end : 32;
+                const int lo = (hi - 3) > r_first ? (hi - 3) : r_first;
+                for (int r = lo; r < hi; ++r) {
+                    const uint32_t off = ptx::sw128_off(r, cb);
+                    const float2 xq = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qrow + off));
+                    const float2 xk = bf2_to_f2(*reinterpret_cast<const uint32_t *>(krow + off));
+                    const float2 xv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(vrow + off));
+                    wqv[0] = wqv[1]; wqv[1] = wqv[2]; wqv[2] = xq;
+                    wkv[0] = wkv[1]; wkv[1] = wkv[2]; wkv[2] = xk;
+                    wvv[0] = wvv[1]; wvv[1] = wvv[2]; wvv[2] = xv;
+                }
+            }
+            float2 ap[4] = {make_float2(1.f, 1.f), make_float2(1.f, 1.f), make_float2(1.f, 1.f), make_float2(1.f, 1.f)};
+#pragma unroll 8
+            for (int rr = 0; rr < 32; ++rr) {
+                const int r = hf * 32 + rr;
+                const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(arow + ptx::sw128_off(r, cb)));
+                const bool valid = r >= r_first && r < r_end;
+                ap[rr & 3].x *= valid ? al.x : 1.f;
+                ap[rr & 3].y *= valid ? al.y : 1.f;
+            }
+            red[hf * 64 + p] = make_float2((ap[0].x * ap[1].x) * (ap[2].x * ap[3].x), (ap[0].y * ap[1].y) * (ap[2].y * ap[3].y));
+            named_bar(kAWg, 128);
+            const float2 h0 = red[p], h1 = red[64 + p];
+            const float gCx = h0.x * h1.x, gCy = h0.y * h1.y;
+            const float icx = 1.f / gCx, icy = 1.f / gCy;
+            if (hf == 0) {
+                gC[c0] = gCx;
+                gC[c0 + 1] = gCy;
+            }
+            float gx = hf ? h0.x : 1.f, gy = hf ? h0.y : 1.f;
+            uint32_t swz[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) swz[u] = ptx::sw128_off(u, cb);
+            // One row: conv, running decay, bf16 operands written in place (Kb over the alpha
+            // tile); the pair-summed share of the diagonal q.k of the row goes to `diag`.
+            auto row_proc = [&](int r, uint32_t off, float2 xq, float2 xk, float2 xv, float2 al, bool valid) {
+                uint32_t oq = 0, ok = 0, okb = 0, ov = 0;
+                float dpart = 0.f;
+                if (valid) {
+                    const float qb0 = wq[0][0] * wqv[0].x + wq[0][1] * wqv[1].x + wq[0][2] * wqv[2].x + wq[0][3] * xq.x;
+                    const float qb1 = wq[1][0] * wqv[0].y + wq[1][1] * wqv[1].y + wq[1][2] * wqv[2].y + wq[1][3] * xq.y;
+                    const float kb0 = wk[0][0] * wkv[0].x + wk[0][1] * wkv[1].x + wk[0][2] * wkv[2].x + wk[0][3] * xk.x;
+                    const float kb1 = wk[1][0] * wkv[0].y + wk[1][1] * wkv[1].y + wk[1][2] * wkv[2].y + wk[1][3] * xk.y;
+                    const float vb0 = wv[0][0] * wvv[0].x + wv[0][1] * wvv[1].x + wv[0][2] * wvv[2].x + wv[0][3] * xv.x;
+                    const float vb1 = wv[1][0] * wvv[0].y + wv[1][1] * wvv[1].y + wv[1][2] * wvv[2].y + wv[1][3] * xv.y;
+                    wqv[0] = wqv[1]; wqv[1] = wqv[2]; wqv[2] = xq;
+                    wkv[0] = wkv[1]; wkv[1] = wkv[2]; wkv[2] = xk;
+                    wvv[0] = wvv[1]; wvv[1] = wvv[2]; wvv[2] = xv;
+                    gx *= al.x;
+                    gy *= al.y;
+                    dpart = qb0 * kb0 + qb1 * kb1;
+                    const float sx = gx * icx, sy = gy * icy;      // gamma_r / gamma_C
+                    oq = pack_bf16x2(qb0 * sx, qb1 * sy);
+                    ok = pack_bf16x2(kb0 * sx, kb1 * sy);
+                    okb = pack_bf16x2(kb0 * rcp_approx(sx), kb1 * rcp_approx(sy));
+                    ov = pack_bf16x2(vb0, vb1);
+                }
+                const float dsum = dpart + __shfl_xor_sync(0xffffffffu, dpart, 1);
+                if ((lane & 1) == 0) diag[r * 32 + (p >> 1)] = dsum;
+                *reinterpret_cast<uint32_t *>(qrow + off) = oq;
+                *reinterpret_cast<uint32_t *>(krow + off) = ok;
+                *reinterpret_cast<uint32_t *>(arow + off) = okb;
+                *reinterpret_cast<uint32_t *>(vrow + off) = ov;
+            };
+            if (r_first == 0 && r_end == C) {
+#pragma unroll 1
+                for (int r0 = hf * 32; r0 < hf * 32 + 32; r0 += 8) {
+#pragma unroll
+                    for (int h4 = 0; h4 < 8; h4 += 4) {
+                        float2 xq[4], xk[4], xv[4], al[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint32_t off = (uint32_t)(r0 + h4 + u) * 128u + (swz[h4 + u] & 127u);
+                            xq[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qrow + off));
+                            xk[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(krow + off));
+                            xv[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(vrow + off));
+                            al[u] = bf2_to_f2(*reinterpret_cast<const uint32_t *>(arow + off));
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            row_proc(r0 + h4 + u, (uint32_t)(r0 + h4 + u) * 128u + (swz[h4 + u] & 127u), xq[u], xk[u],
+                                     xv[u], al[u], true);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int r = hf * 32; r < hf * 32 + 32; ++r) {
+                    const uint32_t off = ptx::sw128_off((uint32_t)r, cb);
+                    const float2 xq = bf2_to_f2(*reinterpret_cast<const uint32_t *>(qrow + off));
+                    const float2 xk = bf2_to_f2(*reinterpret_cast<const uint32_t *>(krow + off));
+                    const float2 xv = bf2_to_f2(*reinterpret_cast<const uint32_t *>(vrow + off));
+                    const float2 al = bf2_to_f2(*reinterpret_cast<const uint32_t *>(arow + off));
+                    row_proc(r, off, xq, xk, xv, al, r >= r_first && r < r_end);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            named_bar(kAWg, 128);
+            if (t == 0) ptx::mbar_arrive(&S.bar[AB_P1]);
+            // conv window after this chunk (the second half holds it)
+            if (hf == 1) {
+#pragma unroll
+                for (int u = 0; u < 3; ++u) {
+                    halo[u * 384 + c0] = __float2bfloat16_rn(wqv[u].x);
+                    halo[u * 384 + c0 + 1] = __float2bfloat16_rn(wqv[u].y);
+                    halo[u * 384 + D + c0] = __float2bfloat16_rn(wkv[u].x);
+                    halo[u * 384 + D + c0 + 1] = __float2bfloat16_rn(wkv[u].y);
+                    halo[u * 384 + 2 * D + c0] = __float2bfloat16_rn(wvv[u].x);
+                    halo[u * 384 + 2 * D + c0 + 1] = __float2bfloat16_rn(wvv[u].y);
+                }
+            }
+            // exact fp32 diagonal of P from the pair sums (rotated order: no bank conflicts)
+            if (t < C) {
+                float acc = 0.f;
+#pragma unroll 8
+                for (int s2 = 0; s2 < 32; ++s2) acc += diag[t * 32 + ((s2 + t) & 31)];
+                pd[t] = acc;
+            }
+            named_bar(kAWg, 128);
+            {
+                // window of a checkpoint ending here; the final window goes to the scratch
+                const int ck = find_ckpt(pa, m, abs0 + r_end);
+                const uint4 *src = reinterpret_cast<const uint4 *>(halo);
+                if (ck >= 0) {
+                    const int32_t *pg = pa.pages + pa.ckpts[ck].pages_off;
+                    for (int x = t; x < 9 * D * 2 / 16; x += 128) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            obj_addr(pa.pool, pg, rec + (uint64_t)D * D * 4 + (uint64_t)x * 16, pa.status));
+                        if (dst) *dst = src[x];
+                    }
+                }
+                if (it.lc == nchunks - 1) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.win_scr + ((int64_t)it.seq * H + h) * (9 * D * 2));
+                    for (int x = t; x < 9 * D * 2 / 16; x += 128) dst[x] = src[x];
+                }
+            }
+            // ---------------- G | P from TMEM; A = Diag(beta) strict_lower(G) into the solve scratch
+            if (!wg_wait(S, AB_GP, 0, t, kAWg, wflag)) break;
+            if (!wg_wait(S, AB_KBF, 0, t, kAWg, wflag)) break;
+            ptx::tc_fence_after();
+            float *Msc = reinterpret_cast<float *>(sm + A_AL);
+            {
+                float g0[32], g1[32];
+                ptx::tmem_ld32(tbase + lanes, g0);
+                ptx::tmem_ld32(tbase + lanes + 32, g1);
+                ptx::tmem_wait_ld();
+                if (t < C) {
+                    const int r = t;
+                    const float br = bs[r];
+                    float4 *row = reinterpret_cast<float4 *>(Msc + r * 64);
+#pragma unroll
+                    for (int c4 = 0; c4 < 16; ++c4) {
+                        float ev[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int s2 = c4 * 4 + u;
+                            const float gv = s2 < 32 ? g0[s2 & 31] : g1[s2 & 31];
+                            ev[u] = s2 < r ? br * gv : 0.f;
+                        }
+                        row[c4 ^ (r & 7)] = make_float4(ev[0], ev[1], ev[2], ev[3]);
+                    }
+                } else {
+                    const int r = t - C;
+                    const float pdr = pd[r];
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint4 v;
+                        uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            const int s0 = ch * 8 + q2 * 2;
+                            const float ga = s0 < 32 ? g0[s0 & 31] : g1[s0 & 31];
+                            const float gb = s0 + 1 < 32 ? g0[(s0 + 1) & 31] : g1[(s0 + 1) & 31];
+                            vv[q2] = pack_bf16x2(s0 < r ? ga : (s0 == r ? pdr : 0.f),
+                                                 s0 + 1 < r ? gb : (s0 + 1 == r ? pdr : 0.f));
+                        }
+                        *reinterpret_cast<uint4 *>(sm + A_P + ptx::sw128_off(r, ch * 16)) = v;
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            named_bar(kAWg, 128);
+            // ---------------- T = (I + A)^{-1} Diag(beta)
+            // level 0: the four 16 x 16 diagonal blocks, one row per thread (from the last row up)
+            if (t < C) {
+                const int r = t, bb = r >> 4, rr = r & 15;
+                float x[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) x[c] = c == rr ? 1.f : 0.f;
+#pragma unroll
+                for (int mm = 15; mm >= 1; --mm) {
+                    const int ar = bb * 16 + mm;
+                    const float4 *arow4 = reinterpret_cast<const float4 *>(Msc + ar * 64);
+                    float av[16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (q * 4 < mm) {
+                            const float4 v4 = arow4[(bb * 4 + q) ^ (ar & 7)];
+                            av[q * 4] = v4.x; av[q * 4 + 1] = v4.y; av[q * 4 + 2] = v4.z; av[q * 4 + 3] = v4.w;
+                        }
+                    }
+                    const float xm = x[mm];
+#pragma unroll
+                    for (int c = 0; c < mm; ++c) x[c] = fmaf(-xm, av[c], x[c]);
+                }
+                named_bar(kAHalf, 64);
+                float4 *row = reinterpret_cast<float4 *>(Msc + r * 64);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    row[(bb * 4 + q) ^ (r & 7)] = make_float4(x[q * 4], x[q * 4 + 1], x[q * 4 + 2], x[q * 4 + 3]);
+            }
+            named_bar(kAWg, 128);
+            // Off-diagonal blocks in 32 x 32 halves (tf32 mma.sync, one warp per 16 x 16 block):
+            //   J0 = [[I00, 0], [-I11 A10 I00, I11]], J1 likewise, lower-left of the inverse -J1 (B J0).
+            {
+                const int pw = warp;
+                if (pw < 2) {
+                    const int i = pw == 0 ? 1 : 3, j = i - 1;
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    blk_mma(acc, Msc, i, j, j, lane);
+                    __syncwarp();
+                    blk_store(Msc, i, j, acc, 1.f, lane);
+                    __syncwarp();
+                    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    blk_mma(acc2, Msc, i, i, j, lane);
+                    __syncwarp();
+                    blk_store(Msc, i, j, acc2, -1.f, lane);
+                }
+                named_bar(kAWg, 128);
+                const int bi = 2 + (pw >> 1), bj = pw & 1;
+                float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if (bj == 0) {
+                    blk_mma(y, Msc, bi, 0, 0, lane);
+                    blk_mma(y, Msc, bi, 1, 0, lane);
+                } else {
+                    blk_mma(y, Msc, bi, 1, 1, lane);
+                }
+                named_bar(kAWg, 128);
+                blk_store(Msc, bi, bj, y, 1.f, lane);
+                named_bar(kAWg, 128);
+                float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if (bi == 2) {
+                    blk_mma(z, Msc, 2, 2, bj, lane);
+                } else {
+                    blk_mma(z, Msc, 3, 2, bj, lane);
+                    blk_mma(z, Msc, 3, 3, bj, lane);
+                }
+                named_bar(kAWg, 128);
+                blk_store(Msc, bi, bj, z, -1.f, lane);
+            }
+            named_bar(kAWg, 128);
+            if (t < C) {
+                const int r = t;
+                const float4 *row = reinterpret_cast<const float4 *>(Msc + r * 64);
+                const float4 *b4 = reinterpret_cast<const float4 *>(bs);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    float ev[8];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int c4 = ch * 2 + h2;
+                        const float4 mv = row[c4 ^ (r & 7)];
+                        const float4 bv = b4[c4];
+                        ev[h2 * 4 + 0] = c4 * 4 + 0 <= r ? mv.x * bv.x : 0.f;
+                        ev[h2 * 4 + 1] = c4 * 4 + 1 <= r ? mv.y * bv.y : 0.f;
+                        ev[h2 * 4 + 2] = c4 * 4 + 2 <= r ? mv.z * bv.z : 0.f;
+                        ev[h2 * 4 + 3] = c4 * 4 + 3 <= r ? mv.w * bv.w : 0.f;
+                    }
+                    uint4 v;
+                    v.x = pack_bf16x2(ev[0], ev[1]);
+                    v.y = pack_bf16x2(ev[2], ev[3]);
+                    v.z = pack_bf16x2(ev[4], ev[5]);
+                    v.w = pack_bf16x2(ev[6], ev[7]);
+                    *reinterpret_cast<uint4 *>(sm + A_T + ptx::sw128_off(r, ch * 16)) = v;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            named_bar(kAWg, 128);
+            if (t == 0) ptx::mbar_arrive(&S.bar[AB_T]);
+            // ---------------- WK'^T (bf16 operand rows, staged for a bulk copy), U and gamma_C
+            if (!wg_wait(S, AB_M2, 0, t, kAWg, wflag)) break;
+            ptx::tc_fence_after();
+            {
+                float w0[32], w1[32];
+                ptx::tmem_ld32(tbase + lanes, w0);
+                ptx::tmem_ld32(tbase + lanes + 32, w1);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 v;
+                    uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        const int c = ch * 8 + 2 * q2;
+                        vv[q2] = c < 32 ? pack_bf16x2(w0[c & 31], w0[(c + 1) & 31])
+                                        : pack_bf16x2(w1[c & 31], w1[(c + 1) & 31]);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + A_AL + ptx::sw128_off(t, ch * 16)) = v;
+                }
+                ptx::tmem_ld32(tbase + lanes + 64, w0);
+                ptx::tmem_ld32(tbase + lanes + 96, w1);
+                ptx::tmem_wait_ld();
+                float *U = reinterpret_cast<float *>(img + IMG_U);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) U[c * D + t] = w0[c];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) U[(32 + c) * D + t] = w1[c];
+                reinterpret_cast<float *>(img + IMG_GC)[t] = gC[t];
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            named_bar(kAWg, 128);
+            if (t == 0) ptx::mbar_arrive(&S.bar[AB_WK]);
+        } while (false);
+    }
+    // ---------------------------------------------------------------------- teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (*S.err && tid == 0) flag_status(pa.status, KDA_DEV_TIMEOUT);
+    if (warp == 4) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tbase, 128);
+    }
+}
+
+// ============================================================================ chain
+constexpr int kBThreads = 256;      // warp 0 loads, warp 1 MMA, warps 4-7 state epilogues
+constexpr uint32_t B_SLOT = 91136;  // image slot stride (kImageBytes rounded up to 1024)
+constexpr uint32_t B_WT = 2 * B_SLOT;         // [128 rows][128 B] W^T bf16
+constexpr uint32_t B_BAR = B_WT + 16384;
+constexpr uint32_t B_SMEM = B_BAR + 256 + 1024;
+constexpr int kBSeq = 1;   // named barrier of the epilogue warpgroup
+
+// TMEM columns: S^T, O^T (two buffers), D_W = -(Gamma S)^T WK'^T, bf16 (Gamma S)^T.
+constexpr uint32_t COL_S = 0, COL_O = 128, COL_DW = 256, COL_SA = 320;
+
+enum { BB_FULL = 0, BB_SB = 2, BB_W = 4, BB_WT = 6, BB_M4 = 8, BB_DO = 10, B_NBARS = 12 };
+
+__global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, int wave) {
+    const PrefillArgs &pa = a.p;
+    const int H = pa.H;
+    const int h = blockIdx.x % H, sq = blockIdx.x / H;
+    const SeqMeta m = pa.seqs[sq];
+    const int64_t start = m.start_pos, end = m.start_pos + m.len;
+    const int64_t c_first = start / C;
+    const int nchunks = m.len > 0 ? (int)((end - 1) / C - c_first + 1) : 0;
+    const uint64_t rec = (uint64_t)h * (uint64_t)pa.pool.rec_bytes;
+    const int32_t *act_pages = pa.pages + m.active_off;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (nchunks == 0) {
+        // empty sequence: a fresh one gets a zero state and window, a resumed one keeps its own
+        if (wave == 0 && !m.has_init) {
+            for (int x = tid; x < (D * D * 4 + 9 * D * 2) / 16; x += kBThreads) {
+                uint4 *dst = reinterpret_cast<uint4 *>(obj_addr(pa.pool, act_pages, rec + (uint64_t)x * 16, pa.status));
+                if (dst) *dst = make_uint4(0, 0, 0, 0);
+            }
+        }
+        return;
+    }
+    const int lc0 = wave * a.cw;
+    if (lc0 >= nchunks) return;
+    const int lc1 = lc0 + a.cw < nchunks ? lc0 + a.cw : nchunks;
+    const int cnt = lc1 - lc0;
+    const bool first = lc0 == 0, last = lc1 == nchunks;
+    const int32_t off0 = a.wave_seq_off[(int64_t)wave * pa.nseq + sq];
+    if (off0 < 0) {
+        if (tid == 0) flag_status(pa.status, KDA_DEV_BAD_META);
+        return;
+    }
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Shared S;
+    S.base = sm;
+    S.bar = reinterpret_cast<uint64_t *>(sm + B_BAR);
+    S.err = reinterpret_cast<volatile int *>(sm + B_BAR + B_NBARS * 8);
+    S.tmem = reinterpret_cast<uint32_t *>(sm + B_BAR + B_NBARS * 8 + 16);
+    volatile int *sflag = reinterpret_cast<volatile int *>(sm + B_BAR + B_NBARS * 8 + 32);
+
+    if (tid == 0) {
+        for (int i = 0; i < B_NBARS; ++i) ptx::mbar_init(&S.bar[i], 1);
+        *S.err = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(S.tmem, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tbase = *S.tmem;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ image loads
+        if (lane == 0) {
+            int issued = 0;
+            for (int n = 0; n < cnt && !*S.err; ++n) {
+                const int b = n & 1;
+                if (n >= 2 && !wait_bar(S, BB_M4 + b, par(n - 2))) break;   // slot consumed
+                ptx::mbar_arrive_expect_tx(&S.bar[BB_FULL + b], (uint32_t)kImageBytes);
+                ptx::bulk_load(sm + b * B_SLOT, image_addr(a, wave, off0 + n, h), (uint32_t)kImageBytes,
+                               &S.bar[BB_FULL + b]);
+                ++issued;
+            }
+            if (*S.err)
+                for (int n = 0; n < issued; ++n) {
+                    uint32_t k = 0;
+                    while (!ptx::mbar_try_wait(&S.bar[BB_FULL + (n & 1)], par(n)) && k < ptx::kSpinLimit) ++k;
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_o = ptx::idesc_bf16(128, 64, 0, 0);
+            const uint32_t id_w = ptx::idesc_bf16(128, 64, 0, 1, 1);
+            const uint32_t id_s = ptx::idesc_bf16(128, 128, 0, 1);
+            const uint32_t id_op = ptx::idesc_bf16(128, 64, 0, 0);
+            const uint32_t sbase = ptx::smem_u32(sm);
+            int n3 = 0, n4 = 0;
+            uint32_t spins = 0;
+            while (n4 < cnt && !*S.err) {
+                bool did = false;
+                // M3: O^T = SA Qt'^T ; D_W = -SA WK'^T
+                if (n3 == n4 && n3 < cnt) {
+                    const int b = n3 & 1;
+                    if (ptx::mbar_test(&S.bar[BB_SB + b], par(n3)) && ptx::mbar_test(&S.bar[BB_FULL + b], par(n3)) &&
+                        (n3 < 2 || ptx::mbar_test(&S.bar[BB_DO + b], par(n3 - 2)))) {
+                        ptx::tc_fence_after();
+                        const uint32_t im = sbase + b * B_SLOT;
+                        for (int s = 0; s < 8; ++s) {
+                            const uint64_t bq = ptx::sdesc_sw128(im + IMG_Q + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024);
+                            ptx::mma_bf16_ta(tbase + COL_O + b * 64, tbase + COL_SA + s * 8, bq, id_o, s > 0 ? 1u : 0u);
+                        }
+                        for (int s = 0; s < 8; ++s) {
+                            const uint64_t bw = ptx::sdesc_sw128(im + IMG_WK + s * 2048, 8192, 1024);
+                            ptx::mma_bf16_ta(tbase + COL_DW, tbase + COL_SA + s * 8, bw, id_w, s > 0 ? 1u : 0u);
+                        }
+                        ptx::mma_commit(&S.bar[BB_W + b]);
+                        ++n3;
+                        did = true;
+                    }
+                }
+                // M4: S^T += W^T Kb ; O^T += W^T P^T
+                if (n4 < n3) {
+                    const int b = n4 & 1;
+                    if (ptx::mbar_test(&S.bar[BB_WT + b], par(n4))) {
+                        ptx::tc_fence_after();
+                        const uint32_t im = sbase + b * B_SLOT, wt = sbase + B_WT;
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
+                            const uint64_t bd = ptx::sdesc_sw128(im + IMG_KB + s * 2048, 8192, 1024);
+                            ptx::mma_bf16(tbase + COL_S, ad, bd, id_s, 1u);
+                        }
+                        for (int s = 0; s < 4; ++s) {
+                            const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
+                            const uint64_t bd = ptx::sdesc_sw128(im + IMG_P + s * 32, 16, 1024);
+                            ptx::mma_bf16(tbase + COL_O + b * 64, ad, bd, id_op, 1u);
+                        }
+                        ptx::mma_commit(&S.bar[BB_M4 + b]);
+                        ++n4;
+                        did = true;
+                    }
+                }
+                if (did) spins = 0;
+                else if (++spins > ptx::kSpinLimit) *S.err = 1;
+            }
+            // leave no MMA in flight
+            if (*S.err && n4 < n3) {
+                uint32_t k = 0;
+                while (!ptx::mbar_try_wait(&S.bar[BB_W + ((n3 - 1) & 1)], par(n3 - 1)) && k < ptx::kSpinLimit) ++k;
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------------ state epilogues
+        const int j = tid - 128;                       // value channel = TMEM lane
+        const uint32_t lanes = (uint32_t)((warp - 4) * 32) << 16;
+        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(pa.o);
+        float *scr = a.state_scr + ((int64_t)sq * H + h) * D * D;
+        // state at the start of this wave
+        for (int i0 = 0; i0 < D; i0 += 32) {
+            float v[32];
+#pragma unroll
+            for (int ii = 0; ii < 32; ++ii) {
+                float x = 0.f;
+                if (!first) {
+                    x = scr[(i0 + ii) * D + j];
+                } else if (m.has_init) {
+                    const float *p = reinterpret_cast<const float *>(
+                        obj_addr(pa.pool, act_pages, rec + ((uint64_t)(i0 + ii) * D + j) * 4, pa.status));
+                    if (p) x = *p;
+                }
+                v[ii] = x;
+            }
+            ptx::tmem_st32(tbase + lanes + COL_S + i0, v);
+        }
+        ptx::tmem_wait_st();
+        // S (fp32, from TMEM) into the checkpoint at `pos` if there is one, into the active
+        // object (final) or into the wave scratch (to_scratch)
+        auto write_state = [&](int64_t pos, bool final_state, bool to_scratch) {
+            const int ck = find_ckpt(pa, m, pos);
+            if (ck < 0 && !final_state && !to_scratch) return;
+            const int32_t *pg = ck >= 0 ? pa.pages + pa.ckpts[ck].pages_off : nullptr;
+            for (int i0 = 0; i0 < D; i0 += 32) {
+                float v[32];
+                ptx::tmem_ld32(tbase + lanes + COL_S + i0, v);
+                ptx::tmem_wait_ld();
+                if (pg) {
+#pragma unroll
+                    for (int ii = 0; ii < 32; ++ii) {
+                        float *dst = reinterpret_cast<float *>(
+                            obj_addr(pa.pool, pg, rec + ((uint64_t)(i0 + ii) * D + j) * 4, pa.status));
+                        if (dst) *dst = v[ii];
+                    }
+                }
+                if (final_state) {
+#pragma unroll
+                    for (int ii = 0; ii < 32; ++ii) {
+                        float *dst = reinterpret_cast<float *>(
+                            obj_addr(pa.pool, act_pages, rec + ((uint64_t)(i0 + ii) * D + j) * 4, pa.status));
+                        if (dst) *dst = v[ii];
+                    }
+                }
+                if (to_scratch) {
+#pragma unroll
+                    for (int ii = 0; ii < 32; ++ii) scr[(i0 + ii) * D + j] = v[ii];
+                }
+            }
+        };
+        auto store_outputs = [&](int n) {
+            const int b = n & 1;
+            const int64_t abs0 = (c_first + lc0 + n) * C;
+            const int r_first = start > abs0 ? (int)(start - abs0) : 0;
+            const int r_end = end - abs0 < C ? (int)(end - abs0) : C;
+            const int64_t row0 = (int64_t)m.tok_begin + (abs0 - start);
+            for (int r0 = 0; r0 < C; r0 += 32) {
+                float v[32];
+                ptx::tmem_ld32(tbase + lanes + COL_O + b * 64 + r0, v);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int r = r0 + rr;
+                    if (r >= r_first && r < r_end) og[((row0 + r) * H + h) * D + j] = __float2bfloat16_rn(v[rr]);
+                }
+            }
+            ptx::tc_fence_before();
+            named_bar(kBSeq, 128);
+            if (j == 0) ptx::mbar_arrive(&S.bar[BB_DO + b]);
+        };
+        bool ok = true;
+        for (int n = 0; n < cnt; ++n) {
+            const int b = n & 1;
+            // ---------------- E1: checkpoint S, Gamma_C S in TMEM, bf16 operand
+            if (n >= 1) {
+                if (!(ok = wg_wait(S, BB_M4 + ((n - 1) & 1), par(n - 1), j, kBSeq, sflag))) break;
+                ptx::tc_fence_after();
+                write_state((c_first + lc0 + n) * C, false, false);
+            }
+            if (!(ok = wg_wait(S, BB_FULL + b, par(n), j, kBSeq, sflag))) break;
+            const float *gcb = reinterpret_cast<const float *>(sm + b * B_SLOT + IMG_GC);
+            for (int i0 = 0; i0 < D; i0 += 64) {
+                float v[32], w[32], pk[32];
+                ptx::tmem_ld32(tbase + lanes + COL_S + i0, v);
+                ptx::tmem_ld32(tbase + lanes + COL_S + i0 + 32, w);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int ii = 0; ii < 32; ++ii) {
+                    v[ii] *= gcb[i0 + ii];
+                    w[ii] *= gcb[i0 + 32 + ii];
+                }
+                ptx::tmem_st32(tbase + lanes + COL_S + i0, v);
+                ptx::tmem_st32(tbase + lanes + COL_S + i0 + 32, w);
+#pragma unroll
+                for (int q2 = 0; q2 < 16; ++q2) {
+                    pk[q2] = __uint_as_float(pack_bf16x2(v[2 * q2], v[2 * q2 + 1]));
+                    pk[16 + q2] = __uint_as_float(pack_bf16x2(w[2 * q2], w[2 * q2 + 1]));
+                }
+                ptx::tmem_st32(tbase + lanes + COL_SA + (i0 >> 1), pk);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            named_bar(kBSeq, 128);
+            if (j == 0) ptx::mbar_arrive(&S.bar[BB_SB + b]);
+            // ---------------- E3 of the previous chunk (off the critical path)
+            if (n >= 1) store_outputs(n - 1);
+            // ---------------- E2: W^T = U^T + D_W -> bf16 operand
+            if (!(ok = wg_wait(S, BB_W + b, par(n), j, kBSeq, sflag))) break;
+            ptx::tc_fence_after();
+            const float *U = reinterpret_cast<const float *>(sm + b * B_SLOT + IMG_U);
+            for (int r0 = 0; r0 < C; r0 += 32) {
+                float v[32];
+                ptx::tmem_ld32(tbase + lanes + COL_DW + r0, v);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint4 pk;
+                    uint32_t *pp = reinterpret_cast<uint32_t *>(&pk);
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        const int c = r0 + ch * 8 + 2 * q2;
+                        pp[q2] = pack_bf16x2(v[ch * 8 + 2 * q2] + U[c * D + j], v[ch * 8 + 2 * q2 + 1] + U[(c + 1) * D + j]);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + B_WT + ptx::sw128_off(j, r0 * 2 + ch * 16)) = pk;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            named_bar(kBSeq, 128);
+            if (j == 0) ptx::mbar_arrive(&S.bar[BB_WT + b]);
+        }
+        if (ok && wg_wait(S, BB_M4 + ((cnt - 1) & 1), par(cnt - 1), j, kBSeq, sflag)) {
+            ptx::tc_fence_after();
+            if (last) {
+                write_state(end, true, false);
+                // final conv window (written by the chunk-prep kernel) into the active object
+                const uint4 *src = reinterpret_cast<const uint4 *>(a.win_scr + ((int64_t)sq * H + h) * (9 * D * 2));
+                for (int x = j; x < 9 * D * 2 / 16; x += 128) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(
+                        obj_addr(pa.pool, act_pages, rec + (uint64_t)D * D * 4 + (uint64_t)x * 16, pa.status));
+                    if (dst) *dst = src[x];
+                }
+            } else {
+                write_state((c_first + lc1) * C, false, true);
+            }
+            store_outputs(cnt - 1);
+        }
+    }
+    // ---------------------------------------------------------------------- teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (*S.err && tid == 0) flag_status(pa.status, KDA_DEV_TIMEOUT);
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tbase, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cudaStream_t s) {
+    const PrefillArgs &p = a.p;
+    CUtensorMap tm[4];
+    const void *src[4] = {p.q, p.k, p.v, p.alpha};
+    for (int i = 0; i < 4; ++i) {
+        std::memset(&tm[i], 0, sizeof(CUtensorMap));
+        const uint64_t rows = p.T_tot > 0 ? (uint64_t)p.T_tot : 1;
+        if (encode_tmap_bf16_2d(&tm[i], src[i], (uint64_t)p.H * D, rows, (uint64_t)p.H * D * 2, 64, 64) != 0)
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)A_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)B_SMEM);
+    if (e != cudaSuccess) return e;
+    const unsigned chains = (unsigned)(p.nseq * p.H);
+    if (plan.nwaves == 0) {   // only empty sequences
+        chain_kernel<<<chains, kBThreads, B_SMEM, s>>>(a, 0);
+        return cudaGetLastError();
+    }
+    for (int w = 0; w < plan.nwaves; ++w) {
+        const int i0 = plan.wave_begin[w], n = plan.wave_begin[w + 1] - i0;
+        if (n > 0)
+            chunk_prep_kernel<<<(unsigned)(n * p.H), kAThreads, A_SMEM, s>>>(a, w, i0, tm[0], tm[1], tm[2], tm[3]);
+        chain_kernel<<<chains, kBThreads, B_SMEM, s>>>(a, w);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace kda

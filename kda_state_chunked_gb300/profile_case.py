@@ -32,7 +32,7 @@ def prefill(T_seq, nseq, H, seed, launches, dev):
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     for _ in range(launches):
         seq, pos, pages = kda.kda_ckpt_plan(pool, H, d, dt, cu, [0] * nseq, 512, 4, True)
-        ws = torch.empty(kda.kda_prefill_workspace_bytes(nseq, len(seq), P), dtype=torch.uint8, device=dev)
+        ws = kda.prefill_workspace(toks["q"], cu, [0] * nseq, len(seq), P)
         kda.kda_prefill_varlen(pool, cu, [0] * nseq, [0] * nseq, toks["q"], toks["k"], toks["v"],
                                toks["alpha"], toks["beta"], toks["conv_w"], o, act, seq, pos, pages, ws, st)
         torch.cuda.synchronize()

@@ -83,8 +83,7 @@ class Prefill:
             self.pos = np.zeros(0, np.int64)
             self.pages = np.zeros((0, P0), np.int32)
         P = pool.object_pages(H, d, dt)
-        ws = torch.empty(kda.kda_prefill_workspace_bytes(len(cu) - 1, len(self.seq), P),
-                         dtype=torch.uint8, device=q.device)
+        ws = kda.prefill_workspace(q, cu, start_pos, len(self.seq), P)
         self.status = torch.zeros(1, dtype=torch.int32, device=q.device)
         self.o = torch.full_like(q, float("nan"))
         kda.kda_prefill_varlen(pool, cu, start_pos, has_init, q, toks["k"], toks["v"], toks["alpha"],

@@ -42,7 +42,7 @@ def _case(pool, dtype, d, H, lens, starts, init, seed):
         o = torch.full_like(toks["q"], float("nan"))
         st = torch.zeros(1, dtype=torch.int32, device=DEV)
         if which == "workspace":
-            ws = torch.empty(kda.kda_prefill_workspace_bytes(n, len(seq), P), dtype=torch.uint8, device=DEV)
+            ws = kda.prefill_workspace(toks["q"], cu, starts, len(seq), P)
             kda.kda_prefill_varlen(pool, cu, starts, init, toks["q"], toks["k"], toks["v"], toks["alpha"],
                                    toks["beta"], toks["conv_w"], o, act, seq, pos, pages, ws, st)
         else:
