@@ -121,6 +121,42 @@ WsLayout ws_layout(int64_t H, int64_t nseq, int64_t nck, int64_t P, const kda::S
     return L;
 }
 
+// The pool's second stream for the split prefill, created on first use; on another device
+// than the one it was created on, or if creation fails, the prefill runs on one stream.
+kda::SideStream side_stream(kda_pool *p) {
+    kda::SideStream ss;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ss;
+    if (!p->side && p->side_dev < 0) {
+        p->side_dev = dev;
+        int least = 0, greatest = 0;
+        bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess;
+        ok = ok && cudaStreamCreateWithPriority(&p->side, cudaStreamNonBlocking, least) == cudaSuccess;
+        ok = ok && cudaStreamCreateWithPriority(&p->main, cudaStreamNonBlocking, greatest) == cudaSuccess;
+        for (cudaEvent_t *e : {&p->ev_in, &p->ev_a, &p->ev_out, &p->ev_b[0], &p->ev_b[1]})
+            ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) {
+            for (cudaStream_t *st : {&p->side, &p->main}) {
+                if (*st) cudaStreamDestroy(*st);
+                *st = nullptr;
+            }
+            for (cudaEvent_t *e : {&p->ev_in, &p->ev_a, &p->ev_out, &p->ev_b[0], &p->ev_b[1]}) {
+                if (*e) cudaEventDestroy(*e);
+                *e = nullptr;
+            }
+        }
+    }
+    if (!p->side || dev != p->side_dev) return ss;
+    ss.side = p->side;
+    ss.main = p->main;
+    ss.ev_in = p->ev_in;
+    ss.ev_a = p->ev_a;
+    ss.ev_out = p->ev_out;
+    ss.ev_b[0] = p->ev_b[0];
+    ss.ev_b[1] = p->ev_b[1];
+    return ss;
+}
+
 // Metadata-only workspace of the fused kernels (also the layout the allocation-free path uses).
 int64_t prefill_ws_bytes(int64_t nseq, int64_t nck, int64_t P) { return ws_layout(1, nseq, nck, P, nullptr).total; }
 
@@ -330,7 +366,7 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
     sa.win_scr = ws + L.o_win;
     sa.cw = plan.cw;
     sa.nwaves = plan.nwaves;
-    return kda::launch_prefill_split(sa, plan, st) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+    return kda::launch_prefill_split(sa, plan, st, side_stream(pool)) == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
 int kda_decode_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B,

@@ -106,8 +106,16 @@ struct CopyArgs {
     int32_t *status;
 };
 
+// Streams and events for overlapping the two kernels of the split prefill: chunk preparation
+// on `side` (low priority), chains on `main` (high priority), joined back to the caller's
+// stream (side == nullptr: everything on the caller's stream).
+struct SideStream {
+    cudaStream_t side = nullptr, main = nullptr;
+    cudaEvent_t ev_in = nullptr, ev_a = nullptr, ev_out = nullptr, ev_b[2] = {nullptr, nullptr};
+};
+
 // Kernel launchers (defined in the .cu files).
-cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cudaStream_t s);
+cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cudaStream_t s, const SideStream &ss);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_supported(const PrefillArgs &a);

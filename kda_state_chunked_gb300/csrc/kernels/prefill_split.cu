@@ -134,29 +134,44 @@ __global__ void __launch_bounds__(kAThreads, 2)
         for (int i = 0; i < A_NBARS; ++i) ptx::mbar_init(&S.bar[i], 1);
         *S.err = 0;
         ptx::fence_mbar_init();
+        // raw q, k, v, alpha tiles of the chunk (rows outside the sequence are masked later)
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+        ptx::prefetch_tmap(&tm_a);
+        const int32_t y = (int32_t)((int64_t)m.tok_begin + (abs0 - start));
+        uint64_t *fb = &S.bar[AB_FULL];
+        ptx::mbar_arrive_expect_tx(fb, 4 * 2 * 64 * 128);
+        for (int kb = 0; kb < 2; ++kb) {
+            const int32_t x = h * D + kb * 64;
+            ptx::tma_load_2d(sm + A_KQ + kb * 16384, &tm_k, fb, x, y);
+            ptx::tma_load_2d(sm + A_KQ + kb * 16384 + 8192, &tm_q, fb, x, y);
+            ptx::tma_load_2d(sm + A_V + kb * 8192, &tm_v, fb, x, y);
+            ptx::tma_load_2d(sm + A_AL + kb * 8192, &tm_a, fb, x, y);
+        }
     }
     if (warp == 4) {
         ptx::tmem_alloc(S.tmem, 128);
         ptx::tmem_relinquish();
     }
-    // Conv window before the first valid row: raw tokens from the input, or from the active
-    // object's window (positions before this call's start), or zeros.
+    // Conv window before the first valid row, 16 bytes per thread: raw tokens from the input,
+    // or from the active object's window (positions before this call's start), or zeros.
     const int64_t fv = abs0 + r_first;
-    for (int x = tid; x < 3 * 3 * D; x += kAThreads) {
-        const int u = x / (3 * D), c = x - u * 3 * D;
+    if (tid < 3 * 3 * D * 2 / 16) {
+        const int u = tid / 48, c = (tid - u * 48) * 8;   // 48 vectors of 8 channels per token
         const int64_t pos = fv - 3 + u;
-        __nv_bfloat16 val = __float2bfloat16_rn(0.f);
+        uint4 val = make_uint4(0, 0, 0, 0);
         if (pos >= start) {
             const int64_t row = (int64_t)m.tok_begin + (pos - start);
             const __nv_bfloat16 *src = c < D ? qg : (c < 2 * D ? kg : vg);
-            val = src[(row * H + h) * D + (c & (D - 1))];
+            val = *reinterpret_cast<const uint4 *>(src + (row * H + h) * D + (c & (D - 1)));
         } else if (m.has_init) {
             const int slot = (int)(pos - start + 3);
-            const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(obj_addr(
+            const uint4 *p = reinterpret_cast<const uint4 *>(obj_addr(
                 pa.pool, act_pages, rec + (uint64_t)D * D * 4 + ((uint64_t)slot * 3 * D + c) * 2, pa.status));
             if (p) val = *p;
         }
-        halo[x] = val;
+        *reinterpret_cast<uint4 *>(halo + u * 3 * D + c) = val;
     }
     if (tid < C) {
         const int64_t pos = abs0 + tid;
@@ -173,22 +188,6 @@ __global__ void __launch_bounds__(kAThreads, 2)
         // ------------------------------------------------------------------ TMA / MMA / stores
         if (lane == 0) {
             bool m1 = false, m2 = false;
-            ptx::prefetch_tmap(&tm_q);
-            ptx::prefetch_tmap(&tm_k);
-            ptx::prefetch_tmap(&tm_v);
-            ptx::prefetch_tmap(&tm_a);
-            {
-                const int32_t y = (int32_t)((int64_t)m.tok_begin + (abs0 - start));
-                uint64_t *fb = &S.bar[AB_FULL];
-                ptx::mbar_arrive_expect_tx(fb, 4 * 2 * 64 * 128);
-                for (int kb = 0; kb < 2; ++kb) {
-                    const int32_t x = h * D + kb * 64;
-                    ptx::tma_load_2d(sm + A_KQ + kb * 16384, &tm_k, fb, x, y);
-                    ptx::tma_load_2d(sm + A_KQ + kb * 16384 + 8192, &tm_q, fb, x, y);
-                    ptx::tma_load_2d(sm + A_V + kb * 8192, &tm_v, fb, x, y);
-                    ptx::tma_load_2d(sm + A_AL + kb * 8192, &tm_a, fb, x, y);
-                }
-            }
             const uint32_t sbase = ptx::smem_u32(sm);
             if (wait_bar(S, AB_P1, 0)) {
                 // M1: G | P = [Kt'; Qt'] Kb^T
@@ -596,17 +595,42 @@ __global__ void __launch_bounds__(kAThreads, 2)
 }
 
 // ============================================================================ chain
-constexpr int kBThreads = 256;      // warp 0 loads, warp 1 MMA, warps 4-7 state epilogues
-constexpr uint32_t B_SLOT = 91136;  // image slot stride (kImageBytes rounded up to 1024)
-constexpr uint32_t B_WT = 2 * B_SLOT;         // [128 rows][128 B] W^T bf16
-constexpr uint32_t B_BAR = B_WT + 16384;
+// 16 warps: warp 0 loads images, warp 1 issues MMAs, warps 4-7 and 8-11 run the state
+// epilogues on the low and high halves of the columns, warps 12-15 write the outputs.
+constexpr int kBThreads = 512;
+constexpr uint32_t B_SLOT = 91136;               // image slot stride (kImageBytes rounded up to 1024)
+constexpr uint32_t B_WT = 2 * B_SLOT;            // [128 rows][128 B] W^T bf16 (A operand)
+constexpr uint32_t B_OST = B_WT + 16384;         // [64 rows][256 B] bf16 output staging
+constexpr uint32_t B_BAR = B_OST + 16384;
 constexpr uint32_t B_SMEM = B_BAR + 256 + 1024;
-constexpr int kBSeq = 1;   // named barrier of the epilogue warpgroup
+constexpr int kBOut = 1;   // named barrier of the output warpgroup
 
-// TMEM columns: S^T, O^T (two buffers), D_W = -(Gamma S)^T WK'^T, bf16 (Gamma S)^T.
+// TMEM columns: S^T, O^T (two buffers), D_W = -(Gamma S)^T WK'^T, bf16 (Gamma S)^T (two buffers,
+// two values per column).
 constexpr uint32_t COL_S = 0, COL_O = 128, COL_DW = 256, COL_SA = 320;
 
-enum { BB_FULL = 0, BB_SB = 2, BB_W = 4, BB_WT = 6, BB_M4 = 8, BB_DO = 10, B_NBARS = 12 };
+// mbarriers ([2] by chunk parity).  SB and WT count the 8 state warps, DO the 4 output warps.
+enum {
+    BB_FULL = 0,    // image landed (tx)
+    BB_SB = 2,      // (Gamma S)^T written, S scaled
+    BB_W = 4,       // D_W in TMEM
+    BB_WT = 6,      // W^T operand written
+    BB_M4S = 8,     // S advanced
+    BB_M4 = 10,     // every MMA of the chunk done (O complete, image free)
+    BB_DO = 12,     // O buffer read
+    B_NBARS = 14
+};
+
+// First checkpoint of sequence m at or after position pos (index relative to the sequence).
+__device__ __forceinline__ int lower_ckpt(const PrefillArgs &a, const SeqMeta &m, int64_t pos) {
+    int lo = 0, hi = m.ckpt_count;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a.ckpts[m.ckpt_begin + mid].pos < pos) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
 
 __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, int wave) {
     const PrefillArgs &pa = a.p;
@@ -648,10 +672,13 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
     S.bar = reinterpret_cast<uint64_t *>(sm + B_BAR);
     S.err = reinterpret_cast<volatile int *>(sm + B_BAR + B_NBARS * 8);
     S.tmem = reinterpret_cast<uint32_t *>(sm + B_BAR + B_NBARS * 8 + 16);
-    volatile int *sflag = reinterpret_cast<volatile int *>(sm + B_BAR + B_NBARS * 8 + 32);
 
     if (tid == 0) {
-        for (int i = 0; i < B_NBARS; ++i) ptx::mbar_init(&S.bar[i], 1);
+        for (int i = 0; i < B_NBARS; ++i) {
+            const uint32_t cntw = (i == BB_SB || i == BB_SB + 1 || i == BB_WT || i == BB_WT + 1) ? 8u
+                                  : (i >= BB_DO) ? 4u : 1u;
+            ptx::mbar_init(&S.bar[i], cntw);
+        }
         *S.err = 0;
         ptx::fence_mbar_init();
     }
@@ -684,46 +711,58 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
+        // Per chunk, in this order: D_W (needs the scaled state), the state update (needs W^T),
+        // then the outputs, which stay off the state's critical path.
         if (lane == 0) {
             const uint32_t id_o = ptx::idesc_bf16(128, 64, 0, 0);
             const uint32_t id_w = ptx::idesc_bf16(128, 64, 0, 1, 1);
             const uint32_t id_s = ptx::idesc_bf16(128, 128, 0, 1);
             const uint32_t id_op = ptx::idesc_bf16(128, 64, 0, 0);
-            const uint32_t sbase = ptx::smem_u32(sm);
-            int n3 = 0, n4 = 0;
+            const uint32_t sbase = ptx::smem_u32(sm), wt = sbase + B_WT;
+            int nd = 0, ns = 0, no = 0;
             uint32_t spins = 0;
-            while (n4 < cnt && !*S.err) {
+            while (no < cnt && !*S.err) {
                 bool did = false;
-                // M3: O^T = SA Qt'^T ; D_W = -SA WK'^T
-                if (n3 == n4 && n3 < cnt) {
-                    const int b = n3 & 1;
-                    if (ptx::mbar_test(&S.bar[BB_SB + b], par(n3)) && ptx::mbar_test(&S.bar[BB_FULL + b], par(n3)) &&
-                        (n3 < 2 || ptx::mbar_test(&S.bar[BB_DO + b], par(n3 - 2)))) {
+                if (nd == no && nd < cnt) {
+                    const int b = nd & 1;
+                    if (ptx::mbar_test(&S.bar[BB_SB + b], par(nd)) && ptx::mbar_test(&S.bar[BB_FULL + b], par(nd))) {
+                        // D_W = -(Gamma S)^T WK'^T
                         ptx::tc_fence_after();
                         const uint32_t im = sbase + b * B_SLOT;
                         for (int s = 0; s < 8; ++s) {
-                            const uint64_t bq = ptx::sdesc_sw128(im + IMG_Q + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024);
-                            ptx::mma_bf16_ta(tbase + COL_O + b * 64, tbase + COL_SA + s * 8, bq, id_o, s > 0 ? 1u : 0u);
-                        }
-                        for (int s = 0; s < 8; ++s) {
                             const uint64_t bw = ptx::sdesc_sw128(im + IMG_WK + s * 2048, 8192, 1024);
-                            ptx::mma_bf16_ta(tbase + COL_DW, tbase + COL_SA + s * 8, bw, id_w, s > 0 ? 1u : 0u);
+                            ptx::mma_bf16_ta(tbase + COL_DW, tbase + COL_SA + b * 64 + s * 8, bw, id_w, s > 0 ? 1u : 0u);
                         }
                         ptx::mma_commit(&S.bar[BB_W + b]);
-                        ++n3;
+                        ++nd;
                         did = true;
                     }
                 }
-                // M4: S^T += W^T Kb ; O^T += W^T P^T
-                if (n4 < n3) {
-                    const int b = n4 & 1;
-                    if (ptx::mbar_test(&S.bar[BB_WT + b], par(n4))) {
+                if (ns < nd) {
+                    const int b = ns & 1;
+                    if (ptx::mbar_test(&S.bar[BB_WT + b], par(ns))) {
+                        // S^T += W^T Kb
                         ptx::tc_fence_after();
-                        const uint32_t im = sbase + b * B_SLOT, wt = sbase + B_WT;
+                        const uint32_t im = sbase + b * B_SLOT;
                         for (int s = 0; s < 4; ++s) {
                             const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
                             const uint64_t bd = ptx::sdesc_sw128(im + IMG_KB + s * 2048, 8192, 1024);
                             ptx::mma_bf16(tbase + COL_S, ad, bd, id_s, 1u);
+                        }
+                        ptx::mma_commit(&S.bar[BB_M4S + b]);
+                        ++ns;
+                        did = true;
+                    }
+                }
+                if (no < ns) {
+                    const int b = no & 1;
+                    if (no < 2 || ptx::mbar_test(&S.bar[BB_DO + b], par(no - 2))) {
+                        // O^T = (Gamma S)^T Qt'^T + W^T P^T
+                        const uint32_t im = sbase + b * B_SLOT;
+                        for (int s = 0; s < 8; ++s) {
+                            const uint64_t bq = ptx::sdesc_sw128(im + IMG_Q + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024);
+                            ptx::mma_bf16_ta(tbase + COL_O + b * 64, tbase + COL_SA + b * 64 + s * 8, bq, id_o,
+                                             s > 0 ? 1u : 0u);
                         }
                         for (int s = 0; s < 4; ++s) {
                             const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
@@ -731,7 +770,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                             ptx::mma_bf16(tbase + COL_O + b * 64, ad, bd, id_op, 1u);
                         }
                         ptx::mma_commit(&S.bar[BB_M4 + b]);
-                        ++n4;
+                        ++no;
                         did = true;
                     }
                 }
@@ -739,22 +778,32 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                 else if (++spins > ptx::kSpinLimit) *S.err = 1;
             }
             // leave no MMA in flight
-            if (*S.err && n4 < n3) {
+            if (*S.err && nd > 0) {
                 uint32_t k = 0;
-                while (!ptx::mbar_try_wait(&S.bar[BB_W + ((n3 - 1) & 1)], par(n3 - 1)) && k < ptx::kSpinLimit) ++k;
+                while (!ptx::mbar_try_wait(&S.bar[BB_W + ((nd - 1) & 1)], par(nd - 1)) && k < ptx::kSpinLimit) ++k;
+                if (ns > 0) {
+                    k = 0;
+                    while (!ptx::mbar_try_wait(&S.bar[BB_M4S + ((ns - 1) & 1)], par(ns - 1)) && k < ptx::kSpinLimit) ++k;
+                }
+                if (no > 0) {
+                    k = 0;
+                    while (!ptx::mbar_try_wait(&S.bar[BB_M4 + ((no - 1) & 1)], par(no - 1)) && k < ptx::kSpinLimit) ++k;
+                }
             }
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------------ state epilogues
-        const int j = tid - 128;                       // value channel = TMEM lane
-        const uint32_t lanes = (uint32_t)((warp - 4) * 32) << 16;
-        __nv_bfloat16 *og = static_cast<__nv_bfloat16 *>(pa.o);
+        const int g = (warp - 4) >> 2;                 // column half
+        const int j = (warp & 3) * 32 + lane;          // value channel = TMEM lane
+        const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+        const int ib = g * 64;                         // key channels [ib, ib + 64) of S^T
         float *scr = a.state_scr + ((int64_t)sq * H + h) * D * D;
         // state at the start of this wave
-        for (int i0 = 0; i0 < D; i0 += 32) {
-            float v[32];
+#pragma unroll 1
+        for (int i0 = ib; i0 < ib + 64; i0 += 8) {
+            float v[8];
 #pragma unroll
-            for (int ii = 0; ii < 32; ++ii) {
+            for (int ii = 0; ii < 8; ++ii) {
                 float x = 0.f;
                 if (!first) {
                     x = scr[(i0 + ii) * D + j];
@@ -765,102 +814,74 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                 }
                 v[ii] = x;
             }
-            ptx::tmem_st32(tbase + lanes + COL_S + i0, v);
+            ptx::tmem_st8(tbase + lanes + COL_S + i0, v);
         }
         ptx::tmem_wait_st();
-        // S (fp32, from TMEM) into the checkpoint at `pos` if there is one, into the active
-        // object (final) or into the wave scratch (to_scratch)
+        // next checkpoint at or after the first chunk boundary of this wave
+        int ck_i = lower_ckpt(pa, m, (c_first + lc0) * C + 1);
+        int64_t ck_pos = ck_i < m.ckpt_count ? pa.ckpts[m.ckpt_begin + ck_i].pos : INT64_MAX;
+        // this half of S (fp32, from TMEM) into the checkpoint at `pos` if there is one, into
+        // the active object (final) or into the wave scratch (to_scratch)
         auto write_state = [&](int64_t pos, bool final_state, bool to_scratch) {
-            const int ck = find_ckpt(pa, m, pos);
-            if (ck < 0 && !final_state && !to_scratch) return;
-            const int32_t *pg = ck >= 0 ? pa.pages + pa.ckpts[ck].pages_off : nullptr;
-            for (int i0 = 0; i0 < D; i0 += 32) {
-                float v[32];
-                ptx::tmem_ld32(tbase + lanes + COL_S + i0, v);
-                ptx::tmem_wait_ld();
-                if (pg) {
-#pragma unroll
-                    for (int ii = 0; ii < 32; ++ii) {
-                        float *dst = reinterpret_cast<float *>(
-                            obj_addr(pa.pool, pg, rec + ((uint64_t)(i0 + ii) * D + j) * 4, pa.status));
-                        if (dst) *dst = v[ii];
-                    }
-                }
-                if (final_state) {
-#pragma unroll
-                    for (int ii = 0; ii < 32; ++ii) {
-                        float *dst = reinterpret_cast<float *>(
-                            obj_addr(pa.pool, act_pages, rec + ((uint64_t)(i0 + ii) * D + j) * 4, pa.status));
-                        if (dst) *dst = v[ii];
-                    }
-                }
-                if (to_scratch) {
-#pragma unroll
-                    for (int ii = 0; ii < 32; ++ii) scr[(i0 + ii) * D + j] = v[ii];
-                }
-            }
-        };
-        auto store_outputs = [&](int n) {
-            const int b = n & 1;
-            const int64_t abs0 = (c_first + lc0 + n) * C;
-            const int r_first = start > abs0 ? (int)(start - abs0) : 0;
-            const int r_end = end - abs0 < C ? (int)(end - abs0) : C;
-            const int64_t row0 = (int64_t)m.tok_begin + (abs0 - start);
-            for (int r0 = 0; r0 < C; r0 += 32) {
-                float v[32];
-                ptx::tmem_ld32(tbase + lanes + COL_O + b * 64 + r0, v);
+            const bool hit = ck_pos == pos;
+            if (!hit && !final_state && !to_scratch) return;
+            const int32_t *pg = hit ? pa.pages + pa.ckpts[m.ckpt_begin + ck_i].pages_off : nullptr;
+#pragma unroll 1
+            for (int i0 = ib; i0 < ib + 64; i0 += 8) {
+                float v[8];
+                ptx::tmem_ld8(tbase + lanes + COL_S + i0, v);
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int rr = 0; rr < 32; ++rr) {
-                    const int r = r0 + rr;
-                    if (r >= r_first && r < r_end) og[((row0 + r) * H + h) * D + j] = __float2bfloat16_rn(v[rr]);
+                for (int ii = 0; ii < 8; ++ii) {
+                    const uint64_t off = rec + ((uint64_t)(i0 + ii) * D + j) * 4;
+                    if (pg) {
+                        float *dst = reinterpret_cast<float *>(obj_addr(pa.pool, pg, off, pa.status));
+                        if (dst) *dst = v[ii];
+                    }
+                    if (final_state) {
+                        float *dst = reinterpret_cast<float *>(obj_addr(pa.pool, act_pages, off, pa.status));
+                        if (dst) *dst = v[ii];
+                    }
+                    if (to_scratch) scr[(i0 + ii) * D + j] = v[ii];
                 }
             }
-            ptx::tc_fence_before();
-            named_bar(kBSeq, 128);
-            if (j == 0) ptx::mbar_arrive(&S.bar[BB_DO + b]);
+            if (hit) {
+                ++ck_i;
+                ck_pos = ck_i < m.ckpt_count ? pa.ckpts[m.ckpt_begin + ck_i].pos : INT64_MAX;
+            }
         };
         bool ok = true;
         for (int n = 0; n < cnt; ++n) {
             const int b = n & 1;
             // ---------------- E1: checkpoint S, Gamma_C S in TMEM, bf16 operand
             if (n >= 1) {
-                if (!(ok = wg_wait(S, BB_M4 + ((n - 1) & 1), par(n - 1), j, kBSeq, sflag))) break;
+                if (!(ok = warp_wait(S, BB_M4S + ((n - 1) & 1), par(n - 1)))) break;
                 ptx::tc_fence_after();
                 write_state((c_first + lc0 + n) * C, false, false);
             }
-            if (!(ok = wg_wait(S, BB_FULL + b, par(n), j, kBSeq, sflag))) break;
+            if (!(ok = warp_wait(S, BB_FULL + b, par(n)))) break;
             const float *gcb = reinterpret_cast<const float *>(sm + b * B_SLOT + IMG_GC);
-            for (int i0 = 0; i0 < D; i0 += 64) {
-                float v[32], w[32], pk[32];
-                ptx::tmem_ld32(tbase + lanes + COL_S + i0, v);
-                ptx::tmem_ld32(tbase + lanes + COL_S + i0 + 32, w);
+#pragma unroll 1
+            for (int i0 = 0; i0 < 64; i0 += 32) {
+                float v[32], pk[16];
+                ptx::tmem_ld32(tbase + lanes + COL_S + ib + i0, v);
                 ptx::tmem_wait_ld();
 #pragma unroll
-                for (int ii = 0; ii < 32; ++ii) {
-                    v[ii] *= gcb[i0 + ii];
-                    w[ii] *= gcb[i0 + 32 + ii];
-                }
-                ptx::tmem_st32(tbase + lanes + COL_S + i0, v);
-                ptx::tmem_st32(tbase + lanes + COL_S + i0 + 32, w);
+                for (int ii = 0; ii < 32; ++ii) v[ii] *= gcb[ib + i0 + ii];
+                ptx::tmem_st32(tbase + lanes + COL_S + ib + i0, v);
 #pragma unroll
-                for (int q2 = 0; q2 < 16; ++q2) {
-                    pk[q2] = __uint_as_float(pack_bf16x2(v[2 * q2], v[2 * q2 + 1]));
-                    pk[16 + q2] = __uint_as_float(pack_bf16x2(w[2 * q2], w[2 * q2 + 1]));
-                }
-                ptx::tmem_st32(tbase + lanes + COL_SA + (i0 >> 1), pk);
+                for (int q2 = 0; q2 < 16; ++q2) pk[q2] = __uint_as_float(pack_bf16x2(v[2 * q2], v[2 * q2 + 1]));
+                ptx::tmem_st16(tbase + lanes + COL_SA + b * 64 + ((ib + i0) >> 1), pk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            named_bar(kBSeq, 128);
-            if (j == 0) ptx::mbar_arrive(&S.bar[BB_SB + b]);
-            // ---------------- E3 of the previous chunk (off the critical path)
-            if (n >= 1) store_outputs(n - 1);
-            // ---------------- E2: W^T = U^T + D_W -> bf16 operand
-            if (!(ok = wg_wait(S, BB_W + b, par(n), j, kBSeq, sflag))) break;
+            warp_arrive(&S.bar[BB_SB + b]);
+            // ---------------- E2: W^T = U^T + D_W -> bf16 operand (chunk rows [32 g, 32 g + 32))
+            if (!(ok = warp_wait(S, BB_W + b, par(n)))) break;
             ptx::tc_fence_after();
             const float *U = reinterpret_cast<const float *>(sm + b * B_SLOT + IMG_U);
-            for (int r0 = 0; r0 < C; r0 += 32) {
+            {
+                const int r0 = g * 32;
                 float v[32];
                 ptx::tmem_ld32(tbase + lanes + COL_DW + r0, v);
                 ptx::tmem_wait_ld();
@@ -878,16 +899,15 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
-            named_bar(kBSeq, 128);
-            if (j == 0) ptx::mbar_arrive(&S.bar[BB_WT + b]);
+            warp_arrive(&S.bar[BB_WT + b]);
         }
-        if (ok && wg_wait(S, BB_M4 + ((cnt - 1) & 1), par(cnt - 1), j, kBSeq, sflag)) {
+        if (ok && warp_wait(S, BB_M4S + ((cnt - 1) & 1), par(cnt - 1))) {
             ptx::tc_fence_after();
             if (last) {
                 write_state(end, true, false);
                 // final conv window (written by the chunk-prep kernel) into the active object
                 const uint4 *src = reinterpret_cast<const uint4 *>(a.win_scr + ((int64_t)sq * H + h) * (9 * D * 2));
-                for (int x = j; x < 9 * D * 2 / 16; x += 128) {
+                for (int x = tid - 128; x < 9 * D * 2 / 16; x += 256) {
                     uint4 *dst = reinterpret_cast<uint4 *>(
                         obj_addr(pa.pool, act_pages, rec + (uint64_t)D * D * 4 + (uint64_t)x * 16, pa.status));
                     if (dst) *dst = src[x];
@@ -895,7 +915,45 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
             } else {
                 write_state((c_first + lc1) * C, false, true);
             }
-            store_outputs(cnt - 1);
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------------ outputs
+        const int j = (warp & 3) * 32 + lane;
+        const int jt = tid - 384;
+        const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+        __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(sm + B_OST);
+        const __nv_bfloat16 *og0 = static_cast<const __nv_bfloat16 *>(pa.o);
+        for (int n = 0; n < cnt; ++n) {
+            const int b = n & 1;
+            if (!warp_wait(S, BB_M4 + b, par(n))) break;
+            ptx::tc_fence_after();
+            float v0[32], v1[32];
+            ptx::tmem_ld32(tbase + lanes + COL_O + b * 64, v0);
+            ptx::tmem_ld32(tbase + lanes + COL_O + b * 64 + 32, v1);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            warp_arrive(&S.bar[BB_DO + b]);
+            // transpose through shared memory: row r of the chunk = 128 channels (256 B)
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+                ost[r * D + j] = __float2bfloat16_rn(v0[r]);
+                ost[(32 + r) * D + j] = __float2bfloat16_rn(v1[r]);
+            }
+            named_bar(kBOut, 128);
+            const int64_t abs0 = (c_first + lc0 + n) * C;
+            const int r_first = start > abs0 ? (int)(start - abs0) : 0;
+            const int r_end = end - abs0 < C ? (int)(end - abs0) : C;
+            const int64_t row0 = (int64_t)m.tok_begin + (abs0 - start);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int x = jt + 128 * k, r = x >> 4, vc = x & 15;
+                if (r >= r_first && r < r_end) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(const_cast<__nv_bfloat16 *>(og0) +
+                                                           ((row0 + r) * H + h) * D + vc * 8);
+                    *dst = *reinterpret_cast<const uint4 *>(ost + r * D + vc * 8);
+                }
+            }
+            named_bar(kBOut, 128);
         }
     }
     // ---------------------------------------------------------------------- teardown
@@ -910,7 +968,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
 
 }  // namespace
 
-cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cudaStream_t s) {
+cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cudaStream_t s, const SideStream &ss) {
     const PrefillArgs &p = a.p;
     CUtensorMap tm[4];
     const void *src[4] = {p.q, p.k, p.v, p.alpha};
@@ -929,13 +987,33 @@ cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cuda
         chain_kernel<<<chains, kBThreads, B_SMEM, s>>>(a, 0);
         return cudaGetLastError();
     }
+    // Wave w: chunk prep on the side stream (after the chains of wave w - 2 released its image
+    // slot), then the chains on the main stream; the prep of wave w + 1 overlaps the chains of
+    // wave w.  Without a side stream both run in order on the caller's stream.
+    const bool two = ss.side != nullptr;
+    cudaStream_t sa = two ? ss.side : s, sb = two ? ss.main : s;
+    if (two) {
+        if ((e = cudaEventRecord(ss.ev_in, s)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(sa, ss.ev_in, 0)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(sb, ss.ev_in, 0)) != cudaSuccess) return e;
+    }
     for (int w = 0; w < plan.nwaves; ++w) {
         const int i0 = plan.wave_begin[w], n = plan.wave_begin[w + 1] - i0;
+        if (two && w >= 2 && (e = cudaStreamWaitEvent(sa, ss.ev_b[w & 1], 0)) != cudaSuccess) return e;
         if (n > 0)
-            chunk_prep_kernel<<<(unsigned)(n * p.H), kAThreads, A_SMEM, s>>>(a, w, i0, tm[0], tm[1], tm[2], tm[3]);
-        chain_kernel<<<chains, kBThreads, B_SMEM, s>>>(a, w);
+            chunk_prep_kernel<<<(unsigned)(n * p.H), kAThreads, A_SMEM, sa>>>(a, w, i0, tm[0], tm[1], tm[2], tm[3]);
+        if (two) {
+            if ((e = cudaEventRecord(ss.ev_a, sa)) != cudaSuccess) return e;
+            if ((e = cudaStreamWaitEvent(sb, ss.ev_a, 0)) != cudaSuccess) return e;
+        }
+        chain_kernel<<<chains, kBThreads, B_SMEM, sb>>>(a, w);
+        if (two && (e = cudaEventRecord(ss.ev_b[w & 1], sb)) != cudaSuccess) return e;
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+    }
+    if (two) {
+        if ((e = cudaEventRecord(ss.ev_out, sb)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(s, ss.ev_out, 0)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

@@ -108,5 +108,19 @@ __device__ __forceinline__ bool wg_wait(const Shared &s, int idx, uint32_t parit
     return ok;
 }
 
+// Warp-uniform wait: lane 0 polls (bounded) and broadcasts the outcome to the warp.
+__device__ __forceinline__ bool warp_wait(const Shared &s, int idx, uint32_t parity) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = ptx::mbar_wait(&s.bar[idx], parity, s.err) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// One arrival for the whole warp once every lane's earlier writes are ordered before it
+// (barriers that count warps rather than threads).
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar);
+}
+
 }  // namespace tcx
 }  // namespace kda
