@@ -75,23 +75,24 @@ __device__ __forceinline__ int find_ckpt(const PrefillArgs &a, const SeqMeta &m,
 // ============================================================================ chunk prep
 constexpr int kAThreads = 160;   // warps 0-3 compute, warp 4 TMA + MMA + bulk stores
 
+// Shared memory (72 KB: three CTAs per SM).  P goes straight to the image from registers.
 constexpr uint32_t A_KQ = 0;        // [2 kb][128 rows: k 0-63 | q 64-127][128 B] -> Kt' | Qt'
+constexpr uint32_t A_T = 8192;      // T [64][128 B], over the first Qt' half once that is stored
 constexpr uint32_t A_V = 32768;     // [2 kb][64][128 B]  raw v -> V
 constexpr uint32_t A_AL = 49152;    // [2 kb][64][128 B]  raw alpha -> Kb -> fp32 solve scratch -> WK'^T
-constexpr uint32_t A_P = 65536;     // [64][128 B]        P
-constexpr uint32_t A_T = 73728;     // fp32 [64][32] diagonal partials, then T [64][128 B]
-constexpr uint32_t A_GC = 81920;    // float [128]  gamma_C
-constexpr uint32_t A_BS = 82432;    // float [64]   beta
-constexpr uint32_t A_PD = 82688;    // float [64]   exact diagonal of P
-constexpr uint32_t A_RED = 82944;   // float2 [2][64] half products of alpha
-constexpr uint32_t A_HALO = 83968;  // bf16 [3][384] conv window
-constexpr uint32_t A_BAR = 86272;   // mbarriers, flags
+constexpr uint32_t A_DG = 65536;    // float [64][8]      partial sums of the diagonal q.k
+constexpr uint32_t A_GC = 67584;    // float [128]  gamma_C
+constexpr uint32_t A_BS = 68096;    // float [64]   beta
+constexpr uint32_t A_PD = 68352;    // float [64]   exact diagonal of P
+constexpr uint32_t A_RED = 68608;   // float2 [2][64] half products of alpha
+constexpr uint32_t A_HALO = 69632;  // bf16 [3][384] conv window
+constexpr uint32_t A_BAR = 71936;   // mbarriers, flags
 constexpr uint32_t A_SMEM = A_BAR + 128 + 1024;
 constexpr int kAWg = 1, kAHalf = 2;   // named barriers (128 and 64 threads)
 
 enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_T, AB_M2, AB_WK, A_NBARS };
 
-__global__ void __launch_bounds__(kAThreads, 2)
+__global__ void __launch_bounds__(kAThreads, 3)
     chunk_prep_kernel(const SplitArgs a, int wave, int item0, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_a) {
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(kAThreads, 2)
     float *bs = reinterpret_cast<float *>(sm + A_BS);
     float *pd = reinterpret_cast<float *>(sm + A_PD);
     float2 *red = reinterpret_cast<float2 *>(sm + A_RED);
-    float *diag = reinterpret_cast<float *>(sm + A_T);
+    float *diag = reinterpret_cast<float *>(sm + A_DG);
     __nv_bfloat16 *halo = reinterpret_cast<__nv_bfloat16 *>(sm + A_HALO);
 
     const PrefillArgs &pa = a.p;
@@ -154,13 +155,17 @@ __global__ void __launch_bounds__(kAThreads, 2)
         ptx::tmem_alloc(S.tmem, 128);
         ptx::tmem_relinquish();
     }
-    // Conv window before the first valid row, 16 bytes per thread: raw tokens from the input,
-    // or from the active object's window (positions before this call's start), or zeros.
+    // Conv window before the first valid row (16 bytes per thread: raw tokens from the input,
+    // or from the active object's window for positions before this call's start, or zeros)
+    // and beta: loaded into registers now, stored to shared memory after the tile wait, so
+    // that their latency overlaps the tile loads.
     const int64_t fv = abs0 + r_first;
-    if (tid < 3 * 3 * D * 2 / 16) {
-        const int u = tid / 48, c = (tid - u * 48) * 8;   // 48 vectors of 8 channels per token
-        const int64_t pos = fv - 3 + u;
+    // 144 vectors of 8 channels (48 per token): compute thread t takes vector t and, for
+    // t < 16, vector 128 + t
+    auto load_halo = [&](int x) {
         uint4 val = make_uint4(0, 0, 0, 0);
+        const int u = x / 48, c = (x - u * 48) * 8;
+        const int64_t pos = fv - 3 + u;
         if (pos >= start) {
             const int64_t row = (int64_t)m.tok_begin + (pos - start);
             const __nv_bfloat16 *src = c < D ? qg : (c < 2 * D ? kg : vg);
@@ -171,13 +176,15 @@ __global__ void __launch_bounds__(kAThreads, 2)
                 pa.pool, act_pages, rec + (uint64_t)D * D * 4 + ((uint64_t)slot * 3 * D + c) * 2, pa.status));
             if (p) val = *p;
         }
-        *reinterpret_cast<uint4 *>(halo + u * 3 * D + c) = val;
-    }
+        return val;
+    };
+    uint4 halo_v = make_uint4(0, 0, 0, 0), halo_w = make_uint4(0, 0, 0, 0);
+    if (tid < 128) halo_v = load_halo(tid);
+    if (tid < 16) halo_w = load_halo(128 + tid);
+    __nv_bfloat16 beta_v = __float2bfloat16_rn(0.f);
     if (tid < C) {
         const int64_t pos = abs0 + tid;
-        bs[tid] = (pos >= start && pos < end)
-                      ? __bfloat162float(betag[((int64_t)m.tok_begin + (pos - start)) * H + h])
-                      : 0.f;
+        if (pos >= start && pos < end) beta_v = betag[((int64_t)m.tok_begin + (pos - start)) * H + h];
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -221,8 +228,6 @@ __global__ void __launch_bounds__(kAThreads, 2)
                 }
                 ptx::mma_commit(&S.bar[AB_M2]);
                 m2 = true;
-                ptx::bulk_store(img + IMG_P, sm + A_P, 8192);
-                ptx::bulk_commit();
             }
             if (!*S.err && wait_bar(S, AB_WK, 0)) {
                 ptx::bulk_store(img + IMG_WK, sm + A_AL, 16384);
@@ -255,6 +260,9 @@ __global__ void __launch_bounds__(kAThreads, 2)
                     wk[ee][j] = pa.conv_w[((int64_t)h * 3 * D + D + c0 + ee) * 4 + j];
                     wv[ee][j] = pa.conv_w[((int64_t)h * 3 * D + 2 * D + c0 + ee) * 4 + j];
                 }
+            *reinterpret_cast<uint4 *>(halo + t * 8) = halo_v;          // vector x at x * 8 elements
+            if (t < 16) *reinterpret_cast<uint4 *>(halo + (128 + t) * 8) = halo_w;
+            if (t < C) bs[t] = __bfloat162float(beta_v);
             if (!wg_wait(S, AB_FULL, 0, t, kAWg, wflag)) break;
             // ---------------- conv, decay, scaled operands (in place)
             uint8_t *const qrow = sm + A_KQ + kb * 16384 + 8192, *const krow = sm + A_KQ + kb * 16384;
@@ -327,8 +335,10 @@ __global__ void __launch_bounds__(kAThreads, 2)
                     okb = pack_bf16x2(kb0 * rcp_approx(sx), kb1 * rcp_approx(sy));
                     ov = pack_bf16x2(vb0, vb1);
                 }
-                const float dsum = dpart + __shfl_xor_sync(0xffffffffu, dpart, 1);
-                if ((lane & 1) == 0) diag[r * 32 + (p >> 1)] = dsum;
+                float dsum = dpart + __shfl_xor_sync(0xffffffffu, dpart, 1);
+                dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
+                dsum += __shfl_xor_sync(0xffffffffu, dsum, 4);
+                if ((lane & 7) == 0) diag[r * 8 + (p >> 3)] = dsum;
                 *reinterpret_cast<uint32_t *>(qrow + off) = oq;
                 *reinterpret_cast<uint32_t *>(krow + off) = ok;
                 *reinterpret_cast<uint32_t *>(arow + off) = okb;
@@ -383,8 +393,8 @@ __global__ void __launch_bounds__(kAThreads, 2)
             // exact fp32 diagonal of P from the pair sums (rotated order: no bank conflicts)
             if (t < C) {
                 float acc = 0.f;
-#pragma unroll 8
-                for (int s2 = 0; s2 < 32; ++s2) acc += diag[t * 32 + ((s2 + t) & 31)];
+#pragma unroll
+                for (int s2 = 0; s2 < 8; ++s2) acc += diag[t * 8 + ((s2 + t) & 7)];
                 pd[t] = acc;
             }
             named_bar(kAWg, 128);
@@ -445,7 +455,7 @@ __global__ void __launch_bounds__(kAThreads, 2)
                             vv[q2] = pack_bf16x2(s0 < r ? ga : (s0 == r ? pdr : 0.f),
                                                  s0 + 1 < r ? gb : (s0 + 1 == r ? pdr : 0.f));
                         }
-                        *reinterpret_cast<uint4 *>(sm + A_P + ptx::sw128_off(r, ch * 16)) = v;
+                        *reinterpret_cast<uint4 *>(img + IMG_P + ptx::sw128_off(r, ch * 16)) = v;
                     }
                 }
             }
