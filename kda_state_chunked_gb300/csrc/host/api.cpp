@@ -61,9 +61,10 @@ int32_t chunks_of(int64_t start, int64_t len) {
     return len > 0 ? (int32_t)((start + len - 1) / kda::kChunk - start / kda::kChunk + 1) : 0;
 }
 
-// Waves of `cw` chunks per chain: one slot of operand images (all chains' items of a wave)
-// stays near 48 MiB so that two slots fit in L2, with at least 8 chunks per wave to amortise
-// a chain launch.
+// Waves of `cw` chunks per chain, balanced: as few waves as keep one slot of operand images
+// (all chains' items of a wave) under kWaveBytes.
+constexpr int64_t kWaveBytes = (int64_t)384 << 20;
+
 void make_split_plan(int32_t H, int32_t nseq, const int32_t *cu, const int64_t *start, kda::SplitPlan &pl) {
     std::vector<int32_t> nch((size_t)nseq);
     int32_t maxc = 0, nact = 0;
@@ -75,9 +76,9 @@ void make_split_plan(int32_t H, int32_t nseq, const int32_t *cu, const int64_t *
     pl = kda::SplitPlan();
     if (maxc == 0) return;
     const int64_t per_chunk = (int64_t)nact * H * kda::kImageBytes;
-    int64_t cw = ((int64_t)48 << 20) / per_chunk;
-    cw = std::max<int64_t>(cw, 8);
-    cw = std::min<int64_t>(cw, maxc);
+    const int64_t cw_max = std::max<int64_t>(1, kWaveBytes / per_chunk);
+    const int64_t nw = (maxc + cw_max - 1) / cw_max;
+    const int64_t cw = (maxc + nw - 1) / nw;
     pl.cw = (int32_t)cw;
     pl.nwaves = (int32_t)((maxc + cw - 1) / cw);
     pl.wave_seq_off.assign((size_t)pl.nwaves * nseq, -1);
