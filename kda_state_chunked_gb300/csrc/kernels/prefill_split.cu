@@ -251,15 +251,19 @@ __global__ void __launch_bounds__(kAThreads, 3)
         const int c0 = 2 * p, kb = c0 >> 6, cb = (c0 & 63) * 2;
         const uint32_t lanes = (uint32_t)(warp * 32) << 16;
         do {
-            float wq[2][4], wk[2][4], wv[2][4];
-#pragma unroll
-            for (int ee = 0; ee < 2; ++ee)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    wq[ee][j] = pa.conv_w[((int64_t)h * 3 * D + c0 + ee) * 4 + j];
-                    wk[ee][j] = pa.conv_w[((int64_t)h * 3 * D + D + c0 + ee) * 4 + j];
-                    wv[ee][j] = pa.conv_w[((int64_t)h * 3 * D + 2 * D + c0 + ee) * 4 + j];
-                }
+            // conv weights of the channel pair, tap by tap: (channel c0, channel c0 + 1)
+            float2 wq[4], wk[4], wv[4];
+            {
+                const float4 *cw = reinterpret_cast<const float4 *>(pa.conv_w + (int64_t)h * 3 * D * 4);
+                const float4 q0 = cw[c0], q1 = cw[c0 + 1], k0 = cw[D + c0], k1 = cw[D + c0 + 1];
+                const float4 v0 = cw[2 * D + c0], v1 = cw[2 * D + c0 + 1];
+                wq[0] = make_float2(q0.x, q1.x); wq[1] = make_float2(q0.y, q1.y);
+                wq[2] = make_float2(q0.z, q1.z); wq[3] = make_float2(q0.w, q1.w);
+                wk[0] = make_float2(k0.x, k1.x); wk[1] = make_float2(k0.y, k1.y);
+                wk[2] = make_float2(k0.z, k1.z); wk[3] = make_float2(k0.w, k1.w);
+                wv[0] = make_float2(v0.x, v1.x); wv[1] = make_float2(v0.y, v1.y);
+                wv[2] = make_float2(v0.z, v1.z); wv[3] = make_float2(v0.w, v1.w);
+            }
             *reinterpret_cast<uint4 *>(halo + t * 8) = halo_v;          // vector x at x * 8 elements
             if (t < 16) *reinterpret_cast<uint4 *>(halo + (128 + t) * 8) = halo_w;
             if (t < C) bs[t] = __bfloat162float(beta_v);
@@ -302,12 +306,12 @@ __global__ void __launch_bounds__(kAThreads, 3)
             named_bar(kAWg, 128);
             const float2 h0 = red[p], h1 = red[64 + p];
             const float gCx = h0.x * h1.x, gCy = h0.y * h1.y;
-            const float icx = 1.f / gCx, icy = 1.f / gCy;
+            const float2 ic = make_float2(1.f / gCx, 1.f / gCy);
             if (hf == 0) {
                 gC[c0] = gCx;
                 gC[c0 + 1] = gCy;
             }
-            float gx = hf ? h0.x : 1.f, gy = hf ? h0.y : 1.f;
+            float2 g2 = hf ? h0 : make_float2(1.f, 1.f);
             uint32_t swz[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) swz[u] = ptx::sw128_off(u, cb);
@@ -317,23 +321,29 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 uint32_t oq = 0, ok = 0, okb = 0, ov = 0;
                 float dpart = 0.f;
                 if (valid) {
-                    const float qb0 = wq[0][0] * wqv[0].x + wq[0][1] * wqv[1].x + wq[0][2] * wqv[2].x + wq[0][3] * xq.x;
-                    const float qb1 = wq[1][0] * wqv[0].y + wq[1][1] * wqv[1].y + wq[1][2] * wqv[2].y + wq[1][3] * xq.y;
-                    const float kb0 = wk[0][0] * wkv[0].x + wk[0][1] * wkv[1].x + wk[0][2] * wkv[2].x + wk[0][3] * xk.x;
-                    const float kb1 = wk[1][0] * wkv[0].y + wk[1][1] * wkv[1].y + wk[1][2] * wkv[2].y + wk[1][3] * xk.y;
-                    const float vb0 = wv[0][0] * wvv[0].x + wv[0][1] * wvv[1].x + wv[0][2] * wvv[2].x + wv[0][3] * xv.x;
-                    const float vb1 = wv[1][0] * wvv[0].y + wv[1][1] * wvv[1].y + wv[1][2] * wvv[2].y + wv[1][3] * xv.y;
+                    float2 qb = fmul2(wq[0], wqv[0]), kbv = fmul2(wk[0], wkv[0]), vb = fmul2(wv[0], wvv[0]);
+                    qb = ffma2(wq[1], wqv[1], qb);
+                    kbv = ffma2(wk[1], wkv[1], kbv);
+                    vb = ffma2(wv[1], wvv[1], vb);
+                    qb = ffma2(wq[2], wqv[2], qb);
+                    kbv = ffma2(wk[2], wkv[2], kbv);
+                    vb = ffma2(wv[2], wvv[2], vb);
+                    qb = ffma2(wq[3], xq, qb);
+                    kbv = ffma2(wk[3], xk, kbv);
+                    vb = ffma2(wv[3], xv, vb);
                     wqv[0] = wqv[1]; wqv[1] = wqv[2]; wqv[2] = xq;
                     wkv[0] = wkv[1]; wkv[1] = wkv[2]; wkv[2] = xk;
                     wvv[0] = wvv[1]; wvv[1] = wvv[2]; wvv[2] = xv;
-                    gx *= al.x;
-                    gy *= al.y;
-                    dpart = qb0 * kb0 + qb1 * kb1;
-                    const float sx = gx * icx, sy = gy * icy;      // gamma_r / gamma_C
-                    oq = pack_bf16x2(qb0 * sx, qb1 * sy);
-                    ok = pack_bf16x2(kb0 * sx, kb1 * sy);
-                    okb = pack_bf16x2(kb0 * rcp_approx(sx), kb1 * rcp_approx(sy));
-                    ov = pack_bf16x2(vb0, vb1);
+                    g2 = fmul2(g2, al);
+                    const float2 qk = fmul2(qb, kbv);
+                    dpart = qk.x + qk.y;
+                    const float2 s2 = fmul2(g2, ic);                  // gamma_r / gamma_C
+                    const float2 qs = fmul2(qb, s2), ks = fmul2(kbv, s2);
+                    const float2 kr = fmul2(kbv, make_float2(rcp_approx(s2.x), rcp_approx(s2.y)));
+                    oq = pack_bf16x2(qs.x, qs.y);
+                    ok = pack_bf16x2(ks.x, ks.y);
+                    okb = pack_bf16x2(kr.x, kr.y);
+                    ov = pack_bf16x2(vb.x, vb.y);
                 }
                 float dsum = dpart + __shfl_xor_sync(0xffffffffu, dpart, 1);
                 dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
@@ -729,63 +739,45 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
             const uint32_t id_s = ptx::idesc_bf16(128, 128, 0, 1);
             const uint32_t id_op = ptx::idesc_bf16(128, 64, 0, 0);
             const uint32_t sbase = ptx::smem_u32(sm), wt = sbase + B_WT;
+            // the three groups of every chunk are issued in a fixed order, each after a
+            // blocking (bounded) wait on what it needs
             int nd = 0, ns = 0, no = 0;
-            uint32_t spins = 0;
-            while (no < cnt && !*S.err) {
-                bool did = false;
-                if (nd == no && nd < cnt) {
-                    const int b = nd & 1;
-                    if (ptx::mbar_test(&S.bar[BB_SB + b], par(nd)) && ptx::mbar_test(&S.bar[BB_FULL + b], par(nd))) {
-                        // D_W = -(Gamma S)^T WK'^T
-                        ptx::tc_fence_after();
-                        const uint32_t im = sbase + b * B_SLOT;
-                        for (int s = 0; s < 8; ++s) {
-                            const uint64_t bw = ptx::sdesc_sw128(im + IMG_WK + s * 2048, 8192, 1024);
-                            ptx::mma_bf16_ta(tbase + COL_DW, tbase + COL_SA + b * 64 + s * 8, bw, id_w, s > 0 ? 1u : 0u);
-                        }
-                        ptx::mma_commit(&S.bar[BB_W + b]);
-                        ++nd;
-                        did = true;
-                    }
+            for (int n = 0; n < cnt; ++n) {
+                const int b = n & 1;
+                const uint32_t im = sbase + b * B_SLOT;
+                if (!wait_bar(S, BB_FULL + b, par(n)) || !wait_bar(S, BB_SB + b, par(n))) break;
+                // D_W = -(Gamma S)^T WK'^T
+                ptx::tc_fence_after();
+                for (int s = 0; s < 8; ++s) {
+                    const uint64_t bw = ptx::sdesc_sw128(im + IMG_WK + s * 2048, 8192, 1024);
+                    ptx::mma_bf16_ta(tbase + COL_DW, tbase + COL_SA + b * 64 + s * 8, bw, id_w, s > 0 ? 1u : 0u);
                 }
-                if (ns < nd) {
-                    const int b = ns & 1;
-                    if (ptx::mbar_test(&S.bar[BB_WT + b], par(ns))) {
-                        // S^T += W^T Kb
-                        ptx::tc_fence_after();
-                        const uint32_t im = sbase + b * B_SLOT;
-                        for (int s = 0; s < 4; ++s) {
-                            const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
-                            const uint64_t bd = ptx::sdesc_sw128(im + IMG_KB + s * 2048, 8192, 1024);
-                            ptx::mma_bf16(tbase + COL_S, ad, bd, id_s, 1u);
-                        }
-                        ptx::mma_commit(&S.bar[BB_M4S + b]);
-                        ++ns;
-                        did = true;
-                    }
+                ptx::mma_commit(&S.bar[BB_W + b]);
+                ++nd;
+                if (!wait_bar(S, BB_WT + b, par(n))) break;
+                // S^T += W^T Kb
+                ptx::tc_fence_after();
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
+                    const uint64_t bd = ptx::sdesc_sw128(im + IMG_KB + s * 2048, 8192, 1024);
+                    ptx::mma_bf16(tbase + COL_S, ad, bd, id_s, 1u);
                 }
-                if (no < ns) {
-                    const int b = no & 1;
-                    if (no < 2 || ptx::mbar_test(&S.bar[BB_DO + b], par(no - 2))) {
-                        // O^T = (Gamma S)^T Qt'^T + W^T P^T
-                        const uint32_t im = sbase + b * B_SLOT;
-                        for (int s = 0; s < 8; ++s) {
-                            const uint64_t bq = ptx::sdesc_sw128(im + IMG_Q + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024);
-                            ptx::mma_bf16_ta(tbase + COL_O + b * 64, tbase + COL_SA + b * 64 + s * 8, bq, id_o,
-                                             s > 0 ? 1u : 0u);
-                        }
-                        for (int s = 0; s < 4; ++s) {
-                            const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
-                            const uint64_t bd = ptx::sdesc_sw128(im + IMG_P + s * 32, 16, 1024);
-                            ptx::mma_bf16(tbase + COL_O + b * 64, ad, bd, id_op, 1u);
-                        }
-                        ptx::mma_commit(&S.bar[BB_M4 + b]);
-                        ++no;
-                        did = true;
-                    }
+                ptx::mma_commit(&S.bar[BB_M4S + b]);
+                ++ns;
+                if (n >= 2 && !wait_bar(S, BB_DO + b, par(n - 2))) break;
+                // O^T = (Gamma S)^T Qt'^T + W^T P^T
+                ptx::tc_fence_after();
+                for (int s = 0; s < 8; ++s) {
+                    const uint64_t bq = ptx::sdesc_sw128(im + IMG_Q + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024);
+                    ptx::mma_bf16_ta(tbase + COL_O + b * 64, tbase + COL_SA + b * 64 + s * 8, bq, id_o, s > 0 ? 1u : 0u);
                 }
-                if (did) spins = 0;
-                else if (++spins > ptx::kSpinLimit) *S.err = 1;
+                for (int s = 0; s < 4; ++s) {
+                    const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
+                    const uint64_t bd = ptx::sdesc_sw128(im + IMG_P + s * 32, 16, 1024);
+                    ptx::mma_bf16(tbase + COL_O + b * 64, ad, bd, id_op, 1u);
+                }
+                ptx::mma_commit(&S.bar[BB_M4 + b]);
+                ++no;
             }
             // leave no MMA in flight
             if (*S.err && nd > 0) {
