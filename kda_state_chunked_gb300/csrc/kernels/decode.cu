@@ -8,14 +8,20 @@
 // block-table gather of "Chapitre 8 — Gestion nouvelle génération du cache KV" §8.1
 // (PagedAttention: logical blocks mapped to physical pages through a table).
 //
-// The kernel is HBM-bound (about 0.84 flop per byte): each CTA streams one 64 KiB fp32
-// state (d = 128) in and out once.  Warp w of 16 owns D/16 consecutive rows of S; lane l owns
-// D/32 consecutive columns, so every row is one coalesced 512-byte (d = 128) access made
-// of 128-bit loads, the state stays in registers between the two passes, the row
-// reductions for S'^T k and S^T q are thread-local and one shared-memory pass combines
-// the sixteen warps.  Sixteen warps per CTA and two CTAs per SM keep 64 KiB of state loads
-// in flight per CTA while the other CTA computes.
+// The step is HBM-bound (about 0.84 flop per byte): every state streams in and out once.
+// Two kernels:
+//   decode_tma_kernel (bf16, d = 128, pages of at least 64 KiB): one persistent CTA per SM with
+//     a three-slot ring of whole records in shared memory; a producer warp bulk-copies the
+//     record of a later (request, head) in and the updated record of an earlier one out while
+//     sixteen compute warps update the current one, so every SM keeps a record load and a
+//     record store in flight.
+//   decode_kernel (other shapes): one CTA per (request, head).  Warp w of 16 owns D/16
+//     consecutive rows of S; lane l owns D/32 consecutive columns, so every row is one
+//     coalesced access of 128-bit loads, the state stays in registers between the two passes,
+//     and one shared-memory pass combines the sixteen warps' partial column sums.
 #include "common.cuh"
+#include "sm100_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace kda {
 namespace {
@@ -164,10 +170,226 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------------------
+// Bulk-copy pipeline for bf16 records of d = 128 (67,840 bytes: S fp32 [128][128], then the
+// window [3][384] bf16) in pools of pages of at least 64 KiB.  One persistent CTA per SM walks
+// the (request, head) items with a three-slot ring: a producer warp bulk-loads the record of
+// item n + 2 (split at page boundaries) and the new token's q, k, v, alpha while sixteen
+// compute warps update item n in shared memory; the producer then bulk-stores the updated
+// record in place.  Every SM thus keeps a record load and a record store in flight.
+constexpr int kDtCompute = 512;                  // 16 compute warps
+constexpr int kDtThreads = kDtCompute + 32;      // + producer warp
+constexpr int kDtSlots = 3;
+constexpr uint32_t kDtRec = 67840;               // record bytes (d = 128, bf16)
+constexpr uint32_t kDtIn = 1024;                 // q | k | v | alpha of the new token (bf16)
+constexpr uint32_t kDtSlot = kDtRec + kDtIn;     // 68,864 (multiple of 128)
+constexpr uint32_t DT_RED = kDtSlots * kDtSlot;  // float [4][128] partial column sums
+constexpr uint32_t DT_XB = DT_RED + 2048;        // float [384] conv output
+constexpr uint32_t DT_MISC = DT_XB + 1536;       // beta per slot, valid flags, barriers
+constexpr uint32_t DT_SMEM = DT_MISC + 256;
+constexpr int kDtBar = 1;                        // named barrier of the compute warps
+
+__device__ __forceinline__ bool dt_wait(uint64_t *bar, uint32_t parity, volatile int *err) {
+    return ptx::mbar_wait(bar, parity, err);
+}
+
+__global__ void __launch_bounds__(kDtThreads, 1) decode_tma_kernel(DecodeArgs a) {
+    using tcx::named_bar;
+    constexpr int D = 128, C3 = 3 * D;
+    extern __shared__ __align__(128) uint8_t sm[];
+    float *red = reinterpret_cast<float *>(sm + DT_RED);
+    float *xb = reinterpret_cast<float *>(sm + DT_XB);
+    float *beta_s = reinterpret_cast<float *>(sm + DT_MISC);            // [3]
+    volatile int *valid = reinterpret_cast<volatile int *>(sm + DT_MISC + 16);   // [3]
+    volatile int *err = reinterpret_cast<volatile int *>(sm + DT_MISC + 32);
+    volatile int *go = reinterpret_cast<volatile int *>(sm + DT_MISC + 48);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + DT_MISC + 64);   // [3]
+    uint64_t *done = full + kDtSlots;                                   // [3]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int total = a.B * a.H;
+    const int64_t PB = a.pool.page_bytes;
+    if (tid == 0) {
+        for (int i = 0; i < kDtSlots; ++i) {
+            ptx::mbar_init(&full[i], 1);
+            ptx::mbar_init(&done[i], 1);
+        }
+        *err = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kDtCompute / 32) {
+        // ------------------------------------------------------------------ producer
+        const __nv_bfloat16 *src[4] = {static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k),
+                                      static_cast<const __nv_bfloat16 *>(a.v),
+                                      static_cast<const __nv_bfloat16 *>(a.alpha)};
+        // walk the record of `item` piece by piece (at most one piece per page it touches)
+        auto record_pieces = [&](int item, auto &&fn) {
+            const int r = item / a.H, hh = item % a.H;
+            const int32_t *pages = a.state_pages + (int64_t)r * a.pool.pages_per_object;
+            int64_t off = (int64_t)hh * a.pool.rec_bytes;
+            uint32_t done_b = 0;
+            while (done_b < kDtRec) {
+                const int64_t pi = off / PB, in = off - pi * PB;
+                const uint32_t len = (uint32_t)((int64_t)(kDtRec - done_b) < PB - in ? (kDtRec - done_b) : (PB - in));
+                fn(pages[pi], in, done_b, len);
+                off += len;
+                done_b += len;
+            }
+        };
+        auto store_item = [&](int n) {
+            const int item = blockIdx.x + n * gridDim.x, b = n % kDtSlots;
+            if (!valid[b]) return;
+            record_pieces(item, [&](int32_t page, int64_t in, uint32_t at, uint32_t len) {
+                ptx::bulk_store(a.pool.base + (int64_t)page * PB + in, sm + b * kDtSlot + at, len);
+            });
+            ptx::bulk_commit();
+        };
+        // The whole warp walks the items; lane 0 issues the copies and the waits, and all
+        // lanes check the request's page ids (a bad id skips the request, as in the other path).
+        int n = 0;
+        for (;; ++n) {
+            const int item = blockIdx.x + n * gridDim.x;
+            if (item >= total) break;
+            const int b = n % kDtSlots;
+            int stop = 0;
+            if (lane == 0) {
+                if (*err) {
+                    stop = 1;
+                } else if (n >= kDtSlots) {
+                    // the record that used this slot goes back to its pages first
+                    if (!dt_wait(&done[b], (uint32_t)(((n - kDtSlots) / kDtSlots) & 1), err)) {
+                        stop = 1;
+                    } else {
+                        store_item(n - kDtSlots);
+                        ptx::bulk_wait_read0();
+                    }
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+            const int32_t *pages = a.state_pages + (int64_t)(item / a.H) * a.pool.pages_per_object;
+            bool ok = true;
+            for (int i = lane; i < a.pool.pages_per_object; i += 32) ok = ok && (uint32_t)pages[i] < (uint32_t)a.pool.num_pages;
+            ok = __all_sync(0xffffffffu, ok);
+            if (lane == 0) {
+                valid[b] = ok ? 1 : 0;
+                if (!ok) {
+                    flag_status(a.status, KDA_DEV_BAD_PAGE);
+                    ptx::mbar_arrive(&full[b]);
+                } else {
+                    ptx::mbar_arrive_expect_tx(&full[b], kDtSlot);
+                    record_pieces(item, [&](int32_t page, int64_t in, uint32_t at, uint32_t len) {
+                        ptx::bulk_load(sm + b * kDtSlot + at, a.pool.base + (int64_t)page * PB + in, len, &full[b]);
+                    });
+                    const int64_t tok = (int64_t)item * D;   // [B][H][D] with item = r * H + h
+                    for (int x = 0; x < 4; ++x)
+                        ptx::bulk_load(sm + b * kDtSlot + kDtRec + x * 256, src[x] + tok, 256, &full[b]);
+                }
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            // the last records (every slot still holding one) go back too
+            for (int m = n - kDtSlots < 0 ? 0 : n - kDtSlots; m < n && !*err; ++m) {
+                const int b = m % kDtSlots;
+                if (!dt_wait(&done[b], (uint32_t)((m / kDtSlots) & 1), err)) break;
+                store_item(m);
+            }
+            ptx::bulk_wait0();
+            if (*err) {
+                // leave no copy in flight
+                for (int m = n - kDtSlots < 0 ? 0 : n - kDtSlots; m < n; ++m) {
+                    uint32_t k = 0;
+                    while (!ptx::mbar_try_wait(&full[m % kDtSlots], (uint32_t)((m / kDtSlots) & 1)) && k < ptx::kSpinLimit) ++k;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ compute
+        const int j = tid & (D - 1), rq = tid >> 7;          // value channel, row quarter
+        for (int n = 0;; ++n) {
+            const int item = blockIdx.x + n * gridDim.x;
+            if (item >= total) break;
+            const int b = n % kDtSlots, hh = item % a.H;
+            // thread 0 waits for the slot and decides for all compute threads whether to go on
+            if (tid == 0) *go = (dt_wait(&full[b], (uint32_t)((n / kDtSlots) & 1), err) && !*err) ? 1 : 0;
+            named_bar(kDtBar, kDtCompute);
+            if (!*go) break;
+            uint8_t *slot = sm + b * kDtSlot;
+            float *S = reinterpret_cast<float *>(slot);
+            __nv_bfloat16 *win = reinterpret_cast<__nv_bfloat16 *>(slot + D * D * 4);
+            const __nv_bfloat16 *xin = reinterpret_cast<const __nv_bfloat16 *>(slot + kDtRec);
+            if (valid[b]) {
+                // conv of the new token with the window; the window shifts in place
+                if (tid < C3) {
+                    const int c = tid;
+                    const float x = __bfloat162float(xin[c]);
+                    const float4 w = *reinterpret_cast<const float4 *>(a.conv_w + ((int64_t)hh * C3 + c) * 4);
+                    const __nv_bfloat16 p0 = win[c], p1 = win[C3 + c], p2 = win[2 * C3 + c];
+                    xb[c] = w.x * __bfloat162float(p0) + w.y * __bfloat162float(p1) + w.z * __bfloat162float(p2) + w.w * x;
+                    win[c] = p1;
+                    win[C3 + c] = p2;
+                    win[2 * C3 + c] = xin[c];
+                }
+                if (tid == 0) beta_s[b] = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.beta)[item]);
+                named_bar(kDtBar, kDtCompute);
+                // S' = Diag(alpha) S; partial column sums of S'^T k over this thread's 32 rows
+                float sv[32];
+                float acc = 0.f;
+#pragma unroll
+                for (int ii = 0; ii < 32; ++ii) {
+                    const int i = rq * 32 + ii;
+                    sv[ii] = __bfloat162float(xin[3 * D + i]) * S[i * D + j];
+                    acc = fmaf(xb[D + i], sv[ii], acc);
+                }
+                red[rq * D + j] = acc;
+                named_bar(kDtBar, kDtCompute);
+                const float u = (red[j] + red[D + j]) + (red[2 * D + j] + red[3 * D + j]);
+                const float wj = beta_s[b] * (xb[2 * D + j] - u);
+                named_bar(kDtBar, kDtCompute);   // red is reused below
+                // S = S' + k w^T in place, and the partial sums of S^T q
+                float ao = 0.f;
+#pragma unroll
+                for (int ii = 0; ii < 32; ++ii) {
+                    const int i = rq * 32 + ii;
+                    const float v = fmaf(xb[D + i], wj, sv[ii]);
+                    S[i * D + j] = v;
+                    ao = fmaf(xb[i], v, ao);
+                }
+                red[rq * D + j] = ao;
+                ptx::fence_proxy_async_smem();
+                named_bar(kDtBar, kDtCompute);
+                if (rq == 0) {
+                    const float o = (red[j] + red[D + j]) + (red[2 * D + j] + red[3 * D + j]);
+                    static_cast<__nv_bfloat16 *>(a.o)[(int64_t)item * D + j] = __float2bfloat16_rn(o);
+                }
+            }
+            // the slot may be stored (and, once the store has read it, refilled); red and xb
+            // are free for the next item
+            named_bar(kDtBar, kDtCompute);
+            if (tid == 0) ptx::mbar_arrive(&done[b]);
+        }
+    }
+    __syncthreads();
+    if (*err && tid == 0) flag_status(a.status, KDA_DEV_TIMEOUT);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     if (a.B <= 0) return cudaSuccess;
+    if (a.d == 128 && a.dtype == KDA_BF16 && a.pool.rec_bytes == (int64_t)kDtRec && a.pool.page_bytes >= 65536) {
+        int dev = 0, nsm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DT_SMEM);
+        if (e != cudaSuccess) return e;
+        const int total = a.B * a.H;
+        decode_tma_kernel<<<(unsigned)(total < nsm ? total : nsm), kDtThreads, DT_SMEM, s>>>(a);
+        return cudaGetLastError();
+    }
     if (a.d == 128) return a.dtype == KDA_BF16 ? launch_decode_t<128, __nv_bfloat16>(a, s)
                                                : launch_decode_t<128, float>(a, s);
     if (a.d == 64) return a.dtype == KDA_BF16 ? launch_decode_t<64, __nv_bfloat16>(a, s)
