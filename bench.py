@@ -30,8 +30,8 @@ sys.path.insert(0, ROOT)
 METRIC = "KDA prefill tokens/s and decode step µs at B=256; % of tensor/HBM roofline"
 WORKLOAD = "batched"
 # sources of the dominant (prefill) kernel, for matching committed ncu traffic to the code
-PREFILL_SOURCES = ["kernels/prefill_tc.cu", "kernels/tc_common.cuh", "kernels/sm100_ptx.cuh",
-                   "kernels/common.cuh", "kda_internal.h"]
+PREFILL_SOURCES = ["kernels/prefill_split.cu", "kernels/tc_common.cuh", "kernels/sm100_ptx.cuh",
+                   "kernels/common.cuh", "kda_internal.h", "host/api.cpp"]
 
 
 # --------------------------------------------------------------------------- helpers
