@@ -157,6 +157,13 @@ int64_t kda_prefill_workspace_bytes(int32_t H, int32_t d, int32_t dtype, int32_t
                                     const int32_t *cu_seqlens, const int64_t *start_pos,
                                     int32_t n_ckpt, int32_t pages_per_object);
 
+/* Number of kernel launches kda_prefill_varlen makes for this batch (same arguments as
+ * kda_prefill_workspace_bytes; cu_seqlens / start_pos host arrays): one for fp32 or d = 64;
+ * for bf16 with d = 128, two per wave of chunks (chunk preparation and chains), or one when
+ * every sequence is empty.  KDA_EINVAL for a bad shape. */
+int32_t kda_prefill_kernel_launches(int32_t H, int32_t d, int32_t dtype, int32_t nseq,
+                                    const int32_t *cu_seqlens, const int64_t *start_pos);
+
 /* Chunked varlen prefill (chunk = 64 tokens, chunks aligned to absolute positions).
  *   H, d, dtype      heads, head dimension (64 or 128), dtype of the token tensors
  *   nseq             number of sequences (>= 1)

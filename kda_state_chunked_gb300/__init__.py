@@ -48,6 +48,7 @@ _SIGS = {
     "kda_ckpt_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _I32, _I32, _I32, _I32,
                                      _P, _P, _P, _P]),
     "kda_prefill_workspace_bytes": (_I64, [_I32, _I32, _I32, _I32, _P, _P, _I32, _I32]),
+    "kda_prefill_kernel_launches": (_I32, [_I32, _I32, _I32, _I32, _P, _P]),
     "kda_prefill_varlen": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                           _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _I64, _P, _P]),
     "kda_prefill_varlen_noalloc": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
@@ -249,6 +250,14 @@ def kda_prefill_workspace_bytes(H: int, d: int, dtype: int, cu_seqlens, start_po
     sp = _i64(start_pos)
     return _check(lib().kda_prefill_workspace_bytes(H, d, dtype, len(cu) - 1, _ptr(cu), _ptr(sp), n_ckpt,
                                                     pages_per_object), "kda_prefill_workspace_bytes")
+
+
+def kda_prefill_kernel_launches(H: int, d: int, dtype: int, cu_seqlens, start_pos) -> int:
+    """Kernel launches one kda_prefill_varlen call makes for this batch."""
+    cu = _i32(cu_seqlens)
+    sp = _i64(start_pos)
+    return _check(lib().kda_prefill_kernel_launches(H, d, dtype, len(cu) - 1, _ptr(cu), _ptr(sp)),
+                  "kda_prefill_kernel_launches")
 
 
 def prefill_workspace(q, cu_seqlens, start_pos, n_ckpt: int, pages_per_object: int):

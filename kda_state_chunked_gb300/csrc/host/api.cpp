@@ -268,6 +268,21 @@ int64_t kda_prefill_workspace_bytes(int32_t H, int32_t d, int32_t dtype, int32_t
     return ws_layout(H, nseq, n_ckpt, pages_per_object, &pl).total;
 }
 
+int32_t kda_prefill_kernel_launches(int32_t H, int32_t d, int32_t dtype, int32_t nseq, const int32_t *cu_seqlens,
+                                    const int64_t *start_pos) {
+    if (!valid_shape(H, d, dtype) || nseq < 0) return KDA_EINVAL;
+    if (!split_applies(d, dtype)) return 1;
+    if (nseq > 0 && (!cu_seqlens || !start_pos)) return KDA_EINVAL;
+    for (int32_t s = 0; s < nseq; ++s)
+        if (cu_seqlens[s + 1] < cu_seqlens[s] || start_pos[s] < 0) return KDA_EINVAL;
+    kda::SplitPlan pl;
+    make_split_plan(H, nseq, cu_seqlens, start_pos, pl);
+    if (pl.nwaves == 0) return 1;
+    int32_t n = 0;
+    for (int32_t w = 0; w < pl.nwaves; ++w) n += 1 + (pl.wave_begin[w + 1] > pl.wave_begin[w] ? 1 : 0);
+    return n;
+}
+
 int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t nseq,
                        const int32_t *cu_seqlens, const int64_t *start_pos,
                        const uint8_t *has_init, const void *q, const void *k, const void *v,

@@ -204,3 +204,25 @@ def test_gpu_calls_reject_bad_arguments_before_touching_the_device():
     assert L.kda_prefill_varlen(*ok[:22], 1 << 20, *ok[23:]) == kda.KDA_EREF
     assert L.kda_decode_step(pool.handle, 2, 80, 0, 4, *([fake] * 10), None) == kda.KDA_EINVAL
     assert L.kda_ckpt_write(pool.handle, 2, 64, 0, 1, None, None, fake, fake, 0, fake, None) == kda.KDA_EINVAL
+
+
+def test_split_prefill_plan_launches_and_workspace():
+    """bf16 d=128 runs as waves of chunk preparation + chains; the host plan decides the
+    launch count and the operand-image workspace."""
+    cu = [0, 8192, 16384, 24576, 32768]
+    st = [0, 0, 0, 0]
+    bf, f32 = kda.KDA_BF16, kda.KDA_F32
+    # 4 x 128 chunks x 16 heads of 90,624-byte images: two balanced waves of 64 chunks
+    assert kda.kda_prefill_kernel_launches(16, 128, bf, cu, st) == 4
+    assert kda.kda_prefill_kernel_launches(16, 128, f32, cu, st) == 1
+    assert kda.kda_prefill_kernel_launches(16, 64, bf, cu, st) == 1
+    assert kda.kda_prefill_kernel_launches(16, 128, bf, [0, 0], [5]) == 1     # empty sequence only
+    assert kda.kda_prefill_kernel_launches(2, 128, bf, [0, 100], [0]) == 2     # one wave
+    ws = kda.kda_prefill_workspace_bytes(16, 128, bf, cu, st, 16, 17)
+    images = 2 * 4 * 64 * 16 * 90624          # two slots of one wave
+    scratch = 4 * 16 * 128 * 128 * 4 + 4 * 16 * 9 * 128 * 2
+    assert images + scratch <= ws <= images + scratch + (1 << 20)
+    # metadata only on the fp32 path
+    assert kda.kda_prefill_workspace_bytes(16, 128, f32, cu, st, 16, 17) < (1 << 20)
+    with pytest.raises(kda.KdaError):
+        kda.kda_prefill_kernel_launches(16, 128, bf, [0, 10, 5], [0, 0])      # decreasing offsets
