@@ -305,6 +305,110 @@ def _ckpt_io_phase(dev, n=256, reps=5):
     return res
 
 
+def _prefill_algorithmic_bytes(token_heads: int, objects: int, H: int, rec: int) -> int:
+    """q, k, v, alpha, beta in and o out (bf16, d = 128) per token-head, plus whole records."""
+    return token_heads * (4 * 256 + 2 + 256) + objects * H * rec
+
+
+def _long_phase(dev, steps=5, warmup=3):
+    """Long-context prefill: one sequence, H = 32, a 65,536-token slice of the 1M-token
+    workload (1,024 chunks per chain; the chain kernel dominates, so the per-token cost is
+    that of the full sequence), checkpoints at every 4th 512-token hash-block end."""
+    import torch
+    import kda_state_chunked_gb300 as kda
+    from kda_state_chunked_gb300 import workloads
+    w = workloads.WORKLOADS["long"]
+    T = 65536
+    dt = kda.DTYPES[w.dtype]
+    toks = workloads.make_tokens(T, w.H, w.d, w.dtype, w.seed, dev)
+    pool = kda.Pool(w.page_bytes, 64 + (T // 2048 + 2) * 34, dev)
+    P = pool.object_pages(w.H, w.d, dt)
+    act = kda.kda_page_alloc(pool, P).reshape(1, P)
+    cu, st0 = [0, T], [0]
+    n_ck = len(kda.kda_ckpt_positions(0, T, w.hash_block, w.stride, w.include_last))
+    ws = kda.prefill_workspace(toks["q"], cu, st0, n_ck, P)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o = torch.empty_like(toks["q"])
+
+    def one():
+        seq, pos, pages = kda.kda_ckpt_plan(pool, w.H, w.d, dt, cu, st0, w.hash_block, w.stride, w.include_last)
+        kda.kda_prefill_varlen(pool, cu, st0, [0], toks["q"], toks["k"], toks["v"], toks["alpha"], toks["beta"],
+                               toks["conv_w"], o, act, seq, pos, pages, ws, status)
+        kda.kda_page_decref(pool, pages.reshape(-1))
+
+    total, per = _time_steps(one, steps, warmup, torch.cuda.current_stream())
+    assert kda.kda_sync_status(status)[0] == kda.KDA_OK
+    ms = statistics.median(per)
+    ab = _prefill_algorithmic_bytes(T * w.H, n_ck + 1, w.H, kda.kda_record_bytes(w.d, dt))
+    return {"workload": "long context: 1 sequence x 65,536 tokens (slice of the 1M-token workload), H=32, "
+                        "stride 4 checkpoints", "tokens": T, "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
+            "algorithmic_bytes": ab, "achieved_gbs": ab / (ms * 1e-3) / 1e9, "steps": steps}
+
+
+def _varlen_phase(dev, steps=5, warmup=3):
+    """Varlen resume: 32 sequences (lengths uniform in [512, 32768], seed 2), H = 32; each
+    step restores every resumed sequence's checkpoint into its private object and prefills
+    the suffixes with new checkpoints (stride 4 + last), then releases the new pages."""
+    import numpy as np
+    import torch
+    import kda_state_chunked_gb300 as kda
+    from kda_state_chunked_gb300 import workloads
+    w = workloads.WORKLOADS["varlen_resume"]
+    H, d, dt = w.H, w.d, kda.DTYPES[w.dtype]
+    L = workloads.varlen_lengths(w.seed, w.nseq)
+    B = workloads.resume_points(L, w.seed)
+    cu = np.concatenate([[0], np.cumsum(L)]).astype(np.int64)
+    toks = workloads.make_tokens(int(cu[-1]), H, d, w.dtype, w.seed, dev)
+    rec = kda.kda_record_bytes(d, dt)
+    n_setup = sum(len(kda.kda_ckpt_positions(0, x, 512, 1, False)) for x in L)
+    n_new = sum(len(kda.kda_ckpt_positions(b, x, 512, w.stride, w.include_last)) for b, x in zip(B, L))
+    pool = kda.Pool(w.page_bytes, 64 + (2 * w.nseq + n_setup + n_new) * 34, dev)
+    P = pool.object_pages(H, d, dt)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # setup (untimed): every sequence in full with a checkpoint at every 512-token end
+    act0 = kda.kda_page_alloc(pool, w.nseq * P).reshape(w.nseq, P)
+    cu_l = [int(x) for x in cu]
+    seq0, pos0, pages0 = kda.kda_ckpt_plan(pool, H, d, dt, cu_l, [0] * w.nseq, 512, 1, False)
+    ws0 = kda.prefill_workspace(toks["q"], cu_l, [0] * w.nseq, len(seq0), P)
+    o0 = torch.empty_like(toks["q"])
+    kda.kda_prefill_varlen(pool, cu_l, [0] * w.nseq, [0] * w.nseq, toks["q"], toks["k"], toks["v"], toks["alpha"],
+                           toks["beta"], toks["conv_w"], o0, act0, seq0, pos0, pages0, ws0, status)
+    assert kda.kda_sync_status(status)[0] == kda.KDA_OK
+    del o0, ws0
+    where = {(int(s), int(p)): i for i, (s, p) in enumerate(zip(seq0, pos0))}
+    rs = [s for s in range(w.nseq) if B[s] > 0]
+    ck = np.stack([pages0[where[(s, B[s])]] for s in rs]).reshape(-1)
+    act = kda.kda_page_alloc(pool, w.nseq * P).reshape(w.nseq, P)
+    act_rs = act[rs].reshape(-1)
+    cws = torch.empty(kda.kda_copy_workspace_bytes(len(rs), P), dtype=torch.uint8, device=dev)
+    idx = torch.cat([torch.arange(int(cu[s]) + B[s], int(cu[s + 1]), device=dev) for s in range(w.nseq)])
+    suf = {k: (v[idx] if k != "conv_w" else v) for k, v in toks.items()}
+    del toks
+    cu2 = [int(x) for x in np.concatenate([[0], np.cumsum([x - b for x, b in zip(L, B)])])]
+    has = [1 if b > 0 else 0 for b in B]
+    ws = kda.prefill_workspace(suf["q"], cu2, B, n_new, P)
+    o = torch.empty_like(suf["q"])
+
+    def one():
+        kda.kda_ckpt_restore(pool, H, d, dt, ck, act_rs, cws, status)
+        seq, pos, pages = kda.kda_ckpt_plan(pool, H, d, dt, cu2, B, 512, w.stride, w.include_last)
+        kda.kda_prefill_varlen(pool, cu2, B, has, suf["q"], suf["k"], suf["v"], suf["alpha"], suf["beta"],
+                               suf["conv_w"], o, act, seq, pos, pages, ws, status)
+        kda.kda_page_decref(pool, pages.reshape(-1))
+        kda.kda_ckpt_release(pool, ck, P)
+
+    total, per = _time_steps(one, steps, warmup, torch.cuda.current_stream())
+    assert kda.kda_sync_status(status)[0] == kda.KDA_OK
+    ms = statistics.median(per)
+    T_suf = cu2[-1]
+    ab = _prefill_algorithmic_bytes(T_suf * H, n_new + w.nseq, H, rec) + 2 * len(rs) * H * rec
+    return {"workload": "varlen resume: 32 sequences (lengths U[512, 32768], seed 2), H=32, restore of each "
+                        "resume checkpoint + suffix prefill with stride-4 + last checkpoints",
+            "suffix_tokens": T_suf, "restored_objects": len(rs), "new_checkpoints": n_new, "ms_per_step": ms,
+            "tokens_per_s": T_suf / (ms * 1e-3), "algorithmic_bytes": ab,
+            "achieved_gbs": ab / (ms * 1e-3) / 1e9, "steps": steps}
+
+
 def _oracle_sample(toks_cpu_fn, threads_note=True):
     """Time the oracle (as it stands) on one sequence of the batched workload."""
     import oracle
@@ -417,6 +521,11 @@ def run_ours(args, rank, world, dev):
         for k in ("write", "restore"):
             io[k]["frac"] = io[k]["gbs"] / peaks["hbm_gbs"]
         line["ckpt_io"] = io
+        for name, fn in (("long_prefill", _long_phase), ("varlen_resume", _varlen_phase)):
+            r = fn(dev)
+            r["roofline"] = {"bound": "hbm", "achieved": r["achieved_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": r["achieved_gbs"] / peaks["hbm_gbs"]}
+            line[name] = r
         line["gpu_launches"] = args.steps * bench.launches_per_step   # headline timed region
     if rank == 0 and world == 1 and not args.no_cpu:
         def cpu_toks():
