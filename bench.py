@@ -302,6 +302,43 @@ def _ckpt_io_phase(dev, n=256, reps=5):
     assert kda.kda_sync_status(st)[0] == kda.KDA_OK
     res["objects"] = n
     res["bytes_moved"] = nb
+    # INT8 checkpoints: quantise the same objects into new INT8 checkpoints, and dequantise
+    # them back into the private objects (bytes: one full and one INT8 object each way)
+    Pq = kda.kda_object_pages_q8(pool, H, d, dt)
+    nbq = (kda.kda_object_bytes(H, d, dt) + kda.kda_object_bytes_q8(H, d, dt)) * n
+    for name in ("write_q8", "restore_q8"):
+        for warm in (True, False):
+            count = 2 if warm else reps
+            made = []
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(count):
+                if name == "write_q8":
+                    made.append(kda.kda_ckpt_write_q8(pool, H, d, dt, src, ws[i % 4], st))
+                else:
+                    kda.kda_ckpt_restore_q8(pool, H, d, dt, q8_ck, act, ws[i % 4], st)
+            b.record(stream)
+            torch.cuda.synchronize()
+            if name == "write_q8":
+                q8_ck = made[-1].reshape(-1)
+                for m in made[:-1]:
+                    kda.kda_page_decref(pool, m.reshape(-1))
+                if not warm:
+                    keep = q8_ck
+                else:
+                    kda.kda_page_decref(pool, q8_ck)
+            else:
+                for _ in range(count):
+                    kda.kda_ckpt_release(pool, q8_ck, Pq)
+            ms = a.elapsed_time(b) / count
+        if name == "write_q8":
+            q8_ck = keep
+        res[name] = {"ms": ms, "gbs": nbq / (ms * 1e-3) / 1e9, "calls_timed": reps}
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+    res["bytes_moved_q8"] = nbq
+    res["q8_compression"] = kda.kda_object_bytes(H, d, dt) / kda.kda_object_bytes_q8(H, d, dt)
     return res
 
 
@@ -518,7 +555,7 @@ def run_ours(args, rank, world, dev):
                            "unit": "GB/s", "frac": dec["achieved_gbs"] / peaks["hbm_gbs"]}
         line["decode"] = dec
         io = _ckpt_io_phase(dev)
-        for k in ("write", "restore"):
+        for k in ("write", "restore", "write_q8", "restore_q8"):
             io[k]["frac"] = io[k]["gbs"] / peaks["hbm_gbs"]
         line["ckpt_io"] = io
         for name, fn in (("long_prefill", _long_phase), ("varlen_resume", _varlen_phase)):

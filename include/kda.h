@@ -265,6 +265,39 @@ int kda_ckpt_restore(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_
 int kda_ckpt_release(kda_pool *pool, int32_t n, int32_t pages_per_object,
                      const int32_t *ckpt_pages);
 
+/* ---------------------------------------------------------------- INT8 checkpoints -- */
+
+/* INT8 compressed checkpoints ("KIMI K3 경량 복제에서 본 KDA의 AI 인프라 과제", §0x05 5.3 and
+ * §0x06 6.6: checkpoints waiting in the cache may hold the recurrent state in INT8 while the
+ * small conv window keeps its native precision; a hit is dequantised once into a fresh active
+ * slot, so the recurrence itself never runs on quantised state).
+ * INT8 head record: scale fp32 [d] | codes int8 [d][d] (row i = key channel i, column j =
+ * value channel j) | window [3][3d] in dtype, zero-padded to a multiple of 256 bytes
+ * (19,200 bytes at d = 128 bf16 against 67,840 for the full record); an INT8 object is the H
+ * records in head order, paged like a full object.  scale_i = max_j |S[i][j]| / 127 and
+ * code = round-to-nearest-even(S[i][j] / scale_i) clamped to [-127, 127], both divisions IEEE
+ * fp32; a zero row has scale 0 and codes 0; dequantisation writes code * scale_i. */
+int64_t kda_record_bytes_q8(int32_t d, int32_t dtype);
+int64_t kda_object_bytes_q8(int32_t H, int32_t d, int32_t dtype);
+int32_t kda_object_pages_q8(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype);
+
+/* Snapshot n full objects (src_pages, host int32 [n * P], allocated) into n new INT8
+ * checkpoint objects: allocates n * Pq fresh pages (lowest free first, refcount 1; Pq =
+ * kda_object_pages_q8), returns them in dst_pages_out (host int32 [n * Pq]) and enqueues the
+ * quantisation.  workspace: device, at least kda_copy_workspace_bytes(n, P).  On an error
+ * nothing is allocated.  The pool's pages and every object must be below 4 GiB. */
+int kda_ckpt_write_q8(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n,
+                      const int32_t *src_pages, int32_t *dst_pages_out, void *pool_base,
+                      void *workspace, int64_t ws_bytes, int32_t *status_dev, void *stream);
+
+/* Restore n INT8 checkpoints (ckpt_pages, host int32 [n * Pq], allocated) into n private full
+ * objects (active_pages, host int32 [n * P], refcount 1, disjoint from the checkpoints): the
+ * checkpoint pages are pinned (incref) for the conversion and released by
+ * kda_ckpt_release(pool, n, Pq, ckpt_pages) once the stream has passed it. */
+int kda_ckpt_restore_q8(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n,
+                        const int32_t *ckpt_pages, const int32_t *active_pages, void *pool_base,
+                        void *workspace, int64_t ws_bytes, int32_t *status_dev, void *stream);
+
 /* ---------------------------------------------------------------- status -------------- */
 
 /* Wait for `stream`, read and clear *status_dev.  Returns KDA_OK, KDA_EDEVICE (bits in

@@ -59,6 +59,11 @@ _SIGS = {
     "kda_ckpt_write": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P]),
     "kda_ckpt_restore": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P]),
     "kda_ckpt_release": (ctypes.c_int, [_P, _I32, _I32, _P]),
+    "kda_record_bytes_q8": (_I64, [_I32, _I32]),
+    "kda_object_bytes_q8": (_I64, [_I32, _I32, _I32]),
+    "kda_object_pages_q8": (_I32, [_P, _I32, _I32, _I32]),
+    "kda_ckpt_write_q8": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P]),
+    "kda_ckpt_restore_q8": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P]),
     "kda_sync_status": (ctypes.c_int, [_P, _P, _P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -365,6 +370,50 @@ def kda_ckpt_release(pool: Pool, ckpt_pages, pages_per_object: int) -> None:
     ck = _i32(ckpt_pages)
     _check(lib().kda_ckpt_release(pool.handle, len(ck) // pages_per_object, pages_per_object,
                                   _ptr(ck)), "kda_ckpt_release")
+
+
+# ------------------------------------------------------------------------------ INT8 checkpoints
+def kda_record_bytes_q8(d: int, dtype: int) -> int:
+    return _check(lib().kda_record_bytes_q8(d, dtype), "kda_record_bytes_q8")
+
+
+def kda_object_bytes_q8(H: int, d: int, dtype: int) -> int:
+    return _check(lib().kda_object_bytes_q8(H, d, dtype), "kda_object_bytes_q8")
+
+
+def kda_object_pages_q8(pool: Pool, H: int, d: int, dtype: int) -> int:
+    return _check(lib().kda_object_pages_q8(pool.handle, H, d, dtype), "kda_object_pages_q8")
+
+
+def kda_ckpt_write_q8(pool: Pool, H: int, d: int, dtype: int, src_pages, workspace, status,
+                      stream=None) -> np.ndarray:
+    """Snapshot full objects into new INT8 checkpoints; returns their pages [n, Pq]."""
+    src = _i32(src_pages)
+    P = kda_object_pages(pool, H, d, dtype)
+    Pq = kda_object_pages_q8(pool, H, d, dtype)
+    n = len(src) // P
+    dst = np.zeros(max(n * Pq, 1), dtype=np.int32)
+    rc = lib().kda_ckpt_write_q8(pool.handle, H, d, dtype, n, _ptr(src), _ptr(dst), _dev(pool.base),
+                                 _dev(workspace), workspace.numel() * workspace.element_size(),
+                                 _dev(status), _stream(stream))
+    _check(rc, "kda_ckpt_write_q8")
+    return dst[:n * Pq].reshape(n, Pq)
+
+
+def kda_ckpt_restore_q8(pool: Pool, H: int, d: int, dtype: int, ckpt_pages, active_pages, workspace,
+                        status, stream=None) -> None:
+    """Dequantise INT8 checkpoints [n, Pq] into private full objects [n, P]."""
+    ck = _i32(ckpt_pages)
+    act = _i32(active_pages)
+    P = kda_object_pages(pool, H, d, dtype)
+    Pq = kda_object_pages_q8(pool, H, d, dtype)
+    n = len(act) // P
+    if len(ck) != n * Pq:
+        raise ValueError("ckpt_pages and active_pages hold different object counts")
+    rc = lib().kda_ckpt_restore_q8(pool.handle, H, d, dtype, n, _ptr(ck), _ptr(act), _dev(pool.base),
+                                   _dev(workspace), workspace.numel() * workspace.element_size(),
+                                   _dev(status), _stream(stream))
+    _check(rc, "kda_ckpt_restore_q8")
 
 
 # ------------------------------------------------------------------------------ status

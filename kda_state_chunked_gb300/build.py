@@ -19,7 +19,7 @@ SO = os.path.join(BUILD, "libkda.so")
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-CU_SOURCES = ["kernels/ckpt_copy.cu", "kernels/decode.cu", "kernels/prefill_simt.cu",
+CU_SOURCES = ["kernels/ckpt_copy.cu", "kernels/ckpt_q8.cu", "kernels/decode.cu", "kernels/prefill_simt.cu",
               "kernels/tc_selftest.cu", "kernels/prefill_tc.cu", "kernels/prefill_split.cu",
               "host/prefill_noalloc.cu"]
 CPP_SOURCES = ["host/pool.cpp", "host/api.cpp"]

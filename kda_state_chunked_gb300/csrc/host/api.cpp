@@ -458,6 +458,101 @@ int kda_ckpt_release(kda_pool *pool, int32_t n, int32_t pages_per_object, const 
     return kda_page_decref(pool, n * pages_per_object, ckpt_pages);
 }
 
+int64_t kda_record_bytes_q8(int32_t d, int32_t dtype) {
+    if (!valid_shape(1, d, dtype)) return KDA_EINVAL;
+    return align_up((int64_t)4 * d + (int64_t)d * d + (int64_t)kda::kWin * 3 * d * elem_size(dtype), 256);
+}
+
+int64_t kda_object_bytes_q8(int32_t H, int32_t d, int32_t dtype) {
+    if (!valid_shape(H, d, dtype)) return KDA_EINVAL;
+    return (int64_t)H * kda_record_bytes_q8(d, dtype);
+}
+
+int32_t kda_object_pages_q8(const kda_pool *p, int32_t H, int32_t d, int32_t dtype) {
+    if (!p || !valid_shape(H, d, dtype)) return KDA_EINVAL;
+    return (int32_t)((kda_object_bytes_q8(H, d, dtype) + p->page_bytes - 1) / p->page_bytes);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Upload [full lists][q8 lists] and run one conversion (quantise or dequantise).
+int convert_q8(kda_pool *p, int32_t H, int32_t d, int32_t dtype, int32_t n, const int32_t *full,
+               const int32_t *q8, void *pool_base, void *ws, int32_t *status, cudaStream_t stream, bool quantize) {
+    const int32_t P = kda_object_pages(p, H, d, dtype), Pq = kda_object_pages_q8(p, H, d, dtype);
+    std::vector<int32_t> both((size_t)n * (P + Pq));
+    std::memcpy(both.data(), full, (size_t)n * P * 4);
+    std::memcpy(both.data() + (size_t)n * P, q8, (size_t)n * Pq * 4);
+    int rc = kda::stage_upload(p, both.data(), both.size() * 4, ws, stream);
+    if (rc != KDA_OK) return rc;
+    kda::Q8Args a;
+    a.n = n;
+    a.H = H;
+    a.d = d;
+    a.dtype = dtype;
+    a.full = pool_view(p, pool_base, H, d, dtype);
+    a.q8 = a.full;
+    a.q8.pages_per_object = Pq;
+    a.q8.rec_bytes = kda_record_bytes_q8(d, dtype);
+    a.full_pages = static_cast<const int32_t *>(ws);
+    a.q8_pages = static_cast<const int32_t *>(ws) + (size_t)n * P;
+    a.status = status;
+    const cudaError_t e = quantize ? kda::launch_ckpt_quantize(a, stream) : kda::launch_ckpt_dequantize(a, stream);
+    return e == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+
+bool q8_sizes_ok(const kda_pool *p, int32_t H, int32_t d, int32_t dtype) {
+    return p->page_bytes < ((int64_t)1 << 32) && kda_object_bytes(H, d, dtype) < ((int64_t)1 << 32);
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_ckpt_write_q8(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n, const int32_t *src_pages,
+                      int32_t *dst_pages_out, void *pool_base, void *workspace, int64_t ws_bytes,
+                      int32_t *status_dev, void *stream) {
+    if (!pool || !valid_shape(H, d, dtype) || n < 0 || !pool_base || !workspace || !status_dev) return KDA_EINVAL;
+    if (n == 0) return KDA_OK;
+    if (!src_pages || !dst_pages_out || !q8_sizes_ok(pool, H, d, dtype)) return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype), Pq = kda_object_pages_q8(pool, H, d, dtype);
+    if (ws_bytes < kda_copy_workspace_bytes(n, P) || (uintptr_t)workspace % 16 != 0) return KDA_EINVAL;
+    std::lock_guard<std::mutex> g(pool->mu);
+    int rc = check_allocated(pool, src_pages, (int64_t)n * P);
+    if (rc != KDA_OK) return rc;
+    rc = kda::pool_alloc(pool, n * Pq, dst_pages_out);
+    if (rc != KDA_OK) return rc;
+    rc = convert_q8(pool, H, d, dtype, n, src_pages, dst_pages_out, pool_base, workspace, status_dev,
+                    static_cast<cudaStream_t>(stream), true);
+    if (rc != KDA_OK) kda::pool_decref(pool, n * Pq, dst_pages_out);
+    return rc;
+}
+
+int kda_ckpt_restore_q8(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n, const int32_t *ckpt_pages,
+                        const int32_t *active_pages, void *pool_base, void *workspace, int64_t ws_bytes,
+                        int32_t *status_dev, void *stream) {
+    if (!pool || !valid_shape(H, d, dtype) || n < 0 || !pool_base || !workspace || !status_dev) return KDA_EINVAL;
+    if (n == 0) return KDA_OK;
+    if (!ckpt_pages || !active_pages || !q8_sizes_ok(pool, H, d, dtype)) return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype), Pq = kda_object_pages_q8(pool, H, d, dtype);
+    if (ws_bytes < kda_copy_workspace_bytes(n, P) || (uintptr_t)workspace % 16 != 0) return KDA_EINVAL;
+    std::lock_guard<std::mutex> g(pool->mu);
+    int rc = check_allocated(pool, ckpt_pages, (int64_t)n * Pq);
+    if (rc != KDA_OK) return rc;
+    const uint32_t gen = kda::pool_new_stamp(pool);
+    rc = check_private(pool, active_pages, (int64_t)n * P, gen);
+    if (rc != KDA_OK) return rc;
+    for (int64_t i = 0; i < (int64_t)n * Pq; ++i)
+        if (pool->stamp[ckpt_pages[i]] == gen) return KDA_EREF;   // never convert onto the source
+    rc = kda::pool_incref(pool, n * Pq, ckpt_pages);
+    if (rc != KDA_OK) return rc;
+    rc = convert_q8(pool, H, d, dtype, n, active_pages, ckpt_pages, pool_base, workspace, status_dev,
+                    static_cast<cudaStream_t>(stream), false);
+    if (rc != KDA_OK) kda::pool_decref(pool, n * Pq, ckpt_pages);
+    return rc;
+}
+
 int kda_sync_status(int32_t *status_dev, void *stream, int32_t *bits_out) {
     if (!status_dev) return KDA_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

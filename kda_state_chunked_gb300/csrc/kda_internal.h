@@ -106,6 +106,15 @@ struct CopyArgs {
     int32_t *status;
 };
 
+// INT8 checkpoint conversion between full-precision objects and INT8 checkpoint objects.
+struct Q8Args {
+    int32_t n, H, d, dtype;
+    PoolView full, q8;            // geometry of the full-precision and of the INT8 objects
+    const int32_t *full_pages;    // [n * full.pages_per_object]
+    const int32_t *q8_pages;      // [n * q8.pages_per_object]
+    int32_t *status;
+};
+
 // Streams and events for overlapping the two kernels of the split prefill: chunk preparation
 // on `side` (low priority), chains on `main` (high priority), joined back to the caller's
 // stream (side == nullptr: everything on the caller's stream).
@@ -126,5 +135,7 @@ inline cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
 }
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_copy_objects(const CopyArgs &a, cudaStream_t s);
+cudaError_t launch_ckpt_quantize(const Q8Args &a, cudaStream_t s);
+cudaError_t launch_ckpt_dequantize(const Q8Args &a, cudaStream_t s);
 
 }  // namespace kda

@@ -226,3 +226,31 @@ def test_split_prefill_plan_launches_and_workspace():
     assert kda.kda_prefill_workspace_bytes(16, 128, f32, cu, st, 16, 17) < (1 << 20)
     with pytest.raises(kda.KdaError):
         kda.kda_prefill_kernel_launches(16, 128, bf, [0, 10, 5], [0, 0])      # decreasing offsets
+
+
+def test_q8_sizes_match_oracle_and_bad_arguments_are_refused():
+    from oracle import q8
+    for d, dt in [(128, "bf16"), (64, "f32"), (128, "f32"), (64, "bf16")]:
+        assert kda.kda_record_bytes_q8(d, kda.DTYPES[dt]) == q8.record_bytes(d, dt)
+        assert kda.kda_object_bytes_q8(5, d, kda.DTYPES[dt]) == q8.object_bytes(5, d, dt)
+    pool = kda.Pool(65536, 64)
+    assert kda.kda_object_pages_q8(pool, 32, 128, kda.KDA_BF16) == q8.object_pages(32, 128, "bf16", 65536) == 10
+    L = kda.lib()
+    dummy = ctypes.c_void_p(16)
+    ids = np.zeros(64, dtype=np.int32)
+    out = np.zeros(64, dtype=np.int32)
+    # bad shape, missing buffers, short workspace: refused before anything is enqueued
+    assert L.kda_ckpt_write_q8(pool.handle, 2, 96, kda.KDA_BF16, 1, kda._ptr(ids), kda._ptr(out), dummy, dummy,
+                               1 << 20, dummy, None) == kda.KDA_EINVAL
+    assert L.kda_ckpt_write_q8(pool.handle, 2, 128, kda.KDA_BF16, 1, None, kda._ptr(out), dummy, dummy,
+                               1 << 20, dummy, None) == kda.KDA_EINVAL
+    assert L.kda_ckpt_write_q8(pool.handle, 2, 128, kda.KDA_BF16, 1, kda._ptr(ids), kda._ptr(out), dummy, dummy,
+                               8, dummy, None) == kda.KDA_EINVAL
+    # unallocated source pages: refcount error, nothing allocated
+    free0 = pool.free_count()
+    assert L.kda_ckpt_write_q8(pool.handle, 2, 128, kda.KDA_BF16, 1, kda._ptr(ids), kda._ptr(out), dummy, dummy,
+                               1 << 20, dummy, None) == kda.KDA_EREF
+    assert pool.free_count() == free0
+    # restore onto pages that are not private
+    assert L.kda_ckpt_restore_q8(pool.handle, 2, 128, kda.KDA_BF16, 1, kda._ptr(ids), kda._ptr(ids), dummy, dummy,
+                                 1 << 20, dummy, None) in (kda.KDA_EREF, kda.KDA_EINVAL)
