@@ -251,14 +251,34 @@ def _decode_phase(dev, steps=64, warmup=3):
 
     total, per = _time_steps(one, steps, warmup, stream)
     assert kda.kda_sync_status(st)[0] == kda.KDA_OK
-    rec = kda.kda_record_bytes(w.d, dt)
     es = 2
     bytes_per = w.nseq * w.H * (2 * w.d * w.d * 4 + 2 * 3 * 3 * w.d * es + 4 * w.d * es + es + w.d * es)
-    del rec
     us = statistics.median(per) * 1e3
+    del pool
+    # ping-pong: every request writes its new state to its second object (all of them at a
+    # decode-checkpoint boundary), alternating between two permuted page tables
+    pool2 = kda.Pool(w.page_bytes, 2 * w.nseq * P, dev)
+    pool2.base.zero_()
+    both = workloads.permuted_page_table(2 * w.nseq * P, 2 * w.nseq, P, w.seed)
+    kda.kda_page_claim(pool2, both.reshape(-1))
+    ta, tb = both[:w.nseq].to(dev), both[w.nseq:].to(dev)
+    it2 = iter(range(10 ** 9))
+
+    def one_pp():
+        i = next(it2)
+        t = step_toks[i % steps]
+        src, dst = (ta, tb) if i % 2 == 0 else (tb, ta)
+        kda.kda_decode_step_pp(pool2, t["q"], t["k"], t["v"], t["alpha"], t["beta"], conv_w, od, src, dst, st)
+
+    _, per_pp = _time_steps(one_pp, steps, warmup, stream)
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+    us_pp = statistics.median(per_pp) * 1e3
     return {"step_us": us, "mean_step_us": total * 1e3 / steps, "steps": steps, "B": w.nseq, "H": w.H,
             "bytes_per_step": bytes_per, "achieved_gbs": bytes_per / (us * 1e-6) / 1e9,
-            "l2": "state set 1.1 GB per step > L2"}
+            "l2": "state set 1.1 GB per step > L2",
+            "pingpong": {"step_us": us_pp, "achieved_gbs": bytes_per / (us_pp * 1e-6) / 1e9,
+                         "note": "every request writes its next state to a second object (a decode checkpoint "
+                                 "by donation at every step)"}}
 
 
 def _ckpt_io_phase(dev, n=256, reps=5):

@@ -241,6 +241,36 @@ int kda_decode_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, i
                     const void *beta, const float *conv_w, void *o, void *pool_base,
                     const int32_t *state_pages, int32_t *status_dev, void *stream);
 
+/* Ping-pong decode step: as kda_decode_step, but each request's state is read from its
+ * source object (src_pages, device int32 [B * P]) and written, with the shifted window, to its
+ * destination object (dst_pages, device int32 [B * P]).  A request whose two page lists are
+ * equal is updated in place; for one whose lists differ (and do not overlap), the source
+ * object is left untouched and holds the state at the request's position: a decode-interval
+ * checkpoint taken without a copy, which the caller donates to the cache while the request
+ * continues on the destination object ("KIMI K3 경량 복제에서 본 KDA의 AI 인프라 과제", §0x05
+ * 5.2: decode checkpoints at a fixed interval; §0x06 6.7 and 6.8: a second slot requested at a
+ * checkpoint boundary, the new state written to it, the old slot donated).  Page ids outside
+ * the pool in either list set KDA_DEV_BAD_PAGE and the request is skipped. */
+int kda_decode_step_pp(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B,
+                       const void *q, const void *k, const void *v, const void *alpha,
+                       const void *beta, const float *conv_w, void *o, void *pool_base,
+                       const int32_t *src_pages, const int32_t *dst_pages, int32_t *status_dev,
+                       void *stream);
+
+/* Host plan of a ping-pong step at decode-checkpoint interval `interval`:
+ *   pos           host int64 [B]: tokens each request has consumed (its state's position)
+ *   active_pages  host int32 [B * P]: the requests' active objects (private: refcount 1)
+ * Requests with pos > 0 and pos % interval == 0 are due: for each of them, in request order,
+ * P fresh pages are allocated (lowest free first, refcount 1) as the destination object, and
+ * the request index is appended to donated_out (host int32 [B]; count in *n_donated_out).
+ * dst_pages_out (host int32 [B * P]) receives the destination lists: the fresh pages for due
+ * requests, the active pages for the others.  After the step, each due request's old active
+ * pages hold its checkpoint at position pos[r] and its new active object is the destination.
+ * All or nothing: KDA_ENOPAGES allocates nothing. */
+int kda_decode_pingpong_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B,
+                             const int64_t *pos, int32_t interval, const int32_t *active_pages,
+                             int32_t *dst_pages_out, int32_t *donated_out, int32_t *n_donated_out);
+
 /* ---------------------------------------------------------------- checkpoints --------- */
 
 /* Workspace bytes for a checkpoint copy of n objects. */

@@ -55,6 +55,9 @@ _SIGS = {
                                                   _P, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P]),
     "kda_decode_step": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                        _P, _P, _P, _P]),
+    "kda_decode_step_pp": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                          _P, _P, _P, _P, _P]),
+    "kda_decode_pingpong_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _I32, _P, _P, _P, _P]),
     "kda_copy_workspace_bytes": (_I64, [_I32, _I32]),
     "kda_ckpt_write": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P]),
     "kda_ckpt_restore": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P]),
@@ -332,6 +335,32 @@ def kda_decode_step(pool: Pool, q, k, v, alpha, beta, conv_w, o, state_pages, st
                                _dev(alpha), _dev(beta), _dev(conv_w), _dev(o), _dev(pool.base),
                                _dev(state_pages), _dev(status), _stream(stream))
     _check(rc, "kda_decode_step")
+
+
+def kda_decode_step_pp(pool: Pool, q, k, v, alpha, beta, conv_w, o, src_pages, dst_pages, status,
+                       stream=None) -> None:
+    """Ping-pong decode step: read each request's state from src_pages, write it to dst_pages
+    (both int32 CUDA [B, P]); requests whose lists are equal update in place."""
+    B, H, d = q.shape
+    rc = lib().kda_decode_step_pp(pool.handle, H, d, dtype_of(q), B, _dev(q), _dev(k), _dev(v),
+                                  _dev(alpha), _dev(beta), _dev(conv_w), _dev(o), _dev(pool.base),
+                                  _dev(src_pages), _dev(dst_pages), _dev(status), _stream(stream))
+    _check(rc, "kda_decode_step_pp")
+
+
+def kda_decode_pingpong_plan(pool: Pool, H: int, d: int, dtype: int, pos, interval: int, active_pages):
+    """-> (dst_pages [B, P], donated request indices): fresh destination objects for the
+    requests at a decode-checkpoint boundary (pos > 0, pos % interval == 0)."""
+    act = _i32(active_pages)
+    P = kda_object_pages(pool, H, d, dtype)
+    B = len(act) // P
+    p = _i64(pos)
+    dst = np.zeros(max(B * P, 1), dtype=np.int32)
+    don = np.zeros(max(B, 1), dtype=np.int32)
+    n = ctypes.c_int32(0)
+    _check(lib().kda_decode_pingpong_plan(pool.handle, H, d, dtype, B, _ptr(p), interval, _ptr(act), _ptr(dst),
+                                          _ptr(don), ctypes.byref(n)), "kda_decode_pingpong_plan")
+    return dst[:B * P].reshape(B, P), don[:n.value]
 
 
 # ------------------------------------------------------------------------------ copies

@@ -385,22 +385,57 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
     return kda::launch_prefill_split(sa, plan, st, side_stream(pool)) == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
-int kda_decode_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B,
-                    const void *q, const void *k, const void *v, const void *alpha,
-                    const void *beta, const float *conv_w, void *o, void *pool_base,
-                    const int32_t *state_pages, int32_t *status_dev, void *stream) {
+int kda_decode_step_pp(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, const void *q,
+                       const void *k, const void *v, const void *alpha, const void *beta, const float *conv_w,
+                       void *o, void *pool_base, const int32_t *src_pages, const int32_t *dst_pages,
+                       int32_t *status_dev, void *stream) {
     if (!pool || !valid_shape(H, d, dtype) || B < 0 || (int64_t)B * H > INT32_MAX || !status_dev)
         return KDA_EINVAL;
     if (B == 0) return KDA_OK;
-    if (!q || !k || !v || !alpha || !beta || !conv_w || !o || !pool_base || !state_pages)
+    if (!q || !k || !v || !alpha || !beta || !conv_w || !o || !pool_base || !src_pages || !dst_pages)
         return KDA_EINVAL;
     kda::DecodeArgs a;
     a.H = H; a.d = d; a.dtype = dtype; a.B = B;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.conv_w = conv_w; a.o = o;
     a.pool = pool_view(pool, pool_base, H, d, dtype);
-    a.state_pages = state_pages;
+    a.state_pages = src_pages;
+    a.dst_pages = dst_pages;
     a.status = status_dev;
     return kda::launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+
+int kda_decode_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, const void *q,
+                    const void *k, const void *v, const void *alpha, const void *beta, const float *conv_w, void *o,
+                    void *pool_base, const int32_t *state_pages, int32_t *status_dev, void *stream) {
+    return kda_decode_step_pp(pool, H, d, dtype, B, q, k, v, alpha, beta, conv_w, o, pool_base, state_pages,
+                              state_pages, status_dev, stream);
+}
+
+int kda_decode_pingpong_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, const int64_t *pos,
+                             int32_t interval, const int32_t *active_pages, int32_t *dst_pages_out,
+                             int32_t *donated_out, int32_t *n_donated_out) {
+    if (!pool || !valid_shape(H, d, dtype) || B < 0 || interval <= 0 || !n_donated_out) return KDA_EINVAL;
+    *n_donated_out = 0;
+    if (B == 0) return KDA_OK;
+    if (!pos || !active_pages || !dst_pages_out || !donated_out) return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype);
+    std::vector<int32_t> due;
+    for (int32_t r = 0; r < B; ++r) {
+        if (pos[r] < 0) return KDA_EINVAL;
+        if (pos[r] > 0 && pos[r] % interval == 0) due.push_back(r);
+    }
+    std::lock_guard<std::mutex> g(pool->mu);
+    const uint32_t gen = kda::pool_new_stamp(pool);
+    int rc = check_private(pool, active_pages, (int64_t)B * P, gen);
+    if (rc != KDA_OK) return rc;
+    if ((int64_t)pool->free_n < (int64_t)due.size() * P) return KDA_ENOPAGES;
+    std::memcpy(dst_pages_out, active_pages, (size_t)B * P * 4);
+    for (size_t i = 0; i < due.size(); ++i) {
+        kda::pool_alloc(pool, P, dst_pages_out + (size_t)due[i] * P);
+        donated_out[i] = due[i];
+    }
+    *n_donated_out = (int32_t)due.size();
+    return KDA_OK;
 }
 
 int64_t kda_copy_workspace_bytes(int32_t n, int32_t pages_per_object) {

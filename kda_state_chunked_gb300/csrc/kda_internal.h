@@ -93,7 +93,8 @@ struct DecodeArgs {
     const float *conv_w;
     void *o;
     PoolView pool;
-    const int32_t *state_pages;   // [B * P]
+    const int32_t *state_pages;   // [B * P] read
+    const int32_t *dst_pages;     // [B * P] written (== state_pages for the in-place step)
     int32_t *status;
 };
 

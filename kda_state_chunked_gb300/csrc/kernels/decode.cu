@@ -1,12 +1,15 @@
 // Batched single-token KDA decode step over states gathered through a page table.
 //
-// Per (request, head): conv of the new token with the stored window (the window is shifted
-// in place), then S' = Diag(alpha) S, w = beta (v - S'^T k), S = S' + k w^T, o = S^T q, with
-// S written back in place.  The order (decay, delta write, read) follows "Lesson 01 ·
-// Architecture map", §两种 Attention，两种状态; the fused conv + recurrent decode on the
-// state indices follows "KIMI K3 경량 복제에서 본 KDA의 AI 인프라 과제" §0x08 8.2.2 and the
-// block-table gather of "Chapitre 8 — Gestion nouvelle génération du cache KV" §8.1
-// (PagedAttention: logical blocks mapped to physical pages through a table).
+// Per (request, head): conv of the new token with the stored window (the window shifts by one
+// token), then S' = Diag(alpha) S, w = beta (v - S'^T k), S = S' + k w^T, o = S^T q.  The state
+// is read from the request's source object and written to its destination object: the same
+// object for the in-place step; another one for the ping-pong step, which leaves the source
+// object as a checkpoint at the request's position.  The order (decay, delta write, read)
+// follows "Lesson 01 · Architecture map", §两种 Attention，两种状态; the fused conv + recurrent
+// decode on the state indices follows "KIMI K3 경량 복제에서 본 KDA의 AI 인프라 과제" §0x08
+// 8.2.2, the second (ping-pong) slot at a decode checkpoint boundary §0x06 6.7 and 6.8, and the
+// block-table gather "Chapitre 8 — Gestion nouvelle génération du cache KV" §8.1 (PagedAttention:
+// logical blocks mapped to physical pages through a table).
 //
 // The step is HBM-bound (about 0.84 flop per byte): every state streams in and out once.
 // Two kernels:
@@ -67,8 +70,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
     const int32_t *pages = a.state_pages + (int64_t)b * a.pool.pages_per_object;
+    const int32_t *dpages = a.dst_pages + (int64_t)b * a.pool.pages_per_object;
     if (tid == 0) {
-        ok_s = pages_ok(a.pool, pages);
+        ok_s = pages_ok(a.pool, pages) && pages_ok(a.pool, dpages);
         if (!ok_s) flag_status(a.status, KDA_DEV_BAD_PAGE);
     }
     __syncthreads();
@@ -87,24 +91,30 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
         vload<VEC>(p, s[rr]);
     }
 
-    // Conv of the new token against the stored window, then shift the window in place.
+    // Conv of the new token against the stored window; the shifted window goes to the
+    // destination object (the same object for the in-place step).
     const T *qp = static_cast<const T *>(a.q), *kp = static_cast<const T *>(a.k),
             *vp = static_cast<const T *>(a.v);
     for (int c = tid; c < C3; c += kDecThreads) {
         const T *src = c < D ? qp + tok + c : (c < 2 * D ? kp + tok + (c - D) : vp + tok + (c - 2 * D));
         const float x = ld_elem(src);
         const float4 w = *reinterpret_cast<const float4 *>(a.conv_w + ((int64_t)h * C3 + c) * 4);
-        T *wp[kWin];
+        T pr[kWin];
         float pv[kWin];
 #pragma unroll
         for (int u = 0; u < kWin; ++u) {
-            wp[u] = reinterpret_cast<T *>(obj_addr(a.pool, pages, win_off + ((uint64_t)u * C3 + c) * sizeof(T), a.status));
-            pv[u] = ld_elem(wp[u]);
+            pr[u] = *reinterpret_cast<const T *>(obj_addr(a.pool, pages, win_off + ((uint64_t)u * C3 + c) * sizeof(T), a.status));
+            pv[u] = ld_elem(&pr[u]);
         }
         xb[c] = w.x * pv[0] + w.y * pv[1] + w.z * pv[2] + w.w * x;
-        *wp[0] = *wp[1];
-        *wp[1] = *wp[2];
-        *wp[2] = *src;
+        // every thread has read its window values before any is overwritten (one thread per channel)
+        T *wd[kWin];
+#pragma unroll
+        for (int u = 0; u < kWin; ++u)
+            wd[u] = reinterpret_cast<T *>(obj_addr(a.pool, dpages, win_off + ((uint64_t)u * C3 + c) * sizeof(T), a.status));
+        *wd[0] = pr[1];
+        *wd[1] = pr[2];
+        *wd[2] = *src;
     }
     const T *ap = static_cast<const T *>(a.alpha);
     for (int i = tid; i < D; i += kDecThreads) al[i] = ld_elem(ap + tok + i);
@@ -136,7 +146,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
     }
     __syncthreads();
 
-    // S = S' + k w^T, written back in place, and the partial sums of S^T q.
+    // S = S' + k w^T, written to the destination object, and the partial sums of S^T q.
     float wl[VEC], po[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) { wl[v] = wv[lane * VEC + v]; po[v] = 0.f; }
@@ -149,7 +159,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) decode_kernel(DecodeArgs a) {
             s[rr][v] = fmaf(ki, wl[v], s[rr][v]);
             po[v] = fmaf(qi, s[rr][v], po[v]);
         }
-        uint8_t *p = obj_addr(a.pool, pages, rec + ((uint64_t)i * D + lane * VEC) * 4, a.status);
+        uint8_t *p = obj_addr(a.pool, dpages, rec + ((uint64_t)i * D + lane * VEC) * 4, a.status);
         vstore<VEC>(p, s[rr]);
     }
 #pragma unroll
@@ -176,7 +186,7 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
 // the (request, head) items with a three-slot ring: a producer warp bulk-loads the record of
 // item n + 2 (split at page boundaries) and the new token's q, k, v, alpha while sixteen
 // compute warps update item n in shared memory; the producer then bulk-stores the updated
-// record in place.  Every SM thus keeps a record load and a record store in flight.
+// record to its destination.  Every SM thus keeps a record load and a record store in flight.
 constexpr int kDtCompute = 512;                  // 16 compute warps
 constexpr int kDtThreads = kDtCompute + 32;      // + producer warp
 constexpr int kDtSlots = 3;
@@ -225,9 +235,9 @@ __global__ void __launch_bounds__(kDtThreads, 1) decode_tma_kernel(DecodeArgs a)
                                       static_cast<const __nv_bfloat16 *>(a.v),
                                       static_cast<const __nv_bfloat16 *>(a.alpha)};
         // walk the record of `item` piece by piece (at most one piece per page it touches)
-        auto record_pieces = [&](int item, auto &&fn) {
+        auto record_pieces = [&](const int32_t *list, int item, auto &&fn) {
             const int r = item / a.H, hh = item % a.H;
-            const int32_t *pages = a.state_pages + (int64_t)r * a.pool.pages_per_object;
+            const int32_t *pages = list + (int64_t)r * a.pool.pages_per_object;
             int64_t off = (int64_t)hh * a.pool.rec_bytes;
             uint32_t done_b = 0;
             while (done_b < kDtRec) {
@@ -241,7 +251,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) decode_tma_kernel(DecodeArgs a)
         auto store_item = [&](int n) {
             const int item = blockIdx.x + n * gridDim.x, b = n % kDtSlots;
             if (!valid[b]) return;
-            record_pieces(item, [&](int32_t page, int64_t in, uint32_t at, uint32_t len) {
+            record_pieces(a.dst_pages, item, [&](int32_t page, int64_t in, uint32_t at, uint32_t len) {
                 ptx::bulk_store(a.pool.base + (int64_t)page * PB + in, sm + b * kDtSlot + at, len);
             });
             ptx::bulk_commit();
@@ -269,8 +279,10 @@ __global__ void __launch_bounds__(kDtThreads, 1) decode_tma_kernel(DecodeArgs a)
             }
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
             const int32_t *pages = a.state_pages + (int64_t)(item / a.H) * a.pool.pages_per_object;
+            const int32_t *dpages = a.dst_pages + (int64_t)(item / a.H) * a.pool.pages_per_object;
             bool ok = true;
-            for (int i = lane; i < a.pool.pages_per_object; i += 32) ok = ok && (uint32_t)pages[i] < (uint32_t)a.pool.num_pages;
+            for (int i = lane; i < a.pool.pages_per_object; i += 32)
+                ok = ok && (uint32_t)pages[i] < (uint32_t)a.pool.num_pages && (uint32_t)dpages[i] < (uint32_t)a.pool.num_pages;
             ok = __all_sync(0xffffffffu, ok);
             if (lane == 0) {
                 valid[b] = ok ? 1 : 0;
@@ -279,7 +291,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) decode_tma_kernel(DecodeArgs a)
                     ptx::mbar_arrive(&full[b]);
                 } else {
                     ptx::mbar_arrive_expect_tx(&full[b], kDtSlot);
-                    record_pieces(item, [&](int32_t page, int64_t in, uint32_t at, uint32_t len) {
+                    record_pieces(a.state_pages, item, [&](int32_t page, int64_t in, uint32_t at, uint32_t len) {
                         ptx::bulk_load(sm + b * kDtSlot + at, a.pool.base + (int64_t)page * PB + in, len, &full[b]);
                     });
                     const int64_t tok = (int64_t)item * D;   // [B][H][D] with item = r * H + h
@@ -321,7 +333,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) decode_tma_kernel(DecodeArgs a)
             __nv_bfloat16 *win = reinterpret_cast<__nv_bfloat16 *>(slot + D * D * 4);
             const __nv_bfloat16 *xin = reinterpret_cast<const __nv_bfloat16 *>(slot + kDtRec);
             if (valid[b]) {
-                // conv of the new token with the window; the window shifts in place
+                // conv of the new token with the window; the window shifts in the slot
                 if (tid < C3) {
                     const int c = tid;
                     const float x = __bfloat162float(xin[c]);
@@ -348,7 +360,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) decode_tma_kernel(DecodeArgs a)
                 const float u = (red[j] + red[D + j]) + (red[2 * D + j] + red[3 * D + j]);
                 const float wj = beta_s[b] * (xb[2 * D + j] - u);
                 named_bar(kDtBar, kDtCompute);   // red is reused below
-                // S = S' + k w^T in place, and the partial sums of S^T q
+                // S = S' + k w^T in the slot, and the partial sums of S^T q
                 float ao = 0.f;
 #pragma unroll
                 for (int ii = 0; ii < 32; ++ii) {

@@ -56,6 +56,26 @@ def ckpt_positions(start: int, end: int, hash_block: int = 512, stride: int = 1,
     return out
 
 
+def decode_ckpt_due(pos: int, interval: int) -> bool:
+    """A decode step that starts from `pos` consumed tokens keeps the state at `pos` as a
+    checkpoint when pos is a positive multiple of the interval ("KIMI K3 경량 복제에서 본 KDA의
+    AI 인프라 과제", §0x05 5.2: decode checkpoints at a fixed interval)."""
+    return pos > 0 and pos % interval == 0
+
+
+def pingpong_plan(pool: "PoolSim", pos: list[int], interval: int, active: list[list[int]],
+                  pages_per_object: int):
+    """Destination page lists of a ping-pong step: fresh pages (lowest free first, in request
+    order) for the requests that are due, the active pages for the others."""
+    due = [r for r, p in enumerate(pos) if decode_ckpt_due(p, interval)]
+    if pool.free_count() < len(due) * pages_per_object:
+        raise AllocError("no pages")
+    dst = [list(a) for a in active]
+    for r in due:
+        dst[r] = pool.alloc(pages_per_object)
+    return dst, due
+
+
 def hit_boundary(stored: list[int], matched: int) -> int:
     """Resume point: the largest stored checkpoint position not above the matched length
     (0, a fresh start, when none qualifies)."""

@@ -254,3 +254,43 @@ def test_q8_sizes_match_oracle_and_bad_arguments_are_refused():
     # restore onto pages that are not private
     assert L.kda_ckpt_restore_q8(pool.handle, 2, 128, kda.KDA_BF16, 1, kda._ptr(ids), kda._ptr(ids), dummy, dummy,
                                  1 << 20, dummy, None) in (kda.KDA_EREF, kda.KDA_EINVAL)
+
+
+def test_pingpong_plan_matches_oracle_under_random_positions():
+    rng = np.random.default_rng(7)
+    H, d, dt = 4, 64, kda.KDA_F32
+    for trial in range(20):
+        pool = kda.Pool(8192, 400)
+        sim = policy.PoolSim(400)
+        P = pool.object_pages(H, d, dt)
+        B = int(rng.integers(1, 12))
+        # some noise in the pool first, mirrored in the simulation
+        noise = int(rng.integers(0, 30))
+        kda.kda_page_alloc(pool, noise)
+        sim.alloc(noise)
+        act = kda.kda_page_alloc(pool, B * P).reshape(B, P)
+        act_sim = [sim.alloc(P) for _ in range(B)]
+        assert [list(a) for a in act] == act_sim
+        interval = int(rng.integers(1, 9))
+        pos = [int(x) for x in rng.integers(0, 40, size=B)]
+        dst, don = kda.kda_decode_pingpong_plan(pool, H, d, dt, pos, interval, act)
+        dst_sim, due = policy.pingpong_plan(sim, pos, interval, act_sim, P)
+        assert list(don) == due
+        assert [list(x) for x in dst] == dst_sim
+        assert pool.free_count() == sim.free_count()
+
+
+def test_pingpong_plan_is_all_or_nothing_and_checks_ownership():
+    H, d, dt = 2, 64, kda.KDA_F32
+    pool = kda.Pool(65536, 3)                      # one page per object, one page free
+    P = pool.object_pages(H, d, dt)
+    assert P == 1
+    act = kda.kda_page_alloc(pool, 2 * P).reshape(2, P)
+    free0 = pool.free_count()
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_decode_pingpong_plan(pool, H, d, dt, [8, 8], 4, act)      # needs 2 objects, 1 fits
+    assert e.value.code == kda.KDA_ENOPAGES and pool.free_count() == free0
+    kda.kda_page_incref(pool, act[0])                                     # shared: not private
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_decode_pingpong_plan(pool, H, d, dt, [1, 1], 4, act)
+    assert e.value.code == kda.KDA_EREF

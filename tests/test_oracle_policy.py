@@ -190,3 +190,24 @@ def test_plan_allocates_in_sequence_then_position_order():
     with pytest.raises(policy.AllocError):
         policy.plan_checkpoints(small, [(0, 2048)], 2, 512, 1, False)
     assert small.free_count() == 5
+
+
+def test_decode_checkpoint_interval():
+    """Decode keeps a checkpoint every `interval` tokens: the state a step starts from is kept
+    when its position is a positive multiple of the interval."""
+    assert not policy.decode_ckpt_due(0, 64)
+    assert policy.decode_ckpt_due(64, 64) and policy.decode_ckpt_due(128, 64)
+    assert not policy.decode_ckpt_due(65, 64) and not policy.decode_ckpt_due(63, 64)
+    assert [p for p in range(1, 20) if policy.decode_ckpt_due(p, 5)] == [5, 10, 15]
+
+
+def test_pingpong_plan_allocates_only_for_due_requests():
+    pool = policy.PoolSim(20)
+    active = [pool.alloc(2) for _ in range(4)]            # pages 0..7
+    dst, due = policy.pingpong_plan(pool, [3, 4, 8, 0], 4, active, 2)
+    assert due == [1, 2]
+    assert dst[0] == active[0] and dst[3] == active[3]
+    assert dst[1] == [8, 9] and dst[2] == [10, 11]        # lowest free first, request order
+    with pytest.raises(policy.AllocError):
+        policy.pingpong_plan(pool, [4, 4, 4, 4], 4, active, 4)   # 16 pages needed, 8 free
+    assert pool.free_count() == 8                          # nothing taken
