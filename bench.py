@@ -359,6 +359,31 @@ def _ckpt_io_phase(dev, n=256, reps=5):
     assert kda.kda_sync_status(st)[0] == kda.KDA_OK
     res["bytes_moved_q8"] = nbq
     res["q8_compression"] = kda.kda_object_bytes(H, d, dt) / kda.kda_object_bytes_q8(H, d, dt)
+    # write-back host offload and prefetch of the same objects through pinned, device-mapped
+    # host memory (CPU-GPU link; one object size per call)
+    nbo = kda.kda_object_bytes(H, d, dt) * n
+    host = torch.empty(nbo, dtype=torch.uint8).pin_memory()
+    for name in ("offload", "prefetch"):
+        for warm in (True, False):
+            count = 2 if warm else reps
+            made = []
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(count):
+                if name == "offload":
+                    kda.kda_ckpt_offload(pool, H, d, dt, src, host, ws[i % 4], st)
+                else:
+                    made.append(kda.kda_ckpt_prefetch(pool, H, d, dt, n, host, ws[i % 4], st))
+            b.record(stream)
+            torch.cuda.synchronize()
+            for m in made:
+                kda.kda_page_decref(pool, m.reshape(-1))
+            ms = a.elapsed_time(b) / count
+        res[name] = {"ms": ms, "gbs": nbo / (ms * 1e-3) / 1e9, "calls_timed": reps,
+                     "bytes": nbo, "link": "CPU-GPU (pinned host memory)"}
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
     return res
 
 

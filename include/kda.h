@@ -295,6 +295,30 @@ int kda_ckpt_restore(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_
 int kda_ckpt_release(kda_pool *pool, int32_t n, int32_t pages_per_object,
                      const int32_t *ckpt_pages);
 
+/* ---------------------------------------------------------------- host offload ------ */
+
+/* Write-back offload and prefetch of checkpoints ("Infrastructure pour le RL à un million de
+ * jetons", §La solution : découpler la rétention de la résidence GPU: an idle reusable prefix
+ * is written to CPU DRAM only when it leaves the GPU, and prefetched before its next reuse).
+ * The host buffer must be pinned and mapped into the device address space (cudaHostAlloc /
+ * cudaHostRegister; pinned torch tensors qualify) and 16-byte aligned; object i occupies
+ * bytes [i * B, (i + 1) * B) with B = kda_object_bytes(H, d, dtype), in the object's logical
+ * byte order (the same bytes as in the pool).
+ *
+ * Offload: copy the n objects (pages: host int32 [n * P], allocated) to host_dst; the pages
+ * stay allocated: the caller decrefs them once the stream has passed the copy (the eviction).
+ * workspace: device, at least kda_copy_workspace_bytes(n, P).  A host buffer that is not
+ * device-accessible returns KDA_EINVAL. */
+int kda_ckpt_offload(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n,
+                     const int32_t *pages, void *host_dst, int64_t host_bytes, void *pool_base,
+                     void *workspace, int64_t ws_bytes, int32_t *status_dev, void *stream);
+
+/* Prefetch: allocate n * P fresh pages (lowest free first, refcount 1; returned in pages_out,
+ * host int32 [n * P]) and copy the n host objects into them.  All or nothing. */
+int kda_ckpt_prefetch(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n,
+                      const void *host_src, int64_t host_bytes, int32_t *pages_out, void *pool_base,
+                      void *workspace, int64_t ws_bytes, int32_t *status_dev, void *stream);
+
 /* ---------------------------------------------------------------- INT8 checkpoints -- */
 
 /* INT8 compressed checkpoints ("KIMI K3 경량 복제에서 본 KDA의 AI 인프라 과제", §0x05 5.3 and

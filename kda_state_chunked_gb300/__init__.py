@@ -62,6 +62,8 @@ _SIGS = {
     "kda_ckpt_write": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P]),
     "kda_ckpt_restore": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P]),
     "kda_ckpt_release": (ctypes.c_int, [_P, _I32, _I32, _P]),
+    "kda_ckpt_offload": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _I64, _P, _P, _I64, _P, _P]),
+    "kda_ckpt_prefetch": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _I64, _P, _P, _P, _I64, _P, _P]),
     "kda_record_bytes_q8": (_I64, [_I32, _I32]),
     "kda_object_bytes_q8": (_I64, [_I32, _I32, _I32]),
     "kda_object_pages_q8": (_I32, [_P, _I32, _I32, _I32]),
@@ -399,6 +401,31 @@ def kda_ckpt_release(pool: Pool, ckpt_pages, pages_per_object: int) -> None:
     ck = _i32(ckpt_pages)
     _check(lib().kda_ckpt_release(pool.handle, len(ck) // pages_per_object, pages_per_object,
                                   _ptr(ck)), "kda_ckpt_release")
+
+
+# ------------------------------------------------------------------------------ host offload
+def kda_ckpt_offload(pool: Pool, H: int, d: int, dtype: int, pages, host, workspace, status, stream=None) -> None:
+    """Copy objects (pages [n, P]) into a pinned host uint8 tensor (object i at i * object_bytes)."""
+    pg = _i32(pages)
+    P = kda_object_pages(pool, H, d, dtype)
+    n = len(pg) // P
+    rc = lib().kda_ckpt_offload(pool.handle, H, d, dtype, n, _ptr(pg), ctypes.c_void_p(host.data_ptr()),
+                                host.numel() * host.element_size(), _dev(pool.base), _dev(workspace),
+                                workspace.numel() * workspace.element_size(), _dev(status), _stream(stream))
+    _check(rc, "kda_ckpt_offload")
+
+
+def kda_ckpt_prefetch(pool: Pool, H: int, d: int, dtype: int, n: int, host, workspace, status,
+                      stream=None) -> np.ndarray:
+    """Allocate n fresh objects and copy them in from a pinned host uint8 tensor; returns the
+    pages [n, P]."""
+    P = kda_object_pages(pool, H, d, dtype)
+    out = np.zeros(max(n * P, 1), dtype=np.int32)
+    rc = lib().kda_ckpt_prefetch(pool.handle, H, d, dtype, n, ctypes.c_void_p(host.data_ptr()),
+                                 host.numel() * host.element_size(), _ptr(out), _dev(pool.base), _dev(workspace),
+                                 workspace.numel() * workspace.element_size(), _dev(status), _stream(stream))
+    _check(rc, "kda_ckpt_prefetch")
+    return out[:n * P].reshape(n, P)
 
 
 # ------------------------------------------------------------------------------ INT8 checkpoints

@@ -588,6 +588,78 @@ int kda_ckpt_restore_q8(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int
     return rc;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Device address of a pinned, mapped host buffer (nullptr when it is not device-accessible).
+void *host_device_ptr(void *host) {
+    void *dev = nullptr;
+    if (cudaHostGetDevicePointer(&dev, host, 0) != cudaSuccess) {
+        cudaGetLastError();   // the failed query leaves a (non-sticky) error: clear it
+        return nullptr;
+    }
+    return dev;
+}
+
+int host_copy(kda_pool *p, int32_t H, int32_t d, int32_t dtype, int32_t n, const int32_t *pages, void *host,
+              void *pool_base, void *ws, int32_t *status, cudaStream_t stream, bool to_host) {
+    const int32_t P = kda_object_pages(p, H, d, dtype);
+    int rc = kda::stage_upload(p, pages, (size_t)n * P * 4, ws, stream);
+    if (rc != KDA_OK) return rc;
+    kda::HostCopyArgs a;
+    a.n = n;
+    a.object_bytes = kda_object_bytes(H, d, dtype);
+    a.pool = pool_view(p, pool_base, H, d, dtype);
+    a.pages = static_cast<const int32_t *>(ws);
+    a.host = static_cast<uint8_t *>(host);
+    a.to_host = to_host ? 1 : 0;
+    a.status = status;
+    return kda::launch_host_copy(a, stream) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_ckpt_offload(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n, const int32_t *pages,
+                     void *host_dst, int64_t host_bytes, void *pool_base, void *workspace, int64_t ws_bytes,
+                     int32_t *status_dev, void *stream) {
+    if (!pool || !valid_shape(H, d, dtype) || n < 0 || !pool_base || !workspace || !status_dev) return KDA_EINVAL;
+    if (n == 0) return KDA_OK;
+    if (!pages || !host_dst || host_bytes < (int64_t)n * kda_object_bytes(H, d, dtype)) return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype);
+    if (ws_bytes < kda_copy_workspace_bytes(n, P) || (uintptr_t)workspace % 16 != 0 || (uintptr_t)host_dst % 16 != 0)
+        return KDA_EINVAL;
+    void *dev = host_device_ptr(host_dst);
+    if (!dev) return KDA_EINVAL;
+    std::lock_guard<std::mutex> g(pool->mu);
+    int rc = check_allocated(pool, pages, (int64_t)n * P);
+    if (rc != KDA_OK) return rc;
+    return host_copy(pool, H, d, dtype, n, pages, dev, pool_base, workspace, status_dev,
+                     static_cast<cudaStream_t>(stream), true);
+}
+
+int kda_ckpt_prefetch(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n, const void *host_src,
+                      int64_t host_bytes, int32_t *pages_out, void *pool_base, void *workspace, int64_t ws_bytes,
+                      int32_t *status_dev, void *stream) {
+    if (!pool || !valid_shape(H, d, dtype) || n < 0 || !pool_base || !workspace || !status_dev) return KDA_EINVAL;
+    if (n == 0) return KDA_OK;
+    if (!pages_out || !host_src || host_bytes < (int64_t)n * kda_object_bytes(H, d, dtype)) return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype);
+    if (ws_bytes < kda_copy_workspace_bytes(n, P) || (uintptr_t)workspace % 16 != 0 || (uintptr_t)host_src % 16 != 0)
+        return KDA_EINVAL;
+    void *dev = host_device_ptr(const_cast<void *>(host_src));
+    if (!dev) return KDA_EINVAL;
+    std::lock_guard<std::mutex> g(pool->mu);
+    int rc = kda::pool_alloc(pool, n * P, pages_out);
+    if (rc != KDA_OK) return rc;
+    rc = host_copy(pool, H, d, dtype, n, pages_out, dev, pool_base, workspace, status_dev,
+                   static_cast<cudaStream_t>(stream), false);
+    if (rc != KDA_OK) kda::pool_decref(pool, n * P, pages_out);
+    return rc;
+}
+
 int kda_sync_status(int32_t *status_dev, void *stream, int32_t *bits_out) {
     if (!status_dev) return KDA_EINVAL;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -107,6 +107,18 @@ struct CopyArgs {
     int32_t *status;
 };
 
+// Object copy between the paged pool and device-mapped host memory (object i at host +
+// i * object_bytes).
+struct HostCopyArgs {
+    int32_t n;
+    int64_t object_bytes;
+    PoolView pool;
+    const int32_t *pages;         // [n * P]
+    uint8_t *host;                // device address of the host buffer
+    int32_t to_host;              // 1: pool -> host (offload), 0: host -> pool (prefetch)
+    int32_t *status;
+};
+
 // INT8 checkpoint conversion between full-precision objects and INT8 checkpoint objects.
 struct Q8Args {
     int32_t n, H, d, dtype;
@@ -136,6 +148,7 @@ inline cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
 }
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_copy_objects(const CopyArgs &a, cudaStream_t s);
+cudaError_t launch_host_copy(const HostCopyArgs &a, cudaStream_t s);
 cudaError_t launch_ckpt_quantize(const Q8Args &a, cudaStream_t s);
 cudaError_t launch_ckpt_dequantize(const Q8Args &a, cudaStream_t s);
 

@@ -294,3 +294,24 @@ def test_pingpong_plan_is_all_or_nothing_and_checks_ownership():
     with pytest.raises(kda.KdaError) as e:
         kda.kda_decode_pingpong_plan(pool, H, d, dt, [1, 1], 4, act)
     assert e.value.code == kda.KDA_EREF
+
+
+def test_offload_and_prefetch_refuse_bad_arguments():
+    pool = kda.Pool(65536, 16)
+    L = kda.lib()
+    dummy = ctypes.c_void_p(16)
+    ids = kda.kda_page_alloc(pool, 2)
+    H, d, dt = 1, 128, kda.KDA_BF16
+    nb = kda.kda_object_bytes(H, d, dt)
+    # host buffer too small, misaligned, or missing: refused before anything is enqueued
+    assert L.kda_ckpt_offload(pool.handle, H, d, dt, 1, kda._ptr(ids), dummy, nb - 16, dummy, dummy, 1 << 20,
+                              dummy, None) == kda.KDA_EINVAL
+    assert L.kda_ckpt_offload(pool.handle, H, d, dt, 1, kda._ptr(ids), ctypes.c_void_p(24), nb, dummy, dummy,
+                              1 << 20, dummy, None) == kda.KDA_EINVAL
+    assert L.kda_ckpt_offload(pool.handle, H, d, dt, 1, kda._ptr(ids), None, nb, dummy, dummy, 1 << 20,
+                              dummy, None) == kda.KDA_EINVAL
+    out = np.zeros(4, dtype=np.int32)
+    free0 = pool.free_count()
+    assert L.kda_ckpt_prefetch(pool.handle, H, d, dt, 1, dummy, nb - 16, kda._ptr(out), dummy, dummy, 1 << 20,
+                               dummy, None) == kda.KDA_EINVAL
+    assert pool.free_count() == free0
