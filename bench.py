@@ -273,12 +273,33 @@ def _decode_phase(dev, steps=64, warmup=3):
     _, per_pp = _time_steps(one_pp, steps, warmup, stream)
     assert kda.kda_sync_status(st)[0] == kda.KDA_OK
     us_pp = statistics.median(per_pp) * 1e3
+    del pool2
+    # speculative verify: K = 4 draft tokens per request, the state after each kept
+    K = 4
+    pool3 = kda.Pool(w.page_bytes, (K + 1) * w.nseq * P, dev)
+    pool3.base.zero_()
+    src3 = kda.kda_page_alloc(pool3, w.nseq * P).reshape(w.nseq, P)
+    inter3 = torch.from_numpy(kda.kda_verify_plan(pool3, w.H, w.d, dt, w.nseq, K)).to(dev)
+    src3_dev = torch.from_numpy(src3).to(dev)
+    drafts = {k: torch.stack([step_toks[j][k] for j in range(K)]) for k in step_toks[0]}
+    ov = torch.empty_like(drafts["q"])
+
+    def one_verify():
+        kda.kda_verify_step(pool3, drafts["q"], drafts["k"], drafts["v"], drafts["alpha"], drafts["beta"], conv_w,
+                            ov, src3_dev, inter3, st)
+
+    _, per_v = _time_steps(one_verify, steps, warmup, stream)
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+    us_v = statistics.median(per_v) * 1e3
     return {"step_us": us, "mean_step_us": total * 1e3 / steps, "steps": steps, "B": w.nseq, "H": w.H,
             "bytes_per_step": bytes_per, "achieved_gbs": bytes_per / (us * 1e-6) / 1e9,
             "l2": "state set 1.1 GB per step > L2",
             "pingpong": {"step_us": us_pp, "achieved_gbs": bytes_per / (us_pp * 1e-6) / 1e9,
                          "note": "every request writes its next state to a second object (a decode checkpoint "
-                                 "by donation at every step)"}}
+                                 "by donation at every step)"},
+            "verify": {"draft_tokens": K, "step_us": us_v, "draft_tokens_per_s": w.nseq * K / (us_v * 1e-6),
+                       "achieved_gbs": K * bytes_per / (us_v * 1e-6) / 1e9,
+                       "note": "K chained ping-pong steps; the state after every draft token kept in its own object"}}
 
 
 def _ckpt_io_phase(dev, n=256, reps=5):

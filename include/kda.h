@@ -271,6 +271,37 @@ int kda_decode_pingpong_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype
                              const int64_t *pos, int32_t interval, const int32_t *active_pages,
                              int32_t *dst_pages_out, int32_t *donated_out, int32_t *n_donated_out);
 
+/* Speculative verify ("KIMI K3 경량 복제에서 본 KDA의 AI 인프라 과제", §0x06 6.4: a verify pass
+ * carries intermediate-state indices next to the recurrent and conv states): K draft tokens per
+ * request are applied one after another and the state after each of them is kept in its own
+ * object, so that the state at any accepted length is available without recomputation.
+ *
+ * kda_verify_plan: allocate the K * B intermediate objects (lowest free first, refcount 1;
+ * all or nothing) into inter_pages_out, host int32 [K][B][P] (object of token j of request b
+ * at (j * B + b) * P). */
+int kda_verify_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, int32_t K,
+                    int32_t *inter_pages_out);
+
+/* kda_verify_step: q, k, v, alpha [K][B][H][d] and beta [K][B][H] (device, dtype; draft token
+ * major), o [K][B][H][d] written.  src_pages (device int32 [B * P]) holds each request's state
+ * before the drafts and is not modified; inter_pages (device int32 [K][B][P]) receives the
+ * state after draft token j.  1 <= K <= 64.  Runs as K stream-ordered ping-pong decode steps
+ * (kda_decode_step_pp): token j reads the object token j - 1 wrote. */
+int kda_verify_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, int32_t K,
+                    const void *q, const void *k, const void *v, const void *alpha,
+                    const void *beta, const float *conv_w, void *o, void *pool_base,
+                    const int32_t *src_pages, const int32_t *inter_pages, int32_t *status_dev,
+                    void *stream);
+
+/* kda_verify_accept (host only): accepted[b] in [0, K] draft tokens kept for request b.  The
+ * request's new active object is written to active_out (host int32 [B * P]): the source
+ * object when accepted[b] == 0, else the object of token accepted[b] - 1.  Every other object
+ * among the request's source and intermediates is released (decref).  Call it once the
+ * stream has passed the verify step. */
+int kda_verify_accept(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, int32_t K,
+                      const int32_t *accepted, const int32_t *src_pages, const int32_t *inter_pages,
+                      int32_t *active_out);
+
 /* ---------------------------------------------------------------- checkpoints --------- */
 
 /* Workspace bytes for a checkpoint copy of n objects. */

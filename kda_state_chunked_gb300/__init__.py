@@ -58,6 +58,10 @@ _SIGS = {
     "kda_decode_step_pp": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                           _P, _P, _P, _P, _P]),
     "kda_decode_pingpong_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _I32, _P, _P, _P, _P]),
+    "kda_verify_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _I32, _P]),
+    "kda_verify_step": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _P, _P, _P]),
+    "kda_verify_accept": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _I32, _P, _P, _P, _P]),
     "kda_copy_workspace_bytes": (_I64, [_I32, _I32]),
     "kda_ckpt_write": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P]),
     "kda_ckpt_restore": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _P, _P]),
@@ -363,6 +367,40 @@ def kda_decode_pingpong_plan(pool: Pool, H: int, d: int, dtype: int, pos, interv
     _check(lib().kda_decode_pingpong_plan(pool.handle, H, d, dtype, B, _ptr(p), interval, _ptr(act), _ptr(dst),
                                           _ptr(don), ctypes.byref(n)), "kda_decode_pingpong_plan")
     return dst[:B * P].reshape(B, P), don[:n.value]
+
+
+def kda_verify_plan(pool: Pool, H: int, d: int, dtype: int, B: int, K: int) -> np.ndarray:
+    """Intermediate objects of a verify step: pages [K, B, P]."""
+    P = kda_object_pages(pool, H, d, dtype)
+    out = np.zeros(max(K * B * P, 1), dtype=np.int32)
+    _check(lib().kda_verify_plan(pool.handle, H, d, dtype, B, K, _ptr(out)), "kda_verify_plan")
+    return out[:K * B * P].reshape(K, B, P)
+
+
+def kda_verify_step(pool: Pool, q, k, v, alpha, beta, conv_w, o, src_pages, inter_pages, status,
+                    stream=None) -> None:
+    """q, k, v, alpha, o: [K, B, H, d]; beta: [K, B, H]; src_pages int32 CUDA [B, P];
+    inter_pages int32 CUDA [K, B, P]."""
+    K, B, H, d = q.shape
+    rc = lib().kda_verify_step(pool.handle, H, d, dtype_of(q), B, K, _dev(q), _dev(k), _dev(v), _dev(alpha),
+                               _dev(beta), _dev(conv_w), _dev(o), _dev(pool.base), _dev(src_pages),
+                               _dev(inter_pages), _dev(status), _stream(stream))
+    _check(rc, "kda_verify_step")
+
+
+def kda_verify_accept(pool: Pool, H: int, d: int, dtype: int, accepted, src_pages, inter_pages) -> np.ndarray:
+    """Keep the object at each request's accepted length; release the rest.  Returns the new
+    active pages [B, P]."""
+    acc = _i32(accepted)
+    src = _i32(src_pages)
+    inter = _i32(inter_pages)
+    P = kda_object_pages(pool, H, d, dtype)
+    B = len(acc)
+    K = len(inter) // (B * P)
+    out = np.zeros(max(B * P, 1), dtype=np.int32)
+    _check(lib().kda_verify_accept(pool.handle, H, d, dtype, B, K, _ptr(acc), _ptr(src), _ptr(inter), _ptr(out)),
+           "kda_verify_accept")
+    return out[:B * P].reshape(B, P)
 
 
 # ------------------------------------------------------------------------------ copies

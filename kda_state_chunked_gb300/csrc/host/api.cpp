@@ -411,6 +411,66 @@ int kda_decode_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, i
                               state_pages, status_dev, stream);
 }
 
+int kda_verify_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, int32_t K,
+                    int32_t *inter_pages_out) {
+    if (!pool || !valid_shape(H, d, dtype) || B < 0 || K < 1 || K > 64 || (B > 0 && !inter_pages_out))
+        return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype);
+    const int64_t need = (int64_t)B * K * P;
+    if (need > INT32_MAX) return KDA_EINVAL;
+    std::lock_guard<std::mutex> g(pool->mu);
+    if ((int64_t)pool->free_n < need) return KDA_ENOPAGES;
+    return need ? kda::pool_alloc(pool, (int32_t)need, inter_pages_out) : KDA_OK;
+}
+
+int kda_verify_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, int32_t K, const void *q,
+                    const void *k, const void *v, const void *alpha, const void *beta, const float *conv_w, void *o,
+                    void *pool_base, const int32_t *src_pages, const int32_t *inter_pages, int32_t *status_dev,
+                    void *stream) {
+    if (!pool || !valid_shape(H, d, dtype) || B < 0 || K < 1 || K > 64 || !status_dev) return KDA_EINVAL;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !alpha || !beta || !conv_w || !o || !pool_base || !src_pages || !inter_pages)
+        return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype);
+    const int64_t e = elem_size(dtype), tok = (int64_t)B * H * d * e, btok = (int64_t)B * H * e;
+    for (int32_t j = 0; j < K; ++j) {
+        // draft token j of every request: state from the previous token's object (or the
+        // source), written to this token's object
+        const int32_t *src = j == 0 ? src_pages : inter_pages + (int64_t)(j - 1) * B * P;
+        const int32_t *dst = inter_pages + (int64_t)j * B * P;
+        auto at = [&](const void *base, int64_t stride) {
+            return static_cast<const void *>(static_cast<const uint8_t *>(base) + j * stride);
+        };
+        const int rc = kda_decode_step_pp(pool, H, d, dtype, B, at(q, tok), at(k, tok), at(v, tok), at(alpha, tok),
+                                          at(beta, btok), conv_w, static_cast<uint8_t *>(o) + j * tok, pool_base,
+                                          src, dst, status_dev, stream);
+        if (rc != KDA_OK) return rc;
+    }
+    return KDA_OK;
+}
+
+int kda_verify_accept(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, int32_t K,
+                      const int32_t *accepted, const int32_t *src_pages, const int32_t *inter_pages,
+                      int32_t *active_out) {
+    if (!pool || !valid_shape(H, d, dtype) || B < 0 || K < 1 || K > 64) return KDA_EINVAL;
+    if (B == 0) return KDA_OK;
+    if (!accepted || !src_pages || !inter_pages || !active_out) return KDA_EINVAL;
+    const int32_t P = kda_object_pages(pool, H, d, dtype);
+    for (int32_t b = 0; b < B; ++b)
+        if (accepted[b] < 0 || accepted[b] > K) return KDA_EINVAL;
+    std::vector<int32_t> drop;
+    drop.reserve((size_t)B * K * P);
+    for (int32_t b = 0; b < B; ++b) {
+        for (int32_t j = -1; j < K; ++j) {   // j = -1: the source object
+            const int32_t *obj = j < 0 ? src_pages + (int64_t)b * P : inter_pages + ((int64_t)j * B + b) * P;
+            if (j + 1 == accepted[b]) std::memcpy(active_out + (int64_t)b * P, obj, (size_t)P * 4);
+            else drop.insert(drop.end(), obj, obj + P);
+        }
+    }
+    std::lock_guard<std::mutex> g(pool->mu);
+    return kda::pool_decref(pool, (int32_t)drop.size(), drop.data());
+}
+
 int kda_decode_pingpong_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, const int64_t *pos,
                              int32_t interval, const int32_t *active_pages, int32_t *dst_pages_out,
                              int32_t *donated_out, int32_t *n_donated_out) {

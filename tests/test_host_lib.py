@@ -315,3 +315,27 @@ def test_offload_and_prefetch_refuse_bad_arguments():
     assert L.kda_ckpt_prefetch(pool.handle, H, d, dt, 1, dummy, nb - 16, kda._ptr(out), dummy, dummy, 1 << 20,
                                dummy, None) == kda.KDA_EINVAL
     assert pool.free_count() == free0
+
+
+def test_verify_plan_and_accept_keep_one_object_per_request():
+    H, d, dt = 2, 64, kda.KDA_F32
+    pool = kda.Pool(65536, 64)
+    P = pool.object_pages(H, d, dt)
+    B, K = 3, 4
+    src = kda.kda_page_alloc(pool, B * P).reshape(B, P)
+    inter = kda.kda_verify_plan(pool, H, d, dt, B, K)
+    assert inter.shape == (K, B, P)
+    # lowest free first, token-major
+    assert list(inter.reshape(-1)) == list(range(B * P, B * P + K * B * P))
+    used = pool.num_pages - pool.free_count()
+    act = kda.kda_verify_accept(pool, H, d, dt, [0, 2, 4], src, inter)
+    assert list(act[0]) == list(src[0]) and list(act[1]) == list(inter[1, 1]) and list(act[2]) == list(inter[3, 2])
+    assert pool.num_pages - pool.free_count() == B * P == used - B * K * P
+    for b in range(B):
+        assert all(kda.kda_page_refcount(pool, int(p)) == 1 for p in act[b])
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_verify_accept(pool, H, d, dt, [5, 0, 0], src, kda.kda_verify_plan(pool, H, d, dt, B, K))
+    assert e.value.code == kda.KDA_EINVAL
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_verify_plan(pool, H, d, dt, B, 64)      # more than the pool holds
+    assert e.value.code == kda.KDA_ENOPAGES
