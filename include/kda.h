@@ -149,7 +149,7 @@ int kda_ckpt_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n
  *                          the path for this shape needs metadata only: fp32 or d = 64)
  *   n_ckpt, pages_per_object      the checkpoint count of the call and kda_object_pages()
  * For bf16 with d = 128 the workspace also holds the chunk-operand images of the split
- * tensor-core prefill: two slots of at most ~48 MiB of images each (one image of 90,624 B per
+ * tensor-core prefill: two slots of at most ~384 MiB of images each (one image of 90,624 B per
  * (chunk, head) of a wave of chunks), plus the state handed between waves (64 KiB per
  * (sequence, head), when there is more than one wave) and the final conv windows.  Returns
  * the byte count, or KDA_EINVAL for a bad shape or inconsistent arrays. */
