@@ -31,7 +31,7 @@ METRIC = "KDA prefill tokens/s and decode step µs at B=256; % of tensor/HBM roo
 WORKLOAD = "batched"
 # sources of the dominant (prefill) kernel, for matching committed ncu traffic to the code
 PREFILL_SOURCES = ["kernels/prefill_split.cu", "kernels/tc_common.cuh", "kernels/sm100_ptx.cuh",
-                   "kernels/common.cuh", "kda_internal.h", "host/api.cpp"]
+                   "kernels/common.cuh", "kda_internal.h", "host/split_plan.cpp"]
 
 
 # --------------------------------------------------------------------------- helpers

@@ -22,7 +22,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_SOURCES = ["kernels/ckpt_copy.cu", "kernels/ckpt_q8.cu", "kernels/decode.cu", "kernels/prefill_simt.cu",
               "kernels/tc_selftest.cu", "kernels/prefill_tc.cu", "kernels/prefill_split.cu",
               "host/prefill_noalloc.cu"]
-CPP_SOURCES = ["host/pool.cpp", "host/api.cpp"]
+CPP_SOURCES = ["host/pool.cpp", "host/split_plan.cpp", "host/api.cpp"]
 
 
 def _cuda_home() -> str:

@@ -3,6 +3,7 @@
 python -m kda_state_chunked_gb300.profile_case prefill-batched --launches 2
 python -m kda_state_chunked_gb300.profile_case decode --launches 3
 python -m kda_state_chunked_gb300.profile_case ckpt-restore --launches 2
+python -m kda_state_chunked_gb300.profile_case ckpt-write-q8 --launches 2
 python -m kda_state_chunked_gb300.profile_case prefill-long-slice --launches 1
 
 Cases
@@ -10,6 +11,8 @@ Cases
   prefill-long-slice  one 65536-token slice of the long workload (H = 32), same layout
   decode              256 requests x 32 heads, 256 KiB pages, permuted page table
   ckpt-restore        256 objects x 32 heads copied checkpoint -> private, 64 KiB pages
+  ckpt-write-q8       the same objects quantised into INT8 checkpoints
+  ckpt-restore-q8     INT8 checkpoints dequantised into the private objects
 """
 from __future__ import annotations
 
@@ -73,9 +76,33 @@ def ckpt_restore(launches, dev, n=256):
     assert kda.kda_sync_status(st)[0] == kda.KDA_OK
 
 
+def ckpt_q8(launches, dev, n=256, restore=False):
+    H, d, dt = 32, 128, kda.KDA_BF16
+    pool = kda.Pool(65536, (launches + 3) * n * 34 + 64, dev)
+    P = pool.object_pages(H, d, dt)
+    Pq = kda.kda_object_pages_q8(pool, H, d, dt)
+    src = kda.kda_page_alloc(pool, n * P)
+    pool.base.zero_()
+    ws = torch.empty(kda.kda_copy_workspace_bytes(n, P), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ck = kda.kda_ckpt_write_q8(pool, H, d, dt, src, ws, st).reshape(-1)
+    torch.cuda.synchronize()
+    for _ in range(launches):
+        if restore:
+            kda.kda_ckpt_restore_q8(pool, H, d, dt, ck, src, ws, st)
+            torch.cuda.synchronize()
+            kda.kda_ckpt_release(pool, ck, Pq)
+        else:
+            made = kda.kda_ckpt_write_q8(pool, H, d, dt, src, ws, st)
+            torch.cuda.synchronize()
+            kda.kda_page_decref(pool, made.reshape(-1))
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill-batched", "prefill-long-slice", "decode", "ckpt-restore"])
+    ap.add_argument("case", choices=["prefill-batched", "prefill-long-slice", "decode", "ckpt-restore",
+                                     "ckpt-write-q8", "ckpt-restore-q8"])
     ap.add_argument("--launches", type=int, default=2)
     a = ap.parse_args()
     from kda_state_chunked_gb300.build import build
@@ -87,6 +114,10 @@ def main():
         prefill(65536, 1, 32, 4, a.launches, dev)
     elif a.case == "decode":
         decode(a.launches, dev)
+    elif a.case == "ckpt-write-q8":
+        ckpt_q8(a.launches, dev)
+    elif a.case == "ckpt-restore-q8":
+        ckpt_q8(a.launches, dev, restore=True)
     else:
         ckpt_restore(a.launches, dev)
     print("ok")
