@@ -149,7 +149,7 @@ int kda_ckpt_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t n
  *                          the path for this shape needs metadata only: fp32 or d = 64)
  *   n_ckpt, pages_per_object      the checkpoint count of the call and kda_object_pages()
  * For bf16 with d = 128 the workspace also holds the chunk-operand images of the split
- * tensor-core prefill: two slots of at most ~384 MiB of images each (one image of 90,624 B per
+ * tensor-core prefill: two slots of at most ~512 MiB of images each (one image of 82,432 B per
  * (chunk, head) of a wave of chunks), plus the state handed between waves (64 KiB per
  * (sequence, head), when there is more than one wave) and the final conv windows.  Returns
  * the byte count, or KDA_EINVAL for a bad shape or inconsistent arrays. */
@@ -159,10 +159,22 @@ int64_t kda_prefill_workspace_bytes(int32_t H, int32_t d, int32_t dtype, int32_t
 
 /* Number of kernel launches kda_prefill_varlen makes for this batch (same arguments as
  * kda_prefill_workspace_bytes; cu_seqlens / start_pos host arrays): one for fp32 or d = 64;
- * for bf16 with d = 128, two per wave of chunks (chunk preparation and chains), or one when
- * every sequence is empty.  KDA_EINVAL for a bad shape. */
+ * for bf16 with d = 128, two per wave of chunks (chunk preparation and chains, the
+ * preparation of a wave overlapping the chains of the one before), or one when every
+ * sequence is empty.
+ * KDA_EINVAL for a bad shape. */
 int32_t kda_prefill_kernel_launches(int32_t H, int32_t d, int32_t dtype, int32_t nseq,
                                     const int32_t *cu_seqlens, const int64_t *start_pos);
+
+/* The wave split of the bf16 d = 128 prefill for this batch (same arguments as
+ * kda_prefill_kernel_launches): wave w covers local chunks [wave_c0[w], wave_c0[w + 1]) of
+ * every sequence (local chunk 0 = the chunk holding start_pos).  Writes min(cap, W + 1) bounds
+ * to the host array wave_c0 (may be NULL when cap = 0) and returns the wave count W (0 when
+ * every sequence is empty, or for shapes that do not take the split path).  The split is
+ * chosen by a cost model among splits whose operand images fit one workspace slot; it changes
+ * speed only, never results.  KDA_EINVAL for a bad shape or inconsistent arrays. */
+int32_t kda_prefill_waves(int32_t H, int32_t d, int32_t dtype, int32_t nseq, const int32_t *cu_seqlens,
+                          const int64_t *start_pos, int32_t *wave_c0, int32_t cap);
 
 /* Chunked varlen prefill (chunk = 64 tokens, chunks aligned to absolute positions).
  *   H, d, dtype      heads, head dimension (64 or 128), dtype of the token tensors

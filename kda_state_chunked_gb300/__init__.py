@@ -49,6 +49,7 @@ _SIGS = {
                                      _P, _P, _P, _P]),
     "kda_prefill_workspace_bytes": (_I64, [_I32, _I32, _I32, _I32, _P, _P, _I32, _I32]),
     "kda_prefill_kernel_launches": (_I32, [_I32, _I32, _I32, _I32, _P, _P]),
+    "kda_prefill_waves": (_I32, [_I32, _I32, _I32, _I32, _P, _P, _P, _I32]),
     "kda_prefill_varlen": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
                                           _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _I64, _P, _P]),
     "kda_prefill_varlen_noalloc": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
@@ -272,6 +273,19 @@ def kda_prefill_kernel_launches(H: int, d: int, dtype: int, cu_seqlens, start_po
     sp = _i64(start_pos)
     return _check(lib().kda_prefill_kernel_launches(H, d, dtype, len(cu) - 1, _ptr(cu), _ptr(sp)),
                   "kda_prefill_kernel_launches")
+
+
+def kda_prefill_waves(H: int, d: int, dtype: int, cu_seqlens, start_pos) -> np.ndarray:
+    """Wave bounds of the bf16 d=128 prefill for this batch: wave w = local chunks
+    [b[w], b[w + 1]) of every sequence (empty for other shapes or only empty sequences)."""
+    cu = _i32(cu_seqlens)
+    sp = _i64(start_pos)
+    n = _check(lib().kda_prefill_waves(H, d, dtype, len(cu) - 1, _ptr(cu), _ptr(sp), None, 0), "kda_prefill_waves")
+    if n == 0:
+        return np.zeros(0, dtype=np.int32)
+    out = np.zeros(n + 1, dtype=np.int32)
+    _check(lib().kda_prefill_waves(H, d, dtype, len(cu) - 1, _ptr(cu), _ptr(sp), _ptr(out), n + 1), "kda_prefill_waves")
+    return out
 
 
 def prefill_workspace(q, cu_seqlens, start_pos, n_ckpt: int, pages_per_object: int):

@@ -32,6 +32,10 @@ kda::PoolView pool_view(const kda_pool *p, void *base, int32_t H, int32_t d, int
     v.num_pages = p->num_pages;
     v.pages_per_object = kda_object_pages(p, H, d, dtype);
     v.rec_bytes = kda_record_bytes(d, dtype);
+    v.page_shift = -1;
+    for (int32_t sh = 0; sh < 63; ++sh)
+        if (((int64_t)1 << sh) == p->page_bytes) v.page_shift = sh;
+    v.pad_ = 0;
     return v;
 }
 
@@ -80,42 +84,6 @@ WsLayout ws_layout(int64_t H, int64_t nseq, int64_t nck, int64_t P, const kda::S
         L.total = L.o_win + nseq * H * 9 * 128 * 2;
     }
     return L;
-}
-
-// The pool's second stream for the split prefill, created on first use; on another device
-// than the one it was created on, or if creation fails, the prefill runs on one stream.
-kda::SideStream side_stream(kda_pool *p) {
-    kda::SideStream ss;
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return ss;
-    if (!p->side && p->side_dev < 0) {
-        p->side_dev = dev;
-        int least = 0, greatest = 0;
-        bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess;
-        ok = ok && cudaStreamCreateWithPriority(&p->side, cudaStreamNonBlocking, least) == cudaSuccess;
-        ok = ok && cudaStreamCreateWithPriority(&p->main, cudaStreamNonBlocking, greatest) == cudaSuccess;
-        for (cudaEvent_t *e : {&p->ev_in, &p->ev_a, &p->ev_out, &p->ev_b[0], &p->ev_b[1]})
-            ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
-        if (!ok) {
-            for (cudaStream_t *st : {&p->side, &p->main}) {
-                if (*st) cudaStreamDestroy(*st);
-                *st = nullptr;
-            }
-            for (cudaEvent_t *e : {&p->ev_in, &p->ev_a, &p->ev_out, &p->ev_b[0], &p->ev_b[1]}) {
-                if (*e) cudaEventDestroy(*e);
-                *e = nullptr;
-            }
-        }
-    }
-    if (!p->side || dev != p->side_dev) return ss;
-    ss.side = p->side;
-    ss.main = p->main;
-    ss.ev_in = p->ev_in;
-    ss.ev_a = p->ev_a;
-    ss.ev_out = p->ev_out;
-    ss.ev_b[0] = p->ev_b[0];
-    ss.ev_b[1] = p->ev_b[1];
-    return ss;
 }
 
 // Metadata-only workspace of the fused kernels (also the layout the allocation-free path uses).
@@ -237,10 +205,21 @@ int32_t kda_prefill_kernel_launches(int32_t H, int32_t d, int32_t dtype, int32_t
         if (cu_seqlens[s + 1] < cu_seqlens[s] || start_pos[s] < 0) return KDA_EINVAL;
     kda::SplitPlan pl;
     make_split_plan(H, nseq, cu_seqlens, start_pos, pl);
-    if (pl.nwaves == 0) return 1;
-    int32_t n = 0;
-    for (int32_t w = 0; w < pl.nwaves; ++w) n += 1 + (pl.wave_begin[w + 1] > pl.wave_begin[w] ? 1 : 0);
-    return n;
+    // chunk preparation and chains per wave; every wave has at least one item
+    return pl.nwaves == 0 ? 1 : 2 * pl.nwaves;
+}
+
+int32_t kda_prefill_waves(int32_t H, int32_t d, int32_t dtype, int32_t nseq, const int32_t *cu_seqlens,
+                          const int64_t *start_pos, int32_t *wave_c0, int32_t cap) {
+    if (!valid_shape(H, d, dtype) || nseq < 0 || cap < 0 || (cap > 0 && !wave_c0)) return KDA_EINVAL;
+    if (nseq > 0 && (!cu_seqlens || !start_pos)) return KDA_EINVAL;
+    for (int32_t s = 0; s < nseq; ++s)
+        if (cu_seqlens[s + 1] < cu_seqlens[s] || start_pos[s] < 0) return KDA_EINVAL;
+    if (!split_applies(d, dtype)) return 0;
+    kda::SplitPlan pl;
+    make_split_plan(H, nseq, cu_seqlens, start_pos, pl);
+    for (int32_t i = 0; i < cap && i < (int32_t)pl.wave_c0.size(); ++i) wave_c0[i] = pl.wave_c0[i];
+    return pl.nwaves;
 }
 
 int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t nseq,
@@ -340,9 +319,8 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
     sa.slot_items = plan.slot_items;
     sa.state_scr = reinterpret_cast<float *>(ws + L.o_state);
     sa.win_scr = ws + L.o_win;
-    sa.cw = plan.cw;
     sa.nwaves = plan.nwaves;
-    return kda::launch_prefill_split(sa, plan, st, side_stream(pool)) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+    return kda::launch_prefill_split(sa, plan, st) == cudaSuccess ? KDA_OK : KDA_ECUDA;
 }
 
 int kda_decode_step_pp(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, const void *q,

@@ -144,13 +144,6 @@ int kda_pool_create(int64_t page_bytes, int32_t num_pages, kda_pool **out) {
 
 int kda_pool_destroy(kda_pool *p) {
     if (!p) return KDA_EINVAL;
-    for (cudaStream_t st : {p->side, p->main})
-        if (st) {
-            cudaStreamSynchronize(st);
-            cudaStreamDestroy(st);
-        }
-    for (cudaEvent_t e : {p->ev_in, p->ev_a, p->ev_out, p->ev_b[0], p->ev_b[1]})
-        if (e) cudaEventDestroy(e);
     for (auto &s : p->slots) {
         if (s.pending) cudaEventSynchronize(s.done);
         if (s.done) cudaEventDestroy(s.done);

@@ -29,14 +29,6 @@ struct kda_pool {
     static constexpr int kSlots = 4;
     Slot slots[kSlots];
     int next_slot = 0;
-
-    // Streams of the split prefill and their events (created on first use, on the device
-    // current at that time): chunk preparation runs on a low-priority stream, the chain kernel
-    // on a high-priority one, so that the chains of wave w get SMs first while the preparation
-    // of wave w + 1 fills the rest.
-    cudaStream_t side = nullptr, main = nullptr;   // low / high priority
-    cudaEvent_t ev_in = nullptr, ev_a = nullptr, ev_out = nullptr, ev_b[2] = {nullptr, nullptr};
-    int side_dev = -1;
     std::mutex mu;
 };
 

@@ -15,8 +15,9 @@ bool split_applies(int32_t d, int32_t dtype);
 // Chunks (aligned to absolute positions, 64 tokens) of a sequence of `len` tokens from `start`.
 int32_t chunks_of(int64_t start, int64_t len);
 
-// Waves of `cw` chunks per chain, balanced: as few waves as keep one slot of operand images
-// (all chains' items of a wave) under 384 MiB.
+// Waves of local chunks [wave_c0[w], wave_c0[w + 1]) of every chain, chosen by a cost model
+// of the wave steps among splits that keep one slot of operand images (all chains' items of a
+// wave) under 512 MiB.
 void make_split_plan(int32_t H, int32_t nseq, const int32_t *cu, const int64_t *start, SplitPlan &pl);
 
 }  // namespace kda

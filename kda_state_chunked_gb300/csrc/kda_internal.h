@@ -41,6 +41,8 @@ struct PoolView {
     int32_t num_pages;
     int32_t pages_per_object;
     int64_t rec_bytes;   // bytes of one head record (multiple of 256)
+    int32_t page_shift;  // log2(page_bytes) when that is a power of two, else -1
+    int32_t pad_;
 };
 
 struct PrefillArgs {
@@ -56,11 +58,11 @@ struct PrefillArgs {
     int32_t *status;
 };
 
-// Split prefill (bf16, d = 128): a parallel chunk-preparation kernel writes one operand image
-// per (chunk, head) item, a sequential chain kernel consumes the images in chunk order.  The
-// chunks of every chain are processed in waves of `cw` local chunks; wave w's images live in
-// slot w % 2 of the image buffer.
-constexpr int64_t kImageBytes = 90624;   // Qt' 16 KiB | Kb 16 KiB | P 8 KiB | WK'^T 16 KiB | U 32 KiB | gamma_C 512 B
+// Split prefill (bf16, d = 128): a parallel chunk preparation writes one operand image per
+// (chunk, head) item, a sequential chain consumes the images in chunk order.  The chunks of
+// every chain are processed in waves (wave w = local chunks [wave_c0[w], wave_c0[w + 1]));
+// wave w's images live in slot w % 2 of the image buffer.
+constexpr int64_t kImageBytes = 82432;   // Qt' 16 KiB | Kb 16 KiB | P 8 KiB | WK'^T 16 KiB | V 16 KiB | T 8 KiB | gamma_C 512 B
 
 struct SplitItem {
     int32_t seq;   // sequence
@@ -70,18 +72,19 @@ struct SplitItem {
 struct SplitArgs {
     PrefillArgs p;
     const SplitItem *items;        // every wave's items, wave after wave
-    const int32_t *wave_seq_off;   // [nwaves][nseq]: index in its wave of item (s, w * cw), -1 if none
+    const int32_t *wave_seq_off;   // [nwaves][nseq]: index in its wave of item (s, wave_c0[w]), -1 if none
     uint8_t *images;               // [2 slots][slot_items][H][kImageBytes]
     int64_t slot_items;            // items one slot holds
     float *state_scr;              // [nseq][H][d][d] state handed from one wave to the next
     uint8_t *win_scr;              // [nseq][H][3][3d] bf16 final conv window
-    int32_t cw, nwaves;
+    int32_t nwaves;
 };
 
 // Host-side wave plan of a split prefill call.
 struct SplitPlan {
-    int32_t cw = 1, nwaves = 0;
+    int32_t nwaves = 0;
     int64_t slot_items = 0;
+    std::vector<int32_t> wave_c0;        // [nwaves + 1] first local chunk of every wave
     std::vector<SplitItem> items;
     std::vector<int32_t> wave_begin;     // [nwaves + 1] offsets into items
     std::vector<int32_t> wave_seq_off;   // [nwaves * nseq]
@@ -128,16 +131,8 @@ struct Q8Args {
     int32_t *status;
 };
 
-// Streams and events for overlapping the two kernels of the split prefill: chunk preparation
-// on `side` (low priority), chains on `main` (high priority), joined back to the caller's
-// stream (side == nullptr: everything on the caller's stream).
-struct SideStream {
-    cudaStream_t side = nullptr, main = nullptr;
-    cudaEvent_t ev_in = nullptr, ev_a = nullptr, ev_out = nullptr, ev_b[2] = {nullptr, nullptr};
-};
-
 // Kernel launchers (defined in the .cu files).
-cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cudaStream_t s, const SideStream &ss);
+cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_supported(const PrefillArgs &a);

@@ -26,7 +26,8 @@ __device__ __forceinline__ void flag_status(int32_t *status, int32_t bits) {
 __device__ __forceinline__ uint8_t *obj_addr(const PoolView &pv, const int32_t *pages,
                                              uint64_t off, int32_t *status) {
     const uint64_t pb = (uint64_t)pv.page_bytes;
-    const uint64_t pi = off / pb;
+    // a shift for the usual power-of-two page sizes; a 64-bit division costs far more
+    const uint64_t pi = pv.page_shift >= 0 ? off >> pv.page_shift : off / pb;
     const int32_t id = pages[pi];
     if ((uint32_t)id >= (uint32_t)pv.num_pages) {
         flag_status(status, KDA_DEV_BAD_PAGE);

@@ -10,22 +10,26 @@
 // Everything of a chunk that does not depend on the state runs in parallel over all
 // (chunk, head) items; only the state contractions remain sequential per chain:
 //
-//   chunk_prep_kernel (one CTA per item, 160 threads, 2 CTAs per SM)
+//   chunk_prep_kernel (one CTA per (item, head), 160 threads, three CTAs per SM)
 //     conv, decay factors, Kt' = k gamma_r/gamma_C, Qt' = q gamma_r/gamma_C, Kb = k gamma_C/gamma_r,
 //     G | P = [Kt'; Qt'] Kb^T (tcgen05), T = (I + Diag(beta) strict_lower(G))^{-1} Diag(beta)
 //     (CUDA cores + tf32 mma.sync), WK'^T = Kt'^T T^T and U^T = V^T T^T (tcgen05), and writes one
 //     operand image per item: Qt', Kb, P, WK'^T (bf16, 128-byte swizzled, as the chain kernel's
 //     MMAs read them), U (fp32) and gamma_C.  Conv windows of checkpoints are written here.
 //
-//   chain_kernel (one CTA per (sequence, head), 256 threads)
+//   chain_kernel (one CTA per (sequence, head), 512 threads)
 //     S^T resident in TMEM; per chunk: S <- Gamma_C S (+ bf16 copy as the next A operand),
 //     O^T = (Gamma_C S)^T Qt'^T + W^T P^T, W^T = U^T - (Gamma_C S)^T WK'^T, S^T += W^T Kb,
 //     checkpoint states and outputs.  Images arrive by bulk copies, double-buffered.
 //
-// The chunks of every chain are processed in waves of `cw` chunks; a wave's images use one of
-// two slots, so the prep of wave w + 1 may run while the chains consume wave w.  The state is
-// handed from one wave to the next through a small fp32 scratch.  Every wait is bounded: on a
-// timeout a kernel records KDA_DEV_TIMEOUT, stops issuing work, frees TMEM and returns.
+// The chunks of every chain are processed in waves; a wave's images use one of two slots.
+// All launches go to one stream: prep 0, chains 0, prep 1, chains 1, ...  Prep w + 1 is a
+// programmatic dependent launch of chains w: every chain CTA allows it as soon as it starts,
+// so the chains hold their SMs before prep w + 1 fills the rest, and the two overlap.  The
+// last CTA of prep w + 1 waits for chains w to complete before it exits, so chains w + 1,
+// launched after prep w + 1 in stream order, find the state chains w handed on through a
+// small fp32 scratch.  Every wait is bounded: on a timeout a kernel records
+// KDA_DEV_TIMEOUT, stops issuing work, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -48,12 +52,12 @@ constexpr int D = 128;
 constexpr int C = kChunk;   // 64
 
 // Operand image of one (chunk, head) item (byte offsets; every operand 1024-byte aligned).
-constexpr uint32_t IMG_Q = 0;        // Qt'   [2 kb][64 rows][128 B]   K-major B operand
-constexpr uint32_t IMG_KB = 16384;   // Kb    [2 kb][64 rows][128 B]   MN-major B operand
-constexpr uint32_t IMG_P = 32768;    // P     [64 rows][128 B]         K-major B operand
-constexpr uint32_t IMG_WK = 40960;   // WK'^T [128 rows][128 B]        MN-major B operand
-constexpr uint32_t IMG_U = 57344;    // U     fp32 [64 chunk rows][128 value channels]
-constexpr uint32_t IMG_GC = 90112;   // gamma_C fp32 [128]
+constexpr uint32_t IMG_WQ = 0;       // [2 kb][128 rows: -WK' 0-63 | Qt' 64-127][128 B]  K-major B
+constexpr uint32_t IMG_KB = 32768;   // Kb    [2 kb][64 rows][128 B]   MN-major B operand
+constexpr uint32_t IMG_P = 49152;    // P     [64 rows][128 B]         K-major B operand
+constexpr uint32_t IMG_V = 57344;    // V     [2 kb][64 rows][128 B]   MN-major A operand
+constexpr uint32_t IMG_T = 73728;    // T     [64 rows][128 B]         K-major B operand
+constexpr uint32_t IMG_GC = 81920;   // gamma_C fp32 [128]
 static_assert(IMG_GC + 512 == kImageBytes, "image layout");
 
 __device__ __forceinline__ uint8_t *image_addr(const SplitArgs &a, int wave, int64_t idx_in_wave, int h) {
@@ -93,11 +97,11 @@ constexpr int kAWg = 1, kAHalf = 2;   // named barriers (128 and 64 threads)
 enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_T, AB_M2, AB_WK, A_NBARS };
 
 __global__ void __launch_bounds__(kAThreads, 3)
-    chunk_prep_kernel(const SplitArgs a, int wave, int item0, const __grid_constant__ CUtensorMap tm_q,
+    chunk_prep_kernel(const SplitArgs a, int wave, int item0, int dep_wait, const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = ptx::smem_align1024(smem_raw);
     Shared S;
     S.base = sm;
     S.bar = reinterpret_cast<uint64_t *>(sm + A_BAR);
@@ -208,29 +212,31 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 ptx::mma_commit(&S.bar[AB_GP]);
                 m1 = true;
                 // Qt' and Kb to the image; the Kb tile is reused once M1 and this copy have read it
-                ptx::bulk_store(img + IMG_Q, sm + A_KQ + 8192, 8192);
-                ptx::bulk_store(img + IMG_Q + 8192, sm + A_KQ + 16384 + 8192, 8192);
+                ptx::bulk_store(img + IMG_WQ + 8192, sm + A_KQ + 8192, 8192);
+                ptx::bulk_store(img + IMG_WQ + 16384 + 8192, sm + A_KQ + 16384 + 8192, 8192);
                 ptx::bulk_store(img + IMG_KB, sm + A_AL, 16384);
+                ptx::bulk_store(img + IMG_V, sm + A_V, 16384);
                 ptx::bulk_commit();
                 ptx::bulk_wait_read0();
                 if (wait_bar(S, AB_GP, 0)) ptx::mbar_arrive(&S.bar[AB_KBF]);
             }
             if (!*S.err && wait_bar(S, AB_T, 0)) {
-                // M2: WK'^T = Kt'^T T^T (columns 0-63), U^T = V^T T^T (columns 64-127)
+                // M2: WK'^T = Kt'^T T^T (the chain forms U^T = V^T T^T itself, from V and T)
                 ptx::tc_fence_after();
                 const uint32_t id_m2 = ptx::idesc_bf16(128, 64, 1, 0);
                 for (int s = 0; s < 4; ++s) {
                     const uint64_t bd = ptx::sdesc_sw128(sbase + A_T + s * 32, 16, 1024);
                     ptx::mma_bf16(tbase, ptx::sdesc_sw128(sbase + A_KQ + s * 2048, 16384, 1024), bd, id_m2,
                                   s > 0 ? 1u : 0u);
-                    ptx::mma_bf16(tbase + 64, ptx::sdesc_sw128(sbase + A_V + s * 2048, 8192, 1024), bd, id_m2,
-                                  s > 0 ? 1u : 0u);
                 }
                 ptx::mma_commit(&S.bar[AB_M2]);
                 m2 = true;
+                ptx::bulk_store(img + IMG_T, sm + A_T, 8192);
+                ptx::bulk_commit();
             }
             if (!*S.err && wait_bar(S, AB_WK, 0)) {
-                ptx::bulk_store(img + IMG_WK, sm + A_AL, 16384);
+                ptx::bulk_store(img + IMG_WQ, sm + A_AL, 8192);
+                ptx::bulk_store(img + IMG_WQ + 16384, sm + A_AL + 8192, 8192);
                 ptx::bulk_commit();
             }
             ptx::bulk_wait0();
@@ -568,7 +574,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
             ptx::fence_proxy_async_smem();
             named_bar(kAWg, 128);
             if (t == 0) ptx::mbar_arrive(&S.bar[AB_T]);
-            // ---------------- WK'^T (bf16 operand rows, staged for a bulk copy), U and gamma_C
+            // ---------------- -WK' (K-major bf16 operand rows, staged for bulk copies) and gamma_C
             if (!wg_wait(S, AB_M2, 0, t, kAWg, wflag)) break;
             ptx::tc_fence_after();
             {
@@ -576,26 +582,15 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 ptx::tmem_ld32(tbase + lanes, w0);
                 ptx::tmem_ld32(tbase + lanes + 32, w1);
                 ptx::tmem_wait_ld();
+                // thread t holds column t (key t) of WK'; row c of the K-major tile of key block
+                // t / 64 gets it at position t % 64, negated (the chain accumulates -(Gamma S)^T WK'^T)
+                uint8_t *const wk = sm + A_AL + (t >> 6) * 8192;
+                const uint32_t cb2 = (uint32_t)(t & 63) * 2;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4 v;
-                    uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        const int c = ch * 8 + 2 * q2;
-                        vv[q2] = c < 32 ? pack_bf16x2(w0[c & 31], w0[(c + 1) & 31])
-                                        : pack_bf16x2(w1[c & 31], w1[(c + 1) & 31]);
-                    }
-                    *reinterpret_cast<uint4 *>(sm + A_AL + ptx::sw128_off(t, ch * 16)) = v;
+                for (int c = 0; c < 32; ++c) {
+                    *reinterpret_cast<__nv_bfloat16 *>(wk + ptx::sw128_off(c, cb2)) = __float2bfloat16_rn(-w0[c]);
+                    *reinterpret_cast<__nv_bfloat16 *>(wk + ptx::sw128_off(32 + c, cb2)) = __float2bfloat16_rn(-w1[c]);
                 }
-                ptx::tmem_ld32(tbase + lanes + 64, w0);
-                ptx::tmem_ld32(tbase + lanes + 96, w1);
-                ptx::tmem_wait_ld();
-                float *U = reinterpret_cast<float *>(img + IMG_U);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) U[c * D + t] = w0[c];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) U[(32 + c) * D + t] = w1[c];
                 reinterpret_cast<float *>(img + IMG_GC)[t] = gC[t];
             }
             ptx::fence_proxy_async_smem();
@@ -612,22 +607,26 @@ __global__ void __launch_bounds__(kAThreads, 3)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tbase, 128);
     }
+    // launched beside the chains of the previous wave: this grid completes only after them
+    if (dep_wait && blockIdx.x == gridDim.x - 1) ptx::grid_dep_wait();
 }
 
 // ============================================================================ chain
 // 16 warps: warp 0 loads images, warp 1 issues MMAs, warps 4-7 and 8-11 run the state
 // epilogues on the low and high halves of the columns, warps 12-15 write the outputs.
 constexpr int kBThreads = 512;
-constexpr uint32_t B_SLOT = 91136;               // image slot stride (kImageBytes rounded up to 1024)
+constexpr uint32_t B_SLOT = (kImageBytes + 1023) / 1024 * 1024;   // image slot stride
 constexpr uint32_t B_WT = 2 * B_SLOT;            // [128 rows][128 B] W^T bf16 (A operand)
 constexpr uint32_t B_OST = B_WT + 16384;         // [64 rows][256 B] bf16 output staging
 constexpr uint32_t B_BAR = B_OST + 16384;
 constexpr uint32_t B_SMEM = B_BAR + 256 + 1024;
 constexpr int kBOut = 1;   // named barrier of the output warpgroup
 
-// TMEM columns: S^T, O^T (two buffers), D_W = -(Gamma S)^T WK'^T, bf16 (Gamma S)^T (two buffers,
-// two values per column).
-constexpr uint32_t COL_S = 0, COL_O = 128, COL_DW = 256, COL_SA = 320;
+// TMEM columns: S^T; two buffers of [W^T | O^T] (64 + 64 columns, adjacent so that one N = 128
+// MMA group forms W^T = U^T - (Gamma S)^T WK'^T and the first half of O^T together); bf16
+// (Gamma S)^T (two buffers, two values per column).
+constexpr uint32_t COL_S = 0, COL_SA = 384;
+__device__ __forceinline__ uint32_t col_w(int b) { return 128u + 128u * (uint32_t)b; }   // W^T; O^T at + 64
 
 // mbarriers ([2] by chunk parity).  SB and WT count the 8 state warps, DO the 4 output warps.
 enum {
@@ -638,7 +637,8 @@ enum {
     BB_M4S = 8,     // S advanced
     BB_M4 = 10,     // every MMA of the chunk done (O complete, image free)
     BB_DO = 12,     // O buffer read
-    B_NBARS = 14
+    BB_DRAIN = 14,  // error path: every issued MMA done
+    B_NBARS = 15
 };
 
 // First checkpoint of sequence m at or after position pos (index relative to the sequence).
@@ -652,7 +652,9 @@ __device__ __forceinline__ int lower_ckpt(const PrefillArgs &a, const SeqMeta &m
     return lo;
 }
 
-__global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, int wave) {
+__global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, int wave, int lc0w, int lc1w) {
+    // the next wave's chunk prep may be placed once every chain CTA holds its SM
+    ptx::grid_dep_launch();
     const PrefillArgs &pa = a.p;
     const int H = pa.H;
     const int h = blockIdx.x % H, sq = blockIdx.x / H;
@@ -674,9 +676,9 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
         }
         return;
     }
-    const int lc0 = wave * a.cw;
+    const int lc0 = lc0w;
     if (lc0 >= nchunks) return;
-    const int lc1 = lc0 + a.cw < nchunks ? lc0 + a.cw : nchunks;
+    const int lc1 = lc1w < nchunks ? lc1w : nchunks;
     const int cnt = lc1 - lc0;
     const bool first = lc0 == 0, last = lc1 == nchunks;
     const int32_t off0 = a.wave_seq_off[(int64_t)wave * pa.nseq + sq];
@@ -686,7 +688,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
     }
 
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = ptx::smem_align1024(smem_raw);
     Shared S;
     S.base = sm;
     S.bar = reinterpret_cast<uint64_t *>(sm + B_BAR);
@@ -696,7 +698,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
     if (tid == 0) {
         for (int i = 0; i < B_NBARS; ++i) {
             const uint32_t cntw = (i == BB_SB || i == BB_SB + 1 || i == BB_WT || i == BB_WT + 1) ? 8u
-                                  : (i >= BB_DO) ? 4u : 1u;
+                                  : (i == BB_DO || i == BB_DO + 1) ? 4u : 1u;
             ptx::mbar_init(&S.bar[i], cntw);
         }
         *S.err = 0;
@@ -731,29 +733,41 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        // Per chunk, in this order: D_W (needs the scaled state), the state update (needs W^T),
-        // then the outputs, which stay off the state's critical path.
         if (lane == 0) {
-            const uint32_t id_o = ptx::idesc_bf16(128, 64, 0, 0);
-            const uint32_t id_w = ptx::idesc_bf16(128, 64, 0, 1, 1);
+            const uint32_t id_wq = ptx::idesc_bf16(128, 128, 0, 0);
             const uint32_t id_s = ptx::idesc_bf16(128, 128, 0, 1);
             const uint32_t id_op = ptx::idesc_bf16(128, 64, 0, 0);
+            const uint32_t id_u = ptx::idesc_bf16(128, 64, 1, 0);
             const uint32_t sbase = ptx::smem_u32(sm), wt = sbase + B_WT;
-            // the three groups of every chunk are issued in a fixed order, each after a
-            // blocking (bounded) wait on what it needs
-            int nd = 0, ns = 0, no = 0;
+            // Per chunk, in this order, each group after a blocking (bounded) wait on what it
+            // needs: [W^T | O^T] += (Gamma S)^T [-WK' | Qt']^T (needs the scaled state and an
+            // emptied O buffer; W^T accumulates onto U^T, O^T onto zeros), the state update (needs
+            // W^T), O^T += W^T P^T, then U^T = V^T T^T of the next chunk into its W columns (last
+            // read by E2 two chunks back).  Every MMA holds the tensor pipe about the same time
+            // whatever its N up to 128, so the groups are as wide and as few as the data allow.
+            auto issue_u = [&](int n) {
+                const int b = n & 1;
+                const uint32_t im = sbase + b * B_SLOT;
+                ptx::tc_fence_after();
+                for (int s = 0; s < 4; ++s)
+                    ptx::mma_bf16(tbase + col_w(b), ptx::sdesc_sw128(im + IMG_V + s * 2048, 8192, 1024),
+                                  ptx::sdesc_sw128(im + IMG_T + s * 32, 16, 1024), id_u, s > 0 ? 1u : 0u);
+            };
             for (int n = 0; n < cnt; ++n) {
                 const int b = n & 1;
                 const uint32_t im = sbase + b * B_SLOT;
-                if (!wait_bar(S, BB_FULL + b, par(n)) || !wait_bar(S, BB_SB + b, par(n))) break;
-                // D_W = -(Gamma S)^T WK'^T
+                if (n == 0) {
+                    if (!wait_bar(S, BB_FULL, 0)) break;
+                    issue_u(0);
+                }
+                if (!wait_bar(S, BB_DO + b, par(n)) || !wait_bar(S, BB_SB + b, par(n))) break;
+                // [W^T | O^T] += (Gamma S)^T [-WK' | Qt']^T
                 ptx::tc_fence_after();
                 for (int s = 0; s < 8; ++s) {
-                    const uint64_t bw = ptx::sdesc_sw128(im + IMG_WK + s * 2048, 8192, 1024);
-                    ptx::mma_bf16_ta(tbase + COL_DW, tbase + COL_SA + b * 64 + s * 8, bw, id_w, s > 0 ? 1u : 0u);
+                    const uint64_t bq = ptx::sdesc_sw128(im + IMG_WQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+                    ptx::mma_bf16_ta(tbase + col_w(b), tbase + COL_SA + b * 64 + s * 8, bq, id_wq, 1u);
                 }
                 ptx::mma_commit(&S.bar[BB_W + b]);
-                ++nd;
                 if (!wait_bar(S, BB_WT + b, par(n))) break;
                 // S^T += W^T Kb
                 ptx::tc_fence_after();
@@ -763,34 +777,23 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                     ptx::mma_bf16(tbase + COL_S, ad, bd, id_s, 1u);
                 }
                 ptx::mma_commit(&S.bar[BB_M4S + b]);
-                ++ns;
-                if (n >= 2 && !wait_bar(S, BB_DO + b, par(n - 2))) break;
-                // O^T = (Gamma S)^T Qt'^T + W^T P^T
-                ptx::tc_fence_after();
-                for (int s = 0; s < 8; ++s) {
-                    const uint64_t bq = ptx::sdesc_sw128(im + IMG_Q + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024);
-                    ptx::mma_bf16_ta(tbase + COL_O + b * 64, tbase + COL_SA + b * 64 + s * 8, bq, id_o, s > 0 ? 1u : 0u);
-                }
+                // O^T += W^T P^T
                 for (int s = 0; s < 4; ++s) {
                     const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
                     const uint64_t bd = ptx::sdesc_sw128(im + IMG_P + s * 32, 16, 1024);
-                    ptx::mma_bf16(tbase + COL_O + b * 64, ad, bd, id_op, 1u);
+                    ptx::mma_bf16(tbase + col_w(b) + 64, ad, bd, id_op, 1u);
                 }
-                ptx::mma_commit(&S.bar[BB_M4 + b]);
-                ++no;
+                ptx::mma_commit(&S.bar[BB_M4 + b]);   // outputs done; frees this image slot for chunk n + 2
+                if (n + 1 < cnt) {
+                    if (!wait_bar(S, BB_FULL + (b ^ 1), par(n + 1))) break;
+                    issue_u(n + 1);
+                }
             }
-            // leave no MMA in flight
-            if (*S.err && nd > 0) {
+            // leave no MMA in flight: one more commit tracks every MMA issued so far
+            if (*S.err) {
+                ptx::mma_commit(&S.bar[BB_DRAIN]);
                 uint32_t k = 0;
-                while (!ptx::mbar_try_wait(&S.bar[BB_W + ((nd - 1) & 1)], par(nd - 1)) && k < ptx::kSpinLimit) ++k;
-                if (ns > 0) {
-                    k = 0;
-                    while (!ptx::mbar_try_wait(&S.bar[BB_M4S + ((ns - 1) & 1)], par(ns - 1)) && k < ptx::kSpinLimit) ++k;
-                }
-                if (no > 0) {
-                    k = 0;
-                    while (!ptx::mbar_try_wait(&S.bar[BB_M4 + ((no - 1) & 1)], par(no - 1)) && k < ptx::kSpinLimit) ++k;
-                }
+                while (!ptx::mbar_try_wait(&S.bar[BB_DRAIN], 0) && k < ptx::kSpinLimit) ++k;
             }
         }
     } else if (warp >= 4 && warp < 12) {
@@ -800,12 +803,12 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
         const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
         const int ib = g * 64;                         // key channels [ib, ib + 64) of S^T
         float *scr = a.state_scr + ((int64_t)sq * H + h) * D * D;
-        // state at the start of this wave
+        // state at the start of this wave, 32 loads in flight per batch
 #pragma unroll 1
-        for (int i0 = ib; i0 < ib + 64; i0 += 8) {
-            float v[8];
+        for (int i0 = ib; i0 < ib + 64; i0 += 32) {
+            float v[32];
 #pragma unroll
-            for (int ii = 0; ii < 8; ++ii) {
+            for (int ii = 0; ii < 32; ++ii) {
                 float x = 0.f;
                 if (!first) {
                     x = scr[(i0 + ii) * D + j];
@@ -816,7 +819,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                 }
                 v[ii] = x;
             }
-            ptx::tmem_st8(tbase + lanes + COL_S + i0, v);
+            ptx::tmem_st32(tbase + lanes + COL_S + i0, v);
         }
         ptx::tmem_wait_st();
         // next checkpoint at or after the first chunk boundary of this wave
@@ -856,10 +859,17 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
         for (int n = 0; n < cnt; ++n) {
             const int b = n & 1;
             // ---------------- E1: checkpoint S, Gamma_C S in TMEM, bf16 operand
+            // A checkpoint at this chunk boundary is stored from the registers E1 loads S into,
+            // before the decay scaling: no separate pass over S on the chain's critical path.
+            const int32_t *ckpg = nullptr;
             if (n >= 1) {
                 if (!(ok = warp_wait(S, BB_M4S + ((n - 1) & 1), par(n - 1)))) break;
                 ptx::tc_fence_after();
-                write_state((c_first + lc0 + n) * C, false, false);
+                if (ck_pos == (c_first + lc0 + n) * C) {
+                    ckpg = pa.pages + pa.ckpts[m.ckpt_begin + ck_i].pages_off;
+                    ++ck_i;
+                    ck_pos = ck_i < m.ckpt_count ? pa.ckpts[m.ckpt_begin + ck_i].pos : INT64_MAX;
+                }
             }
             if (!(ok = warp_wait(S, BB_FULL + b, par(n)))) break;
             const float *gcb = reinterpret_cast<const float *>(sm + b * B_SLOT + IMG_GC);
@@ -868,9 +878,16 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                 float v[32], pk[16];
                 ptx::tmem_ld32(tbase + lanes + COL_S + ib + i0, v);
                 ptx::tmem_wait_ld();
+                if (ckpg) {
+#pragma unroll
+                    for (int ii = 0; ii < 32; ++ii) {
+                        float *dst = reinterpret_cast<float *>(
+                            obj_addr(pa.pool, ckpg, rec + ((uint64_t)(ib + i0 + ii) * D + j) * 4, pa.status));
+                        if (dst) *dst = v[ii];
+                    }
+                }
 #pragma unroll
                 for (int ii = 0; ii < 32; ++ii) v[ii] *= gcb[ib + i0 + ii];
-                ptx::tmem_st32(tbase + lanes + COL_S + ib + i0, v);
 #pragma unroll
                 for (int q2 = 0; q2 < 16; ++q2) pk[q2] = __uint_as_float(pack_bf16x2(v[2 * q2], v[2 * q2 + 1]));
                 ptx::tmem_st16(tbase + lanes + COL_SA + b * 64 + ((ib + i0) >> 1), pk);
@@ -878,14 +895,25 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             warp_arrive(&S.bar[BB_SB + b]);
-            // ---------------- E2: W^T = U^T + D_W -> bf16 operand (chunk rows [32 g, 32 g + 32))
+            // S <- Gamma_C S in fp32 while the MMAs form W: the state update reads it only after
+            // E2 below, which these stores precede
+#pragma unroll 1
+            for (int i0 = 0; i0 < 64; i0 += 32) {
+                float v[32];
+                ptx::tmem_ld32(tbase + lanes + COL_S + ib + i0, v);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int ii = 0; ii < 32; ++ii) v[ii] *= gcb[ib + i0 + ii];
+                ptx::tmem_st32(tbase + lanes + COL_S + ib + i0, v);
+            }
+            ptx::tmem_wait_st();
+            // ---------------- E2: W^T (U^T with D_W accumulated) -> bf16 operand (chunk rows [32 g, 32 g + 32))
             if (!(ok = warp_wait(S, BB_W + b, par(n)))) break;
             ptx::tc_fence_after();
-            const float *U = reinterpret_cast<const float *>(sm + b * B_SLOT + IMG_U);
             {
                 const int r0 = g * 32;
                 float v[32];
-                ptx::tmem_ld32(tbase + lanes + COL_DW + r0, v);
+                ptx::tmem_ld32(tbase + lanes + col_w(b) + r0, v);
                 ptx::tmem_wait_ld();
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
@@ -893,8 +921,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                     uint32_t *pp = reinterpret_cast<uint32_t *>(&pk);
 #pragma unroll
                     for (int q2 = 0; q2 < 4; ++q2) {
-                        const int c = r0 + ch * 8 + 2 * q2;
-                        pp[q2] = pack_bf16x2(v[ch * 8 + 2 * q2] + U[c * D + j], v[ch * 8 + 2 * q2 + 1] + U[(c + 1) * D + j]);
+                        pp[q2] = pack_bf16x2(v[ch * 8 + 2 * q2], v[ch * 8 + 2 * q2 + 1]);
                     }
                     *reinterpret_cast<uint4 *>(sm + B_WT + ptx::sw128_off(j, r0 * 2 + ch * 16)) = pk;
                 }
@@ -925,14 +952,30 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
         const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
         __nv_bfloat16 *ost = reinterpret_cast<__nv_bfloat16 *>(sm + B_OST);
         const __nv_bfloat16 *og0 = static_cast<const __nv_bfloat16 *>(pa.o);
+        // The first MMA group of a chunk accumulates O^T onto its buffer: both buffers start
+        // zeroed, and each is zeroed again once read.
+        float zero[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) zero[i] = 0.f;
+        for (int b = 0; b < 2; ++b) {
+            ptx::tmem_st32(tbase + lanes + col_w(b) + 64, zero);
+            ptx::tmem_st32(tbase + lanes + col_w(b) + 96, zero);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        warp_arrive(&S.bar[BB_DO]);
+        warp_arrive(&S.bar[BB_DO + 1]);
         for (int n = 0; n < cnt; ++n) {
             const int b = n & 1;
             if (!warp_wait(S, BB_M4 + b, par(n))) break;
             ptx::tc_fence_after();
             float v0[32], v1[32];
-            ptx::tmem_ld32(tbase + lanes + COL_O + b * 64, v0);
-            ptx::tmem_ld32(tbase + lanes + COL_O + b * 64 + 32, v1);
+            ptx::tmem_ld32(tbase + lanes + col_w(b) + 64, v0);
+            ptx::tmem_ld32(tbase + lanes + col_w(b) + 96, v1);
             ptx::tmem_wait_ld();
+            ptx::tmem_st32(tbase + lanes + col_w(b) + 64, zero);
+            ptx::tmem_st32(tbase + lanes + col_w(b) + 96, zero);
+            ptx::tmem_wait_st();
             ptx::tc_fence_before();
             warp_arrive(&S.bar[BB_DO + b]);
             // transpose through shared memory: row r of the chunk = 128 channels (256 B)
@@ -970,7 +1013,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
 
 }  // namespace
 
-cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cudaStream_t s, const SideStream &ss) {
+cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cudaStream_t s) {
     const PrefillArgs &p = a.p;
     CUtensorMap tm[4];
     const void *src[4] = {p.q, p.k, p.v, p.alpha};
@@ -986,36 +1029,28 @@ cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cuda
     if (e != cudaSuccess) return e;
     const unsigned chains = (unsigned)(p.nseq * p.H);
     if (plan.nwaves == 0) {   // only empty sequences
-        chain_kernel<<<chains, kBThreads, B_SMEM, s>>>(a, 0);
+        chain_kernel<<<chains, kBThreads, B_SMEM, s>>>(a, 0, 0, 0);
         return cudaGetLastError();
-    }
-    // Wave w: chunk prep on the side stream (after the chains of wave w - 2 released its image
-    // slot), then the chains on the main stream; the prep of wave w + 1 overlaps the chains of
-    // wave w.  Without a side stream both run in order on the caller's stream.
-    const bool two = ss.side != nullptr;
-    cudaStream_t sa = two ? ss.side : s, sb = two ? ss.main : s;
-    if (two) {
-        if ((e = cudaEventRecord(ss.ev_in, s)) != cudaSuccess) return e;
-        if ((e = cudaStreamWaitEvent(sa, ss.ev_in, 0)) != cudaSuccess) return e;
-        if ((e = cudaStreamWaitEvent(sb, ss.ev_in, 0)) != cudaSuccess) return e;
     }
     for (int w = 0; w < plan.nwaves; ++w) {
         const int i0 = plan.wave_begin[w], n = plan.wave_begin[w + 1] - i0;
-        if (two && w >= 2 && (e = cudaStreamWaitEvent(sa, ss.ev_b[w & 1], 0)) != cudaSuccess) return e;
-        if (n > 0)
-            chunk_prep_kernel<<<(unsigned)(n * p.H), kAThreads, A_SMEM, sa>>>(a, w, i0, tm[0], tm[1], tm[2], tm[3]);
-        if (two) {
-            if ((e = cudaEventRecord(ss.ev_a, sa)) != cudaSuccess) return e;
-            if ((e = cudaStreamWaitEvent(sb, ss.ev_a, 0)) != cudaSuccess) return e;
+        if (n > 0) {
+            // wave 0: a plain launch; later waves: dependent launches beside the previous chains
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(n * p.H));
+            cfg.blockDim = dim3(kAThreads);
+            cfg.dynamicSmemBytes = A_SMEM;
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = w > 0 ? 1 : 0;
+            e = cudaLaunchKernelEx(&cfg, chunk_prep_kernel, a, w, i0, w > 0 ? 1 : 0, tm[0], tm[1], tm[2], tm[3]);
+            if (e != cudaSuccess) return e;
         }
-        chain_kernel<<<chains, kBThreads, B_SMEM, sb>>>(a, w);
-        if (two && (e = cudaEventRecord(ss.ev_b[w & 1], sb)) != cudaSuccess) return e;
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    if (two) {
-        if ((e = cudaEventRecord(ss.ev_out, sb)) != cudaSuccess) return e;
-        if ((e = cudaStreamWaitEvent(s, ss.ev_out, 0)) != cudaSuccess) return e;
+        chain_kernel<<<chains, kBThreads, B_SMEM, s>>>(a, w, plan.wave_c0[w], plan.wave_c0[w + 1]);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

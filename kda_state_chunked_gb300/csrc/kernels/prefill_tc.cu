@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = ptx::smem_align1024(smem_raw);
     Shared S;
     S.base = sm;
     S.bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);

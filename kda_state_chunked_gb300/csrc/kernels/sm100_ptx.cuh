@@ -17,6 +17,20 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch: allow the next grid of the stream (launched with
+// programmatic stream serialization) to be scheduled, and wait until the grid this one
+// depends on has completed with its memory operations visible.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// The dynamic shared-memory array rounded up to a 1024-byte boundary (the 128-byte swizzle
+// atoms need it).  The offset is applied by pointer arithmetic on the __shared__ array itself,
+// not by integer casts, so the compiler still knows every access through the result is a
+// shared-memory access and emits shared loads and stores rather than generic ones.
+__device__ __forceinline__ uint8_t *smem_align1024(uint8_t *raw) {
+    return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -27,7 +27,7 @@ struct SelftestArgs {
 
 __global__ void __launch_bounds__(128, 1) mma_selftest_kernel(SelftestArgs a, const __grid_constant__ CUtensorMap tmA) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = ptx::smem_align1024(smem_raw);
     uint8_t *sA = sm;                        // up to 128 x 128 bf16 = 32 KiB
     uint8_t *sB = sm + 32768;                // up to 128 x 128 bf16 = 32 KiB
     __shared__ uint64_t bar_mma, bar_tma;

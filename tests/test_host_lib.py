@@ -207,25 +207,54 @@ def test_gpu_calls_reject_bad_arguments_before_touching_the_device():
 
 
 def test_split_prefill_plan_launches_and_workspace():
-    """bf16 d=128 runs as waves of chunk preparation + chains; the host plan decides the
-    launch count and the operand-image workspace."""
+    """bf16 d=128 runs as waves of chunk preparation + chains (the preparation of a wave beside
+    the chains of the one before); the host plan decides the wave split, the launch count and
+    the operand-image workspace."""
     cu = [0, 8192, 16384, 24576, 32768]
     st = [0, 0, 0, 0]
     bf, f32 = kda.KDA_BF16, kda.KDA_F32
-    # 4 x 128 chunks x 16 heads of 90,624-byte images: two balanced waves of 64 chunks
-    assert kda.kda_prefill_kernel_launches(16, 128, bf, cu, st) == 4
+    unit = 82432
+    b = kda.kda_prefill_waves(16, 128, bf, cu, st)
+    W = len(b) - 1
+    # the waves tile the 128 chunks of every chain, each wave's images fit one 512 MiB slot
+    assert W >= 2 and b[0] == 0 and b[-1] == 128 and np.all(np.diff(b) > 0)
+    assert np.max(np.diff(b)) * 4 * 16 * unit <= 512 << 20
+    assert kda.kda_prefill_kernel_launches(16, 128, bf, cu, st) == 2 * W
     assert kda.kda_prefill_kernel_launches(16, 128, f32, cu, st) == 1
     assert kda.kda_prefill_kernel_launches(16, 64, bf, cu, st) == 1
     assert kda.kda_prefill_kernel_launches(16, 128, bf, [0, 0], [5]) == 1     # empty sequence only
+    assert len(kda.kda_prefill_waves(16, 128, bf, [0, 0], [5])) == 0
+    assert len(kda.kda_prefill_waves(16, 128, f32, cu, st)) == 0
     assert kda.kda_prefill_kernel_launches(2, 128, bf, [0, 100], [0]) == 2     # one wave
     ws = kda.kda_prefill_workspace_bytes(16, 128, bf, cu, st, 16, 17)
-    images = 2 * 4 * 64 * 16 * 90624          # two slots of one wave
+    images = 2 * int(np.max(np.diff(b))) * 4 * 16 * unit     # two slots of the largest wave
     scratch = 4 * 16 * 128 * 128 * 4 + 4 * 16 * 9 * 128 * 2
     assert images + scratch <= ws <= images + scratch + (1 << 20)
     # metadata only on the fp32 path
     assert kda.kda_prefill_workspace_bytes(16, 128, f32, cu, st, 16, 17) < (1 << 20)
     with pytest.raises(kda.KdaError):
         kda.kda_prefill_kernel_launches(16, 128, bf, [0, 10, 5], [0, 0])      # decreasing offsets
+
+
+@pytest.mark.parametrize("H,lens,starts", [
+    (32, [65536], [0]),                                  # one long chain per head
+    (32, [1 << 20], [0]),                                # the 1M-token sequence: many waves
+    (16, [8192, 100, 0, 5000], [0, 30, 7, 64 * 9 + 3]),  # ragged, an empty one, unaligned starts
+    (4, [64 * 3 + 1], [63]),
+])
+def test_wave_split_covers_every_chunk_within_the_slot(H, lens, starts):
+    """Whatever split the cost model picks: ascending bounds from 0 to the longest chain's
+    chunk count, no empty wave, every wave's images (all chains' chunks in it) within one
+    512 MiB slot."""
+    bf = kda.KDA_BF16
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    b = kda.kda_prefill_waves(H, 128, bf, cu, starts)
+    nch = [0 if n == 0 else (s + n - 1) // 64 - s // 64 + 1 for n, s in zip(lens, starts)]
+    assert b[0] == 0 and b[-1] == max(nch) and np.all(np.diff(b) > 0)
+    for w in range(len(b) - 1):
+        chunks = sum(max(0, min(n, b[w + 1]) - b[w]) for n in nch)
+        assert chunks * H * 82432 <= 512 << 20
+    assert kda.kda_prefill_kernel_launches(H, 128, bf, cu, starts) == 2 * (len(b) - 1)
 
 
 def test_q8_sizes_match_oracle_and_bad_arguments_are_refused():
