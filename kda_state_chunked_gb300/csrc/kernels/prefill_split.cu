@@ -13,23 +13,25 @@
 //   chunk_prep_kernel (one CTA per (item, head), 160 threads, three CTAs per SM)
 //     conv, decay factors, Kt' = k gamma_r/gamma_C, Qt' = q gamma_r/gamma_C, Kb = k gamma_C/gamma_r,
 //     G | P = [Kt'; Qt'] Kb^T (tcgen05), T = (I + Diag(beta) strict_lower(G))^{-1} Diag(beta)
-//     (CUDA cores + tf32 mma.sync), WK'^T = Kt'^T T^T and U^T = V^T T^T (tcgen05), and writes one
-//     operand image per item: Qt', Kb, P, WK'^T (bf16, 128-byte swizzled, as the chain kernel's
-//     MMAs read them), U (fp32) and gamma_C.  Conv windows of checkpoints are written here.
+//     (CUDA cores + tf32 mma.sync), WK'^T = Kt'^T T^T (tcgen05), and writes one operand image
+//     per item, bf16 and 128-byte swizzled as the chain kernel's MMAs read it: [-WK' | Qt'], Kb,
+//     P, V, T, and gamma_C (fp32).  Conv windows of checkpoints are written here.
 //
 //   chain_kernel (one CTA per (sequence, head), 512 threads)
-//     S^T resident in TMEM; per chunk: S <- Gamma_C S (+ bf16 copy as the next A operand),
-//     O^T = (Gamma_C S)^T Qt'^T + W^T P^T, W^T = U^T - (Gamma_C S)^T WK'^T, S^T += W^T Kb,
-//     checkpoint states and outputs.  Images arrive by bulk copies, double-buffered.
+//     S^T resident in TMEM; per chunk: U^T = V^T T^T, then [W^T | O^T] = [U^T | 0] +
+//     (Gamma_C S)^T [-WK' | Qt']^T in one MMA group, S^T <- Gamma_C S^T + W^T Kb,
+//     O^T += W^T P^T; checkpoint states and outputs.  Images arrive by bulk copies,
+//     double-buffered.
 //
 // The chunks of every chain are processed in waves; a wave's images use one of two slots.
-// All launches go to one stream: prep 0, chains 0, prep 1, chains 1, ...  Prep w + 1 is a
-// programmatic dependent launch of chains w: every chain CTA allows it as soon as it starts,
-// so the chains hold their SMs before prep w + 1 fills the rest, and the two overlap.  The
-// last CTA of prep w + 1 waits for chains w to complete before it exits, so chains w + 1,
-// launched after prep w + 1 in stream order, find the state chains w handed on through a
-// small fp32 scratch.  Every wait is bounded: on a timeout a kernel records
-// KDA_DEV_TIMEOUT, stops issuing work, frees TMEM and returns.
+// All launches go to one stream, each a programmatic dependent launch of the one before:
+// prep 0, chains 0, prep 1, chains 1, ...  Chains w are placed once every CTA of prep w has
+// started and wait in hardware for prep w to complete (and so for chains w - 1, which hand
+// the state on through a small fp32 scratch) before reading anything; each chain CTA then
+// allows prep w + 1, so the chains hold their SMs before prep w + 1 fills the rest and the
+// two overlap.  Prep w + 1 overwrites the slot chains w - 1 read, which are complete by
+// then; its last CTA waits for chains w to complete before it exits.  Every wait of the kernels' own is bounded: on a timeout a kernel
+// records KDA_DEV_TIMEOUT, stops issuing work, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -115,6 +117,9 @@ __global__ void __launch_bounds__(kAThreads, 3)
     float *diag = reinterpret_cast<float *>(sm + A_DG);
     __nv_bfloat16 *halo = reinterpret_cast<__nv_bfloat16 *>(sm + A_HALO);
 
+    // the chains of this wave may be placed (they wait for this grid to complete before
+    // reading anything it writes) once every CTA of it has started
+    ptx::grid_dep_launch();
     const PrefillArgs &pa = a.p;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = pa.H;
@@ -653,8 +658,6 @@ __device__ __forceinline__ int lower_ckpt(const PrefillArgs &a, const SeqMeta &m
 }
 
 __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, int wave, int lc0w, int lc1w) {
-    // the next wave's chunk prep may be placed once every chain CTA holds its SM
-    ptx::grid_dep_launch();
     const PrefillArgs &pa = a.p;
     const int H = pa.H;
     const int h = blockIdx.x % H, sq = blockIdx.x / H;
@@ -668,6 +671,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
 
     if (nchunks == 0) {
         // empty sequence: a fresh one gets a zero state and window, a resumed one keeps its own
+        ptx::grid_dep_wait();
         if (wave == 0 && !m.has_init) {
             for (int x = tid; x < (D * D * 4 + 9 * D * 2) / 16; x += kBThreads) {
                 uint4 *dst = reinterpret_cast<uint4 *>(obj_addr(pa.pool, act_pages, rec + (uint64_t)x * 16, pa.status));
@@ -712,6 +716,12 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tbase = *S.tmem;
+    // launched while the chunk prep of this wave (and through it the chains of the previous
+    // wave) may still run: nothing they write is read before this point.  Only then may the
+    // next wave's prep be placed: it overwrites the image slot that the chains two waves
+    // back read, and those are complete once this wave's prep is.
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
 
     if (warp == 0) {
         // ------------------------------------------------------------------ image loads
@@ -1049,8 +1059,18 @@ cudaError_t launch_prefill_split(const SplitArgs &a, const SplitPlan &plan, cuda
             e = cudaLaunchKernelEx(&cfg, chunk_prep_kernel, a, w, i0, w > 0 ? 1 : 0, tm[0], tm[1], tm[2], tm[3]);
             if (e != cudaSuccess) return e;
         }
-        chain_kernel<<<chains, kBThreads, B_SMEM, s>>>(a, w, plan.wave_c0[w], plan.wave_c0[w + 1]);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(chains);
+        cfg.blockDim = dim3(kBThreads);
+        cfg.dynamicSmemBytes = B_SMEM;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = n > 0 ? 1 : 0;
+        e = cudaLaunchKernelEx(&cfg, chain_kernel, a, w, plan.wave_c0[w], plan.wave_c0[w + 1]);
+        if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
