@@ -35,7 +35,11 @@ kda::PoolView pool_view(const kda_pool *p, void *base, int32_t H, int32_t d, int
     v.page_shift = -1;
     for (int32_t sh = 0; sh < 63; ++sh)
         if (((int64_t)1 << sh) == p->page_bytes) v.page_shift = sh;
-    v.pad_ = 0;
+    // pages of 4 GiB or more: every in-object offset (below 4 GiB) is on page 0, which the
+    // multiply gives with a zero reciprocal
+    v.page_magic = p->page_bytes < ((int64_t)1 << 32)
+                       ? (uint32_t)((((uint64_t)1 << 32) + (uint64_t)p->page_bytes - 1) / (uint64_t)p->page_bytes)
+                       : 0u;
     return v;
 }
 

@@ -42,7 +42,7 @@ struct PoolView {
     int32_t pages_per_object;
     int64_t rec_bytes;   // bytes of one head record (multiple of 256)
     int32_t page_shift;  // log2(page_bytes) when that is a power of two, else -1
-    int32_t pad_;
+    uint32_t page_magic; // ceil(2^32 / page_bytes) for other sizes below 4 GiB, else 0
 };
 
 struct PrefillArgs {

@@ -26,14 +26,33 @@ __device__ __forceinline__ void flag_status(int32_t *status, int32_t bits) {
 __device__ __forceinline__ uint8_t *obj_addr(const PoolView &pv, const int32_t *pages,
                                              uint64_t off, int32_t *status) {
     const uint64_t pb = (uint64_t)pv.page_bytes;
-    // a shift for the usual power-of-two page sizes; a 64-bit division costs far more
-    const uint64_t pi = pv.page_shift >= 0 ? off >> pv.page_shift : off / pb;
+    // Page index: a shift for power-of-two page sizes; otherwise off / pb without a division
+    // (an object is below 4 GiB, so off fits 32 bits): q = high half of off * ceil(2^32 / pb)
+    // is off / pb or one more, and one multiply-compare corrects it.
+    uint64_t pi;
+    if (pv.page_shift >= 0) {
+        pi = off >> pv.page_shift;
+    } else {
+        const uint32_t o = (uint32_t)off;
+        uint32_t q = __umulhi(o, pv.page_magic);
+        if ((uint64_t)q * pb > o) --q;
+        pi = q;
+    }
     const int32_t id = pages[pi];
     if ((uint32_t)id >= (uint32_t)pv.num_pages) {
         flag_status(status, KDA_DEV_BAD_PAGE);
         return nullptr;
     }
     return pv.base + (uint64_t)id * pb + (off - pi * pb);
+}
+
+// Base address of a run of accesses at off0 .. off0 + span of one object when the run is
+// contiguous in the pool (one page, or physically adjacent pages), so that every access in it
+// is base + (off - off0); nullptr otherwise (the caller then translates each access).
+__device__ __forceinline__ uint8_t *run_addr(const PoolView &pv, const int32_t *pages, uint64_t off0,
+                                             uint64_t span, int32_t *status) {
+    uint8_t *a = obj_addr(pv, pages, off0, status), *b = obj_addr(pv, pages, off0 + span, status);
+    return (a && b && b - a == (int64_t)span) ? a : nullptr;
 }
 
 // True when every page id of an object's list is inside the pool.

@@ -55,8 +55,7 @@ constexpr int C = kChunk;   // 64
 
 // Operand image of one (chunk, head) item (byte offsets; every operand 1024-byte aligned).
 constexpr uint32_t IMG_WQ = 0;       // [2 kb][128 rows: -WK' 0-63 | Qt' 64-127][128 B]  K-major B
-constexpr uint32_t IMG_KB = 32768;   // Kb    [2 kb][64 rows][128 B]   MN-major B operand
-constexpr uint32_t IMG_P = 49152;    // P     [64 rows][128 B]         K-major B operand
+constexpr uint32_t IMG_PK = 32768;   // [3 N blocks: P^T | Kb keys 0-63 | Kb keys 64-127][64 rows j][128 B]  MN-major B
 constexpr uint32_t IMG_V = 57344;    // V     [2 kb][64 rows][128 B]   MN-major A operand
 constexpr uint32_t IMG_T = 73728;    // T     [64 rows][128 B]         K-major B operand
 constexpr uint32_t IMG_GC = 81920;   // gamma_C fp32 [128]
@@ -96,7 +95,7 @@ constexpr uint32_t A_BAR = 71936;   // mbarriers, flags
 constexpr uint32_t A_SMEM = A_BAR + 128 + 1024;
 constexpr int kAWg = 1, kAHalf = 2;   // named barriers (128 and 64 threads)
 
-enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_T, AB_M2, AB_WK, A_NBARS };
+enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_PT, AB_T, AB_M2, AB_WK, A_NBARS };
 
 __global__ void __launch_bounds__(kAThreads, 3)
     chunk_prep_kernel(const SplitArgs a, int wave, int item0, int dep_wait, const __grid_constant__ CUtensorMap tm_q,
@@ -219,11 +218,15 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 // Qt' and Kb to the image; the Kb tile is reused once M1 and this copy have read it
                 ptx::bulk_store(img + IMG_WQ + 8192, sm + A_KQ + 8192, 8192);
                 ptx::bulk_store(img + IMG_WQ + 16384 + 8192, sm + A_KQ + 16384 + 8192, 8192);
-                ptx::bulk_store(img + IMG_KB, sm + A_AL, 16384);
+                ptx::bulk_store(img + IMG_PK + 8192, sm + A_AL, 16384);
                 ptx::bulk_store(img + IMG_V, sm + A_V, 16384);
                 ptx::bulk_commit();
                 ptx::bulk_wait_read0();
                 if (wait_bar(S, AB_GP, 0)) ptx::mbar_arrive(&S.bar[AB_KBF]);
+            }
+            if (!*S.err && wait_bar(S, AB_PT, 0)) {
+                ptx::bulk_store(img + IMG_PK, sm + A_V, 8192);
+                ptx::bulk_commit();
             }
             if (!*S.err && wait_bar(S, AB_T, 0)) {
                 // M2: WK'^T = Kt'^T T^T (the chain forms U^T = V^T T^T itself, from V and T)
@@ -462,26 +465,23 @@ __global__ void __launch_bounds__(kAThreads, 3)
                         row[c4 ^ (r & 7)] = make_float4(ev[0], ev[1], ev[2], ev[3]);
                     }
                 } else {
+                    // P^T staged MN-major over the V tile (free once its bulk copy has read it):
+                    // row j holds P[0..63][j]; thread r writes column r
                     const int r = t - C;
                     const float pdr = pd[r];
+                    uint8_t *const pt = sm + A_V;
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint4 v;
-                        uint32_t *vv = reinterpret_cast<uint32_t *>(&v);
-#pragma unroll
-                        for (int q2 = 0; q2 < 4; ++q2) {
-                            const int s0 = ch * 8 + q2 * 2;
-                            const float ga = s0 < 32 ? g0[s0 & 31] : g1[s0 & 31];
-                            const float gb = s0 + 1 < 32 ? g0[(s0 + 1) & 31] : g1[(s0 + 1) & 31];
-                            vv[q2] = pack_bf16x2(s0 < r ? ga : (s0 == r ? pdr : 0.f),
-                                                 s0 + 1 < r ? gb : (s0 + 1 == r ? pdr : 0.f));
-                        }
-                        *reinterpret_cast<uint4 *>(img + IMG_P + ptx::sw128_off(r, ch * 16)) = v;
+                    for (int s0 = 0; s0 < 64; ++s0) {
+                        const float gv = s0 < 32 ? g0[s0 & 31] : g1[s0 & 31];
+                        *reinterpret_cast<__nv_bfloat16 *>(pt + ptx::sw128_off(s0, (uint32_t)r * 2)) =
+                            __float2bfloat16_rn(s0 < r ? gv : (s0 == r ? pdr : 0.f));
                     }
                 }
             }
+            ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             named_bar(kAWg, 128);
+            if (t == 0) ptx::mbar_arrive(&S.bar[AB_PT]);
             // ---------------- T = (I + A)^{-1} Diag(beta)
             // level 0: the four 16 x 16 diagonal blocks, one row per thread (from the last row up)
             if (t < C) {
@@ -623,27 +623,28 @@ constexpr int kBThreads = 512;
 constexpr uint32_t B_SLOT = (kImageBytes + 1023) / 1024 * 1024;   // image slot stride
 constexpr uint32_t B_WT = 2 * B_SLOT;            // [128 rows][128 B] W^T bf16 (A operand)
 constexpr uint32_t B_OST = B_WT + 16384;         // [64 rows][256 B] bf16 output staging
-constexpr uint32_t B_BAR = B_OST + 16384;
+constexpr uint32_t B_PGL = B_OST + 16384;        // int32 [kPglCap]: page lists of this wave's checkpoints
+constexpr int kPglCap = 1024;
+constexpr uint32_t B_BAR = B_PGL + kPglCap * 4;
+constexpr int kBPgl = 2;   // named barrier: page-list copy (warp 2) -> state warps
 constexpr uint32_t B_SMEM = B_BAR + 256 + 1024;
 constexpr int kBOut = 1;   // named barrier of the output warpgroup
 
-// TMEM columns: S^T; two buffers of [W^T | O^T] (64 + 64 columns, adjacent so that one N = 128
-// MMA group forms W^T = U^T - (Gamma S)^T WK'^T and the first half of O^T together); bf16
-// (Gamma S)^T (two buffers, two values per column).
-constexpr uint32_t COL_S = 0, COL_SA = 384;
-__device__ __forceinline__ uint32_t col_w(int b) { return 128u + 128u * (uint32_t)b; }   // W^T; O^T at + 64
+// TMEM columns: W^T | O^T | S^T (64 + 64 + 128), adjacent so that one N = 128 MMA group forms
+// W^T = U^T - (Gamma S)^T WK'^T with the first half of O^T, and one N = 192 group the second
+// half of O^T with the state update; then bf16 (Gamma S)^T (two buffers, two values per column).
+constexpr uint32_t COL_W = 0, COL_O = 64, COL_S = 128, COL_SA = 256;
 
 // mbarriers ([2] by chunk parity).  SB and WT count the 8 state warps, DO the 4 output warps.
 enum {
     BB_FULL = 0,    // image landed (tx)
     BB_SB = 2,      // (Gamma S)^T written, S scaled
-    BB_W = 4,       // D_W in TMEM
+    BB_W = 4,       // W^T (and the first half of O^T) in TMEM
     BB_WT = 6,      // W^T operand written
-    BB_M4S = 8,     // S advanced
-    BB_M4 = 10,     // every MMA of the chunk done (O complete, image free)
-    BB_DO = 12,     // O buffer read
-    BB_DRAIN = 14,  // error path: every issued MMA done
-    B_NBARS = 15
+    BB_M4S = 8,     // every MMA of the chunk done: S advanced, O^T complete, image slot free
+    BB_DO = 10,     // O^T read and zeroed (one buffer: counts chunks)
+    BB_DRAIN = 11,  // error path: every issued MMA done
+    B_NBARS = 12
 };
 
 // First checkpoint of sequence m at or after position pos (index relative to the sequence).
@@ -698,11 +699,21 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
     S.bar = reinterpret_cast<uint64_t *>(sm + B_BAR);
     S.err = reinterpret_cast<volatile int *>(sm + B_BAR + B_NBARS * 8);
     S.tmem = reinterpret_cast<uint32_t *>(sm + B_BAR + B_NBARS * 8 + 16);
+    // Checkpoints of this wave (positions in ((c_first + lc0) C, (c_first + lc1) C]): their page
+    // lists are copied to shared memory by warp 2 while the state warps load the state, so a
+    // checkpoint store never waits on a global page-list load; more than fit: read in place.
+    const int ck_lo = lower_ckpt(pa, m, (c_first + lc0) * C + 1), ck_hi = lower_ckpt(pa, m, (c_first + lc1) * C + 1);
+    const int P = pa.pool.pages_per_object;
+    const bool pgl_smem = (ck_hi - ck_lo) * P <= kPglCap;
+    int32_t *pgl = reinterpret_cast<int32_t *>(sm + B_PGL);
+    auto ck_pages = [&](int ck) -> const int32_t * {   // ck: index within the sequence
+        return pgl_smem ? pgl + (ck - ck_lo) * P : pa.pages + pa.ckpts[m.ckpt_begin + ck].pages_off;
+    };
 
     if (tid == 0) {
         for (int i = 0; i < B_NBARS; ++i) {
             const uint32_t cntw = (i == BB_SB || i == BB_SB + 1 || i == BB_WT || i == BB_WT + 1) ? 8u
-                                  : (i == BB_DO || i == BB_DO + 1) ? 4u : 1u;
+                                  : i == BB_DO ? 4u : 1u;
             ptx::mbar_init(&S.bar[i], cntw);
         }
         *S.err = 0;
@@ -729,7 +740,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
             int issued = 0;
             for (int n = 0; n < cnt && !*S.err; ++n) {
                 const int b = n & 1;
-                if (n >= 2 && !wait_bar(S, BB_M4 + b, par(n - 2))) break;   // slot consumed
+                if (n >= 2 && !wait_bar(S, BB_M4S + b, par(n - 2))) break;   // slot consumed
                 ptx::mbar_arrive_expect_tx(&S.bar[BB_FULL + b], (uint32_t)kImageBytes);
                 ptx::bulk_load(sm + b * B_SLOT, image_addr(a, wave, off0 + n, h), (uint32_t)kImageBytes,
                                &S.bar[BB_FULL + b]);
@@ -745,22 +756,20 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t id_wq = ptx::idesc_bf16(128, 128, 0, 0);
-            const uint32_t id_s = ptx::idesc_bf16(128, 128, 0, 1);
-            const uint32_t id_op = ptx::idesc_bf16(128, 64, 0, 0);
+            const uint32_t id_sp = ptx::idesc_bf16(128, 192, 0, 1);
             const uint32_t id_u = ptx::idesc_bf16(128, 64, 1, 0);
             const uint32_t sbase = ptx::smem_u32(sm), wt = sbase + B_WT;
             // Per chunk, in this order, each group after a blocking (bounded) wait on what it
-            // needs: [W^T | O^T] += (Gamma S)^T [-WK' | Qt']^T (needs the scaled state and an
-            // emptied O buffer; W^T accumulates onto U^T, O^T onto zeros), the state update (needs
-            // W^T), O^T += W^T P^T, then U^T = V^T T^T of the next chunk into its W columns (last
-            // read by E2 two chunks back).  Every MMA holds the tensor pipe about the same time
-            // whatever its N up to 128, so the groups are as wide and as few as the data allow.
+            // needs: [W^T | O^T] += (Gamma S)^T [-WK' | Qt']^T (needs the scaled state and the
+            // emptied O^T; W^T accumulates onto U^T, O^T onto zeros), then [O^T | S^T] +=
+            // W^T [P^T | Kb] (needs W^T), then U^T = V^T T^T of the next chunk into the W columns
+            // (which E2 has read).  Every MMA holds the tensor pipe about the same time whatever
+            // its N up to 128, so the groups are as wide and as few as the data allow.
             auto issue_u = [&](int n) {
-                const int b = n & 1;
-                const uint32_t im = sbase + b * B_SLOT;
+                const uint32_t im = sbase + (n & 1) * B_SLOT;
                 ptx::tc_fence_after();
                 for (int s = 0; s < 4; ++s)
-                    ptx::mma_bf16(tbase + col_w(b), ptx::sdesc_sw128(im + IMG_V + s * 2048, 8192, 1024),
+                    ptx::mma_bf16(tbase + COL_W, ptx::sdesc_sw128(im + IMG_V + s * 2048, 8192, 1024),
                                   ptx::sdesc_sw128(im + IMG_T + s * 32, 16, 1024), id_u, s > 0 ? 1u : 0u);
             };
             for (int n = 0; n < cnt; ++n) {
@@ -770,30 +779,23 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                     if (!wait_bar(S, BB_FULL, 0)) break;
                     issue_u(0);
                 }
-                if (!wait_bar(S, BB_DO + b, par(n)) || !wait_bar(S, BB_SB + b, par(n))) break;
+                if (!wait_bar(S, BB_DO, (uint32_t)(n & 1)) || !wait_bar(S, BB_SB + b, par(n))) break;
                 // [W^T | O^T] += (Gamma S)^T [-WK' | Qt']^T
                 ptx::tc_fence_after();
                 for (int s = 0; s < 8; ++s) {
                     const uint64_t bq = ptx::sdesc_sw128(im + IMG_WQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
-                    ptx::mma_bf16_ta(tbase + col_w(b), tbase + COL_SA + b * 64 + s * 8, bq, id_wq, 1u);
+                    ptx::mma_bf16_ta(tbase + COL_W, tbase + COL_SA + b * 64 + s * 8, bq, id_wq, 1u);
                 }
                 ptx::mma_commit(&S.bar[BB_W + b]);
                 if (!wait_bar(S, BB_WT + b, par(n))) break;
-                // S^T += W^T Kb
+                // [O^T | S^T] += W^T [P^T | Kb]
                 ptx::tc_fence_after();
                 for (int s = 0; s < 4; ++s) {
                     const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
-                    const uint64_t bd = ptx::sdesc_sw128(im + IMG_KB + s * 2048, 8192, 1024);
-                    ptx::mma_bf16(tbase + COL_S, ad, bd, id_s, 1u);
+                    const uint64_t bd = ptx::sdesc_sw128(im + IMG_PK + s * 2048, 8192, 1024);
+                    ptx::mma_bf16(tbase + COL_O, ad, bd, id_sp, 1u);
                 }
-                ptx::mma_commit(&S.bar[BB_M4S + b]);
-                // O^T += W^T P^T
-                for (int s = 0; s < 4; ++s) {
-                    const uint64_t ad = ptx::sdesc_sw128(wt + s * 32, 16, 1024);
-                    const uint64_t bd = ptx::sdesc_sw128(im + IMG_P + s * 32, 16, 1024);
-                    ptx::mma_bf16(tbase + col_w(b) + 64, ad, bd, id_op, 1u);
-                }
-                ptx::mma_commit(&S.bar[BB_M4 + b]);   // outputs done; frees this image slot for chunk n + 2
+                ptx::mma_commit(&S.bar[BB_M4S + b]);   // frees this image slot for chunk n + 2
                 if (n + 1 < cnt) {
                     if (!wait_bar(S, BB_FULL + (b ^ 1), par(n + 1))) break;
                     issue_u(n + 1);
@@ -806,6 +808,15 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                 while (!ptx::mbar_try_wait(&S.bar[BB_DRAIN], 0) && k < ptx::kSpinLimit) ++k;
             }
         }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------------ checkpoint page lists
+        if (pgl_smem && ck_hi > ck_lo) {
+            for (int x = lane; x < (ck_hi - ck_lo) * P; x += 32) {
+                const int k = x / P;
+                pgl[x] = pa.pages[pa.ckpts[m.ckpt_begin + ck_lo + k].pages_off + (x - k * P)];
+            }
+            named_bar(kBPgl, 32 * 9);
+        }
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------------ state epilogues
         const int g = (warp - 4) >> 2;                 // column half
@@ -817,14 +828,18 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
 #pragma unroll 1
         for (int i0 = ib; i0 < ib + 64; i0 += 32) {
             float v[32];
+            const uint64_t o0 = rec + ((uint64_t)i0 * D + j) * 4;
+            const uint8_t *run = first && m.has_init ? run_addr(pa.pool, act_pages, o0, 31 * D * 4, pa.status) : nullptr;
 #pragma unroll
             for (int ii = 0; ii < 32; ++ii) {
                 float x = 0.f;
                 if (!first) {
                     x = scr[(i0 + ii) * D + j];
+                } else if (run) {
+                    x = *reinterpret_cast<const float *>(run + ii * D * 4);
                 } else if (m.has_init) {
                     const float *p = reinterpret_cast<const float *>(
-                        obj_addr(pa.pool, act_pages, rec + ((uint64_t)(i0 + ii) * D + j) * 4, pa.status));
+                        obj_addr(pa.pool, act_pages, o0 + (uint64_t)ii * D * 4, pa.status));
                     if (p) x = *p;
                 }
                 v[ii] = x;
@@ -832,32 +847,41 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
             ptx::tmem_st32(tbase + lanes + COL_S + i0, v);
         }
         ptx::tmem_wait_st();
+        if (pgl_smem && ck_hi > ck_lo) named_bar(kBPgl, 32 * 9);   // page lists copied
         // next checkpoint at or after the first chunk boundary of this wave
-        int ck_i = lower_ckpt(pa, m, (c_first + lc0) * C + 1);
+        int ck_i = ck_lo, pf_i = -1;   // next checkpoint; the last one prefetched
         int64_t ck_pos = ck_i < m.ckpt_count ? pa.ckpts[m.ckpt_begin + ck_i].pos : INT64_MAX;
         // this half of S (fp32, from TMEM) into the checkpoint at `pos` if there is one, into
         // the active object (final) or into the wave scratch (to_scratch)
+        // 8 rows of column j (offsets o0 + 512 ii) of an object
+        auto store_rows = [&](const int32_t *pgs, uint64_t o0, const float (&v)[8]) {
+            uint8_t *run = run_addr(pa.pool, pgs, o0, 7 * D * 4, pa.status);
+            if (run) {
+#pragma unroll
+                for (int ii = 0; ii < 8; ++ii) *reinterpret_cast<float *>(run + ii * D * 4) = v[ii];
+            } else {
+#pragma unroll
+                for (int ii = 0; ii < 8; ++ii) {
+                    float *dst = reinterpret_cast<float *>(obj_addr(pa.pool, pgs, o0 + (uint64_t)ii * D * 4, pa.status));
+                    if (dst) *dst = v[ii];
+                }
+            }
+        };
         auto write_state = [&](int64_t pos, bool final_state, bool to_scratch) {
             const bool hit = ck_pos == pos;
             if (!hit && !final_state && !to_scratch) return;
-            const int32_t *pg = hit ? pa.pages + pa.ckpts[m.ckpt_begin + ck_i].pages_off : nullptr;
+            const int32_t *pg = hit ? ck_pages(ck_i) : nullptr;
 #pragma unroll 1
             for (int i0 = ib; i0 < ib + 64; i0 += 8) {
                 float v[8];
                 ptx::tmem_ld8(tbase + lanes + COL_S + i0, v);
                 ptx::tmem_wait_ld();
+                const uint64_t o0 = rec + ((uint64_t)i0 * D + j) * 4;
+                if (pg) store_rows(pg, o0, v);
+                if (final_state) store_rows(act_pages, o0, v);
+                if (to_scratch) {
 #pragma unroll
-                for (int ii = 0; ii < 8; ++ii) {
-                    const uint64_t off = rec + ((uint64_t)(i0 + ii) * D + j) * 4;
-                    if (pg) {
-                        float *dst = reinterpret_cast<float *>(obj_addr(pa.pool, pg, off, pa.status));
-                        if (dst) *dst = v[ii];
-                    }
-                    if (final_state) {
-                        float *dst = reinterpret_cast<float *>(obj_addr(pa.pool, act_pages, off, pa.status));
-                        if (dst) *dst = v[ii];
-                    }
-                    if (to_scratch) scr[(i0 + ii) * D + j] = v[ii];
+                    for (int ii = 0; ii < 8; ++ii) scr[(i0 + ii) * D + j] = v[ii];
                 }
             }
             if (hit) {
@@ -876,7 +900,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                 if (!(ok = warp_wait(S, BB_M4S + ((n - 1) & 1), par(n - 1)))) break;
                 ptx::tc_fence_after();
                 if (ck_pos == (c_first + lc0 + n) * C) {
-                    ckpg = pa.pages + pa.ckpts[m.ckpt_begin + ck_i].pages_off;
+                    ckpg = ck_pages(ck_i);
                     ++ck_i;
                     ck_pos = ck_i < m.ckpt_count ? pa.ckpts[m.ckpt_begin + ck_i].pos : INT64_MAX;
                 }
@@ -889,11 +913,17 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                 ptx::tmem_ld32(tbase + lanes + COL_S + ib + i0, v);
                 ptx::tmem_wait_ld();
                 if (ckpg) {
+                    const uint64_t o0 = rec + ((uint64_t)(ib + i0) * D + j) * 4;
+                    uint8_t *run = run_addr(pa.pool, ckpg, o0, 31 * D * 4, pa.status);
+                    if (run) {
 #pragma unroll
-                    for (int ii = 0; ii < 32; ++ii) {
-                        float *dst = reinterpret_cast<float *>(
-                            obj_addr(pa.pool, ckpg, rec + ((uint64_t)(ib + i0 + ii) * D + j) * 4, pa.status));
-                        if (dst) *dst = v[ii];
+                        for (int ii = 0; ii < 32; ++ii) *reinterpret_cast<float *>(run + ii * D * 4) = v[ii];
+                    } else {
+#pragma unroll
+                        for (int ii = 0; ii < 32; ++ii) {
+                            float *dst = reinterpret_cast<float *>(obj_addr(pa.pool, ckpg, o0 + (uint64_t)ii * D * 4, pa.status));
+                            if (dst) *dst = v[ii];
+                        }
                     }
                 }
 #pragma unroll
@@ -923,7 +953,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
             {
                 const int r0 = g * 32;
                 float v[32];
-                ptx::tmem_ld32(tbase + lanes + col_w(b) + r0, v);
+                ptx::tmem_ld32(tbase + lanes + COL_W + r0, v);
                 ptx::tmem_wait_ld();
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
@@ -939,6 +969,18 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             warp_arrive(&S.bar[BB_WT + b]);
+            // The next checkpoint's record into L2 a few chunks before E1 stores it there (its
+            // first touch otherwise stalls those stores): two lines per state thread.
+            if (ck_i < ck_hi && ck_i != pf_i && ck_pos <= (c_first + lc0 + n + 4) * C) {
+                pf_i = ck_i;
+                const int32_t *pg = ck_pages(ck_i);
+                const int st = (warp - 4) * 32 + lane;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint8_t *q = obj_addr(pa.pool, pg, rec + (uint64_t)(st + 256 * u) * 128, pa.status);
+                    if (q) ptx::prefetch_l2(q);
+                }
+            }
         }
         if (ok && warp_wait(S, BB_M4S + ((cnt - 1) & 1), par(cnt - 1))) {
             ptx::tc_fence_after();
@@ -967,27 +1009,24 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
         float zero[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) zero[i] = 0.f;
-        for (int b = 0; b < 2; ++b) {
-            ptx::tmem_st32(tbase + lanes + col_w(b) + 64, zero);
-            ptx::tmem_st32(tbase + lanes + col_w(b) + 96, zero);
-        }
+        ptx::tmem_st32(tbase + lanes + COL_O, zero);
+        ptx::tmem_st32(tbase + lanes + COL_O + 32, zero);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         warp_arrive(&S.bar[BB_DO]);
-        warp_arrive(&S.bar[BB_DO + 1]);
         for (int n = 0; n < cnt; ++n) {
             const int b = n & 1;
-            if (!warp_wait(S, BB_M4 + b, par(n))) break;
+            if (!warp_wait(S, BB_M4S + b, par(n))) break;
             ptx::tc_fence_after();
             float v0[32], v1[32];
-            ptx::tmem_ld32(tbase + lanes + col_w(b) + 64, v0);
-            ptx::tmem_ld32(tbase + lanes + col_w(b) + 96, v1);
+            ptx::tmem_ld32(tbase + lanes + COL_O, v0);
+            ptx::tmem_ld32(tbase + lanes + COL_O + 32, v1);
             ptx::tmem_wait_ld();
-            ptx::tmem_st32(tbase + lanes + col_w(b) + 64, zero);
-            ptx::tmem_st32(tbase + lanes + col_w(b) + 96, zero);
+            ptx::tmem_st32(tbase + lanes + COL_O, zero);
+            ptx::tmem_st32(tbase + lanes + COL_O + 32, zero);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            warp_arrive(&S.bar[BB_DO + b]);
+            warp_arrive(&S.bar[BB_DO]);
             // transpose through shared memory: row r of the chunk = 128 channels (256 B)
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
