@@ -67,6 +67,9 @@ constexpr int64_t kImageBytes = 82432;   // Qt' 16 KiB | Kb 16 KiB | P 8 KiB | W
 struct SplitItem {
     int32_t seq;   // sequence
     int32_t lc;    // chunk index within the sequence's chain
+    int32_t row0;  // packed-token row of the chunk's first position (below the sequence's first
+                   // row for a chunk that starts before start_pos)
+    int32_t pad;
 };
 
 struct SplitArgs {

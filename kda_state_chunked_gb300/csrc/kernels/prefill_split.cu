@@ -95,7 +95,9 @@ constexpr uint32_t A_BAR = 71936;   // mbarriers, flags
 constexpr uint32_t A_SMEM = A_BAR + 128 + 1024;
 constexpr int kAWg = 1, kAHalf = 2;   // named barriers (128 and 64 threads)
 
-enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_PT, AB_T, AB_M2, AB_WK, A_NBARS };
+enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_QVF, AB_PT, AB_T, AB_M2, AB_WK, A_NBARS };
+constexpr uint32_t A_ERR = 96;   // error flag, TMEM address and wait flag after the mbarriers
+static_assert(A_NBARS * 8 <= A_ERR && A_ERR + 24 <= 128, "prep barrier block");
 
 __global__ void __launch_bounds__(kAThreads, 3)
     chunk_prep_kernel(const SplitArgs a, int wave, int item0, int dep_wait, const __grid_constant__ CUtensorMap tm_q,
@@ -106,9 +108,9 @@ __global__ void __launch_bounds__(kAThreads, 3)
     Shared S;
     S.base = sm;
     S.bar = reinterpret_cast<uint64_t *>(sm + A_BAR);
-    S.err = reinterpret_cast<volatile int *>(sm + A_BAR + 64);
-    S.tmem = reinterpret_cast<uint32_t *>(sm + A_BAR + 80);
-    volatile int *wflag = reinterpret_cast<volatile int *>(sm + A_BAR + 96);
+    S.err = reinterpret_cast<volatile int *>(sm + A_BAR + A_ERR);
+    S.tmem = reinterpret_cast<uint32_t *>(sm + A_BAR + A_ERR + 8);
+    volatile int *wflag = reinterpret_cast<volatile int *>(sm + A_BAR + A_ERR + 16);
     float *gC = reinterpret_cast<float *>(sm + A_GC);
     float *bs = reinterpret_cast<float *>(sm + A_BS);
     float *pd = reinterpret_cast<float *>(sm + A_PD);
@@ -148,7 +150,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
         ptx::prefetch_tmap(&tm_a);
-        const int32_t y = (int32_t)((int64_t)m.tok_begin + (abs0 - start));
+        const int32_t y = it.row0;
         uint64_t *fb = &S.bar[AB_FULL];
         ptx::mbar_arrive_expect_tx(fb, 4 * 2 * 64 * 128);
         for (int kb = 0; kb < 2; ++kb) {
@@ -215,14 +217,19 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 }
                 ptx::mma_commit(&S.bar[AB_GP]);
                 m1 = true;
-                // Qt' and Kb to the image; the Kb tile is reused once M1 and this copy have read it
+                // Kb, Qt' and V to the image, Kb in a group of its own: its tile becomes the solve
+                // scratch once M1 and this copy have read it (KBF); the Qt' and V tiles are
+                // reused later, for T and P^T (QVF)
+                ptx::bulk_store(img + IMG_PK + 8192, sm + A_AL, 16384);
+                ptx::bulk_commit();
                 ptx::bulk_store(img + IMG_WQ + 8192, sm + A_KQ + 8192, 8192);
                 ptx::bulk_store(img + IMG_WQ + 16384 + 8192, sm + A_KQ + 16384 + 8192, 8192);
-                ptx::bulk_store(img + IMG_PK + 8192, sm + A_AL, 16384);
                 ptx::bulk_store(img + IMG_V, sm + A_V, 16384);
                 ptx::bulk_commit();
-                ptx::bulk_wait_read0();
+                ptx::bulk_wait_read1();
                 if (wait_bar(S, AB_GP, 0)) ptx::mbar_arrive(&S.bar[AB_KBF]);
+                ptx::bulk_wait_read0();
+                ptx::mbar_arrive(&S.bar[AB_QVF]);
             }
             if (!*S.err && wait_bar(S, AB_PT, 0)) {
                 ptx::bulk_store(img + IMG_PK, sm + A_V, 8192);
@@ -466,7 +473,9 @@ __global__ void __launch_bounds__(kAThreads, 3)
                     }
                 } else {
                     // P^T staged MN-major over the V tile (free once its bulk copy has read it):
-                    // row j holds P[0..63][j]; thread r writes column r
+                    // row j holds P[0..63][j]; thread r writes column r.  (A timeout of this
+                    // warp-level wait is recorded; the warps carry on together to the barriers.)
+                    (void)warp_wait(S, AB_QVF, 0);
                     const int r = t - C;
                     const float pdr = pd[r];
                     uint8_t *const pt = sm + A_V;
@@ -552,6 +561,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
             }
             named_bar(kAWg, 128);
             if (t < C) {
+                (void)warp_wait(S, AB_QVF, 0);   // T goes over the first Qt' half: read by then
                 const int r = t;
                 const float4 *row = reinterpret_cast<const float4 *>(Msc + r * 64);
                 const float4 *b4 = reinterpret_cast<const float4 *>(bs);
