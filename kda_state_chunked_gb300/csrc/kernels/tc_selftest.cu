@@ -131,6 +131,61 @@ __global__ void __launch_bounds__(128, 1) mma_selftest_kernel(SelftestArgs a, co
     if (warp == 0) ptx::tmem_dealloc(tmem_base, 256);
 }
 
+// Issue-rate probe of tcgen05.mma (kind::f16, M = 128, one CTA): `reps` rounds of `nmma`
+// back-to-back MMAs of one shape on zero operands, each round ended by a commit and a bounded
+// wait; out[2 r] = clock cycles to issue round r, out[2 r + 1] = cycles until it completed.
+// mode: 0 / 1 / 2 = A and B in shared memory with N = 64 / 128 / 256; 3 / 4 = A in TMEM with
+// N = 64 / 128.  Every descriptor stays inside the 48 KiB of zeroed shared memory.
+__global__ void __launch_bounds__(128, 1) mma_issue_probe_kernel(long long *out, int mode, int nmma, int reps, int *err) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = ptx::smem_align1024(smem_raw);
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int err_s;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (tid == 0) {
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_mbar_init();
+        err_s = 0;
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(&tmem_base, 512);
+        ptx::tmem_relinquish();
+    }
+    for (int i = tid; i < 49152 / 16; i += 128) reinterpret_cast<uint4 *>(sm)[i] = make_uint4(0, 0, 0, 0);
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tb = tmem_base;
+    if (tid == 0) {
+        const int N = (mode == 0 || mode == 3) ? 64 : (mode == 1 || mode == 4) ? 128 : 256;
+        const bool ta = mode >= 3;
+        const uint32_t idesc = ptx::idesc_bf16(128, N, 0, 0);
+        const uint32_t sbase = ptx::smem_u32(sm);
+        for (int r = 0; r < reps && !err_s; ++r) {
+            ptx::tc_fence_after();
+            const long long t0 = clock64();
+            for (int i = 0; i < nmma; ++i) {
+                const uint64_t bd = ptx::sdesc_sw128(sbase + 16384 + (i & 3) * 32, 16, 1024);   // N rows x 128 B
+                if (ta) ptx::mma_bf16_ta(tb, tb + 256 + (i & 3) * 8, bd, idesc, 1u);
+                else ptx::mma_bf16(tb, ptx::sdesc_sw128(sbase + (i & 3) * 32, 16, 1024), bd, idesc, 1u);
+            }
+            const long long t1 = clock64();
+            ptx::mma_commit(&bar);
+            const bool ok = ptx::mbar_wait(&bar, (uint32_t)(r & 1), &err_s);
+            const long long t2 = clock64();
+            out[2 * r] = t1 - t0;
+            out[2 * r + 1] = ok ? t2 - t0 : -1;
+        }
+        if (err_s) *err = 1;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 0) ptx::tmem_dealloc(tb, 512);
+}
+
 }  // namespace
 
 // Encode a 2-D bf16 tensor map with 128-byte swizzle (host side).
@@ -202,4 +257,17 @@ extern "C" int kda_internal_mma_selftest(const void *A, const void *B, float *D,
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return -4;
     kern<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(a, tm);
     return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+// Internal diagnostic entry point (not part of the public header): the tcgen05.mma issue-rate
+// probe above on a device buffer out[2 * reps] (int64); 0, or -1 for bad arguments / launch.
+extern "C" int kda_internal_mma_issue_probe(long long *out_dev, int mode, int nmma, int reps, int *err_dev,
+                                            void *stream) {
+    using namespace kda;
+    if (!out_dev || !err_dev || mode < 0 || mode > 4 || nmma < 1 || nmma > 1024 || reps < 1) return -1;
+    const int smem = 49152 + 1024;
+    if (cudaFuncSetAttribute(mma_issue_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return -1;
+    mma_issue_probe_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(out_dev, mode, nmma, reps, err_dev);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
