@@ -80,19 +80,21 @@ __device__ __forceinline__ int find_ckpt(const PrefillArgs &a, const SeqMeta &m,
 // ============================================================================ chunk prep
 constexpr int kAThreads = 160;   // warps 0-3 compute, warp 4 TMA + MMA + bulk stores
 
-// Shared memory (72 KB: three CTAs per SM).  P goes straight to the image from registers.
+// Shared memory (73 KiB: three CTAs per SM).  P^T is staged over the V tile.
 constexpr uint32_t A_KQ = 0;        // [2 kb][128 rows: k 0-63 | q 64-127][128 B] -> Kt' | Qt'
 constexpr uint32_t A_T = 8192;      // T [64][128 B], over the first Qt' half once that is stored
 constexpr uint32_t A_V = 32768;     // [2 kb][64][128 B]  raw v -> V
 constexpr uint32_t A_AL = 49152;    // [2 kb][64][128 B]  raw alpha -> Kb -> fp32 solve scratch -> WK'^T
-constexpr uint32_t A_DG = 65536;    // float [64][8]      partial sums of the diagonal q.k
-constexpr uint32_t A_GC = 67584;    // float [128]  gamma_C
-constexpr uint32_t A_BS = 68096;    // float [64]   beta
-constexpr uint32_t A_PD = 68352;    // float [64]   exact diagonal of P
-constexpr uint32_t A_RED = 68608;   // float2 [2][64] half products of alpha
-constexpr uint32_t A_HALO = 69632;  // bf16 [3][384] conv window
-constexpr uint32_t A_BAR = 71936;   // mbarriers, flags
+constexpr uint32_t A_DG = 65536;    // float [64][16]     partial sums of the diagonal q.k
+constexpr uint32_t A_GC = 69632;    // float [128]  gamma_C
+constexpr uint32_t A_BS = 70144;    // float [64]   beta
+constexpr uint32_t A_PD = 70400;    // float [64]   exact diagonal of P
+constexpr uint32_t A_RED = 70656;   // float2 [2][64] half products of alpha
+constexpr uint32_t A_HALO = 71680;  // bf16 [3][384] conv window
+constexpr uint32_t A_BAR = 73984;   // mbarriers, flags
 constexpr uint32_t A_SMEM = A_BAR + 128 + 1024;
+// three CTAs per SM: 228 KiB of shared memory per SM, 1 KiB of it reserved per CTA
+static_assert(3 * (A_SMEM + 1024) <= 228 * 1024, "three chunk-prep CTAs per SM");
 constexpr int kAWg = 1, kAHalf = 2;   // named barriers (128 and 64 threads)
 
 enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_QVF, AB_PT, AB_T, AB_M2, AB_WK, A_NBARS };
@@ -366,10 +368,10 @@ __global__ void __launch_bounds__(kAThreads, 3)
                     okb = pack_bf16x2(kr.x, kr.y);
                     ov = pack_bf16x2(vb.x, vb.y);
                 }
+                // sum over groups of four lanes (eight channels); 16 partials per row
                 float dsum = dpart + __shfl_xor_sync(0xffffffffu, dpart, 1);
                 dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
-                dsum += __shfl_xor_sync(0xffffffffu, dsum, 4);
-                if ((lane & 7) == 0) diag[r * 8 + (p >> 3)] = dsum;
+                if ((lane & 3) == 0) diag[r * 16 + (p >> 2)] = dsum;
                 *reinterpret_cast<uint32_t *>(qrow + off) = oq;
                 *reinterpret_cast<uint32_t *>(krow + off) = ok;
                 *reinterpret_cast<uint32_t *>(arow + off) = okb;
@@ -425,7 +427,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
             if (t < C) {
                 float acc = 0.f;
 #pragma unroll
-                for (int s2 = 0; s2 < 8; ++s2) acc += diag[t * 8 + ((s2 + t) & 7)];
+                for (int s2 = 0; s2 < 16; ++s2) acc += diag[t * 16 + ((s2 + t) & 15)];
                 pd[t] = acc;
             }
             named_bar(kAWg, 128);
