@@ -562,13 +562,14 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 blk_store(Msc, bi, bj, z, -1.f, lane);
             }
             named_bar(kAWg, 128);
-            if (t < C) {
+            {
+                // T = inverse * Diag(beta) as the bf16 operand; two threads per row (32 columns each)
                 (void)warp_wait(S, AB_QVF, 0);   // T goes over the first Qt' half: read by then
-                const int r = t;
+                const int r = t & 63, c8 = (t >> 6) * 4;
                 const float4 *row = reinterpret_cast<const float4 *>(Msc + r * 64);
                 const float4 *b4 = reinterpret_cast<const float4 *>(bs);
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
+                for (int ch = c8; ch < c8 + 4; ++ch) {
                     float ev[8];
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
