@@ -174,3 +174,34 @@ def test_bad_checkpoint_page_is_reported_not_faulted():
         kda.kda_prefill_varlen(pool, [0, T], [0], [0], dev["q"], dev["k"], dev["v"], dev["alpha"],
                                dev["beta"], dev["conv_w"], o, act, [0], [512], [[99]], ws, st)
     assert e.value.code == kda.KDA_EINVAL
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
+def test_scattered_pages_of_a_non_power_of_two_size(dtype, d):
+    """Pages of 19 x 256 bytes, every object's pages three ids apart in a fragmented pool: page
+    translation without a power-of-two shift, and state records that cross non-adjacent pages
+    (the kernels' contiguous-run fast path cannot apply)."""
+    H = 3
+    lens = [700, 1, 64, 1500, 333, 0, 2100]
+    starts = [0, 512, 1024, 96, 2048 + 37, 4096, 5]
+    init = [0, 1, 1, 1, 1, 1, 1]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cpu, dev = _toks(int(cu[-1]), H, d, dtype, 17)
+    page_bytes = 19 * 256
+    pool = kda.Pool(page_bytes, 3000, DEV)
+    held = kda.kda_page_alloc(pool, 3000)
+    kda.kda_page_decref(pool, held[1::3])          # later allocations get ids 1, 4, 7, ...
+    P = pool.object_pages(H, d, kda.DTYPES[dtype])
+    act = kda.kda_page_alloc(pool, len(lens) * P).reshape(len(lens), P)
+    assert np.all(np.diff(act.reshape(-1)) == 3)
+    g = torch.Generator().manual_seed(19)
+    S0 = np.zeros((len(lens), H, d, d))
+    W0 = np.zeros((len(lens), H, 3, 3 * d))
+    for s in range(len(lens)):
+        if init[s]:
+            S0[s], W0[s] = random_state(H, d, dtype, g)
+            write_object(pool, act[s], S0[s], W0[s], dtype)
+    run = Prefill(pool, dev, cu, starts, init, act, stride=2, include_last=True)
+    ck = oracle_positions(cu, starts, 2, True)
+    ref = oracle_prefill(cpu, cu, starts, S0=S0, win0=W0, ckpt_abs=ck)
+    compare_prefill(pool, run, ref, cu, act, dtype, ck)
