@@ -630,8 +630,9 @@ __global__ void __launch_bounds__(kAThreads, 3)
 }
 
 // ============================================================================ chain
-// 16 warps: warp 0 loads images, warp 1 issues MMAs, warps 4-7 and 8-11 run the state
-// epilogues on the low and high halves of the columns, warps 12-15 write the outputs.
+// 16 warps: warp 0 loads images, warp 1 issues MMAs, warp 2 stages the wave's checkpoint
+// page lists, warps 4-7 and 8-11 run the state epilogues on the low and high halves of the
+// key columns, warps 12-15 write the outputs; warp 3 idles.
 constexpr int kBThreads = 512;
 constexpr uint32_t B_SLOT = (kImageBytes + 1023) / 1024 * 1024;   // image slot stride
 constexpr uint32_t B_WT = 2 * B_SLOT;            // [128 rows][128 B] W^T bf16 (A operand)
