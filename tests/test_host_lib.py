@@ -368,3 +368,30 @@ def test_verify_plan_and_accept_keep_one_object_per_request():
     with pytest.raises(kda.KdaError) as e:
         kda.kda_verify_plan(pool, H, d, dt, B, 64)      # more than the pool holds
     assert e.value.code == kda.KDA_ENOPAGES
+
+
+def test_prefill_waves_arguments():
+    """kda_prefill_waves returns the wave count and writes at most `cap` bounds; bad shapes,
+    decreasing offsets, negative starts and a NULL array with cap > 0 are refused."""
+    L = kda.lib()
+    bf = kda.KDA_BF16
+    cu = np.array([0, 8192, 16384, 24576, 32768], dtype=np.int32)
+    st = np.zeros(4, dtype=np.int64)
+    W = L.kda_prefill_waves(16, 128, bf, 4, kda._ptr(cu), kda._ptr(st), None, 0)
+    assert W >= 1
+    full = np.full(W + 3, -7, dtype=np.int32)
+    assert L.kda_prefill_waves(16, 128, bf, 4, kda._ptr(cu), kda._ptr(st), kda._ptr(full), W + 3) == W
+    assert full[0] == 0 and full[W] == 128 and np.all(full[W + 1:] == -7)   # W + 1 bounds written
+    part = np.full(2, -7, dtype=np.int32)
+    assert L.kda_prefill_waves(16, 128, bf, 4, kda._ptr(cu), kda._ptr(st), kda._ptr(part), 2) == W
+    assert list(part) == list(full[:2])
+    assert L.kda_prefill_waves(16, 128, bf, 4, kda._ptr(cu), kda._ptr(st), None, 2) == kda.KDA_EINVAL
+    assert L.kda_prefill_waves(16, 128, bf, 4, kda._ptr(cu), kda._ptr(st), kda._ptr(part), -1) == kda.KDA_EINVAL
+    assert L.kda_prefill_waves(16, 96, bf, 4, kda._ptr(cu), kda._ptr(st), None, 0) == kda.KDA_EINVAL
+    bad = np.array([0, 10, 5], dtype=np.int32)
+    assert L.kda_prefill_waves(16, 128, bf, 2, kda._ptr(bad), kda._ptr(st), None, 0) == kda.KDA_EINVAL
+    neg = np.array([-1, 0, 0, 0], dtype=np.int64)
+    assert L.kda_prefill_waves(16, 128, bf, 4, kda._ptr(cu), kda._ptr(neg), None, 0) == kda.KDA_EINVAL
+    # shapes that do not take the split path have no waves
+    assert L.kda_prefill_waves(16, 64, bf, 4, kda._ptr(cu), kda._ptr(st), None, 0) == 0
+    assert L.kda_prefill_waves(16, 128, kda.KDA_F32, 4, kda._ptr(cu), kda._ptr(st), None, 0) == 0
