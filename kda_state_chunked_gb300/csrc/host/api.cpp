@@ -25,24 +25,6 @@ int64_t elem_size(int32_t dtype) { return dtype == KDA_BF16 ? 2 : 4; }
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-kda::PoolView pool_view(const kda_pool *p, void *base, int32_t H, int32_t d, int32_t dtype) {
-    kda::PoolView v;
-    v.base = static_cast<uint8_t *>(base);
-    v.page_bytes = p->page_bytes;
-    v.num_pages = p->num_pages;
-    v.pages_per_object = kda_object_pages(p, H, d, dtype);
-    v.rec_bytes = kda_record_bytes(d, dtype);
-    v.page_shift = -1;
-    for (int32_t sh = 0; sh < 63; ++sh)
-        if (((int64_t)1 << sh) == p->page_bytes) v.page_shift = sh;
-    // pages of 4 GiB or more: every in-object offset (below 4 GiB) is on page 0, which the
-    // multiply gives with a zero reciprocal
-    v.page_magic = p->page_bytes < ((int64_t)1 << 32)
-                       ? (uint32_t)((((uint64_t)1 << 32) + (uint64_t)p->page_bytes - 1) / (uint64_t)p->page_bytes)
-                       : 0u;
-    return v;
-}
-
 // Pages written by a call must be private to it: allocated, refcount exactly 1, and not
 // repeated (a checkpoint visible to others is never written in place).  `g` is the
 // duplicate-check generation of this call (kda::pool_new_stamp).
@@ -103,10 +85,10 @@ int copy_objects(kda_pool *p, int32_t H, int32_t d, int32_t dtype, int32_t n, co
     std::memcpy(both.data() + (size_t)n * P, dst, (size_t)list);
     int rc = kda::stage_upload(p, both.data(), (size_t)(2 * list), ws, stream);
     if (rc != KDA_OK) return rc;
-    kda::CopyArgs a;
+    kda::CopyArgs a{};
     a.n = n;
     a.object_bytes = kda_object_bytes(H, d, dtype);
-    a.pool = pool_view(p, pool_base, H, d, dtype);
+    a.pool = kda::pool_view(p, pool_base, H, d, dtype);
     a.src_pages = static_cast<const int32_t *>(ws);
     a.dst_pages = static_cast<const int32_t *>(ws) + (size_t)n * P;
     a.status = status;
@@ -114,6 +96,28 @@ int copy_objects(kda_pool *p, int32_t H, int32_t d, int32_t dtype, int32_t n, co
 }
 
 }  // namespace
+
+namespace kda {
+
+PoolView pool_view(const kda_pool *p, void *base, int32_t H, int32_t d, int32_t dtype) {
+    PoolView v;
+    v.base = static_cast<uint8_t *>(base);
+    v.page_bytes = p->page_bytes;
+    v.num_pages = p->num_pages;
+    v.pages_per_object = kda_object_pages(p, H, d, dtype);
+    v.rec_bytes = kda_record_bytes(d, dtype);
+    v.page_shift = -1;
+    for (int32_t sh = 0; sh < 63; ++sh)
+        if (((int64_t)1 << sh) == p->page_bytes) v.page_shift = sh;
+    // pages of 4 GiB or more: every in-object offset (below 4 GiB) is on page 0, which the
+    // multiply gives with a zero reciprocal
+    v.page_magic = p->page_bytes < ((int64_t)1 << 32)
+                       ? (uint32_t)((((uint64_t)1 << 32) + (uint64_t)p->page_bytes - 1) / (uint64_t)p->page_bytes)
+                       : 0u;
+    return v;
+}
+
+}  // namespace kda
 
 extern "C" {
 
@@ -304,11 +308,11 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
     int rc = kda::stage_upload(pool, blob.data(), (size_t)L.meta, workspace, st);
     if (rc != KDA_OK) return rc;
 
-    kda::PrefillArgs a;
+    kda::PrefillArgs a{};
     a.H = H; a.d = d; a.dtype = dtype; a.nseq = nseq;
     a.T_tot = T_tot;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.conv_w = conv_w; a.o = o;
-    a.pool = pool_view(pool, pool_base, H, d, dtype);
+    a.pool = kda::pool_view(pool, pool_base, H, d, dtype);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     a.seqs = reinterpret_cast<const SeqMeta *>(ws);
     a.ckpts = reinterpret_cast<const CkptMeta *>(ws + L.o_ck);
@@ -336,10 +340,10 @@ int kda_decode_step_pp(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype
     if (B == 0) return KDA_OK;
     if (!q || !k || !v || !alpha || !beta || !conv_w || !o || !pool_base || !src_pages || !dst_pages)
         return KDA_EINVAL;
-    kda::DecodeArgs a;
+    kda::DecodeArgs a{};
     a.H = H; a.d = d; a.dtype = dtype; a.B = B;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.conv_w = conv_w; a.o = o;
-    a.pool = pool_view(pool, pool_base, H, d, dtype);
+    a.pool = kda::pool_view(pool, pool_base, H, d, dtype);
     a.state_pages = src_pages;
     a.dst_pages = dst_pages;
     a.status = status_dev;
@@ -523,12 +527,12 @@ int convert_q8(kda_pool *p, int32_t H, int32_t d, int32_t dtype, int32_t n, cons
     std::memcpy(both.data() + (size_t)n * P, q8, (size_t)n * Pq * 4);
     int rc = kda::stage_upload(p, both.data(), both.size() * 4, ws, stream);
     if (rc != KDA_OK) return rc;
-    kda::Q8Args a;
+    kda::Q8Args a{};
     a.n = n;
     a.H = H;
     a.d = d;
     a.dtype = dtype;
-    a.full = pool_view(p, pool_base, H, d, dtype);
+    a.full = kda::pool_view(p, pool_base, H, d, dtype);
     a.q8 = a.full;
     a.q8.pages_per_object = Pq;
     a.q8.rec_bytes = kda_record_bytes_q8(d, dtype);
@@ -609,10 +613,10 @@ int host_copy(kda_pool *p, int32_t H, int32_t d, int32_t dtype, int32_t n, const
     const int32_t P = kda_object_pages(p, H, d, dtype);
     int rc = kda::stage_upload(p, pages, (size_t)n * P * 4, ws, stream);
     if (rc != KDA_OK) return rc;
-    kda::HostCopyArgs a;
+    kda::HostCopyArgs a{};
     a.n = n;
     a.object_bytes = kda_object_bytes(H, d, dtype);
-    a.pool = pool_view(p, pool_base, H, d, dtype);
+    a.pool = kda::pool_view(p, pool_base, H, d, dtype);
     a.pages = static_cast<const int32_t *>(ws);
     a.host = static_cast<uint8_t *>(host);
     a.to_host = to_host ? 1 : 0;

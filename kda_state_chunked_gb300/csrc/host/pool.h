@@ -8,6 +8,8 @@
 
 #include <cuda_runtime.h>
 
+#include "../kda_internal.h"
+
 struct kda_pool {
     int64_t page_bytes = 0;
     int32_t num_pages = 0;
@@ -43,6 +45,10 @@ uint32_t pool_new_stamp(kda_pool *p);
 int pool_alloc(kda_pool *p, int32_t n, int32_t *out);
 int pool_decref(kda_pool *p, int32_t n, const int32_t *ids);
 int pool_incref(kda_pool *p, int32_t n, const int32_t *ids);
+
+// Geometry of `p` for objects of H heads (d, dtype), with the page translation constants
+// (shift for power-of-two page sizes, reciprocal otherwise) that every kernel uses.
+PoolView pool_view(const kda_pool *p, void *base, int32_t H, int32_t d, int32_t dtype);
 
 // Copy `bytes` of host data to device memory `dst` on `stream` through a pinned slot.
 // The host data may be reused as soon as this returns.

@@ -128,15 +128,12 @@ extern "C" int kda_prefill_varlen_noalloc(kda_pool *pool, int32_t H, int32_t d, 
     if (cudaMemcpyAsync(g_dev_ptr[dev], g_host_meta, total, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return KDA_ECUDA;
 
-    kda::PrefillArgs a;
+    kda::PrefillArgs a{};
     a.H = H; a.d = d; a.dtype = dtype; a.nseq = nseq;
     a.T_tot = T_tot;
     a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.conv_w = conv_w; a.o = o;
-    a.pool.base = static_cast<uint8_t *>(pool_base);
-    a.pool.page_bytes = pool->page_bytes;
-    a.pool.num_pages = pool->num_pages;
-    a.pool.pages_per_object = P;
-    a.pool.rec_bytes = kda_record_bytes(d, dtype);
+    // the same pool geometry (page translation constants included) as every other call
+    a.pool = kda::pool_view(pool, pool_base, H, d, dtype);
     uint8_t *ws = static_cast<uint8_t *>(g_dev_ptr[dev]);
     a.seqs = reinterpret_cast<const SeqMeta *>(ws);
     a.ckpts = reinterpret_cast<const CkptMeta *>(ws + o_ck);
