@@ -48,11 +48,12 @@ def _decode_case(dtype, d, B, H, steps, page_bytes, seed):
         og = o.float().cpu().numpy()
         for b in range(B):
             for h in range(H):
-                assert_close(og[b, h], r["o"][b, h], TOL[dtype], f"step {step} o req {b} head {h}")
+                assert_close(og[b, h], r["o"][b, h], TOL[dtype], f"step {step} o req {b} head {h}",
+                             name=f"decode cases ({dtype})")
     for b in range(B):
         S, W = read_object(pool, table[b], H, d, dtype)
         for h in range(H):
-            assert_close(S[h], S_ref[b, h], TOL[dtype], f"final S req {b} head {h}")
+            assert_close(S[h], S_ref[b, h], TOL[dtype], f"final S req {b} head {h}", name=f"decode cases ({dtype})")
         assert np.array_equal(W, W_ref[b])
 
 

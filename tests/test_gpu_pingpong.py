@@ -107,9 +107,11 @@ def test_decode_interval_checkpoints_by_donation_match_the_oracle():
             Sg, Wg = read_object(pool, pages, H, d, dtype)
             Sref, Wref = states[pp]
             for h in range(H):
-                assert_close(Sg[h], Sref[h], TOL[dtype], f"checkpoint req {r} pos {pp} head {h}")
+                assert_close(Sg[h], Sref[h], TOL[dtype], f"checkpoint req {r} pos {pp} head {h}",
+                             name=f"ping-pong decode checkpoints ({dtype})")
             assert np.array_equal(Wg, Wref), f"window req {r} pos {pp}"
         Sg, Wg = read_object(pool, act[r], H, d, dtype)
         for h in range(H):
-            assert_close(Sg[h], S[0, h], TOL[dtype], f"final req {r} head {h}")
+            assert_close(Sg[h], S[0, h], TOL[dtype], f"final req {r} head {h}",
+                         name=f"ping-pong decode checkpoints ({dtype})")
         assert np.array_equal(Wg, W[0])

@@ -35,7 +35,7 @@ def test_single_sequence(dtype, d, T):
     run = Prefill(pool, dev, cu, sp, [0], act, stride=1, include_last=True)
     ck = oracle_positions(cu, sp, 1, True)
     ref = oracle_prefill(cpu, cu, sp, ckpt_abs=ck)
-    compare_prefill(pool, run, ref, cu, act, dtype, ck)
+    compare_prefill(pool, run, ref, cu, act, dtype, ck, name=f"prefill cases ({dtype})")
 
 
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
@@ -59,7 +59,7 @@ def test_varlen_batch_with_restored_states(dtype, d):
     run = Prefill(pool, dev, cu, starts, init, act, stride=2, include_last=True)
     ck = oracle_positions(cu, starts, 2, True)
     ref = oracle_prefill(cpu, cu, starts, S0=S0, win0=W0, ckpt_abs=ck)
-    compare_prefill(pool, run, ref, cu, act, dtype, ck)
+    compare_prefill(pool, run, ref, cu, act, dtype, ck, name=f"prefill cases ({dtype})")
 
 
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
@@ -97,7 +97,8 @@ def test_resume_from_every_512_boundary(dtype, d):
         for h in range(H):
             from kda_cases import assert_close
             assert_close(o_part[:, h], o_full[:, h], TOL[dtype], f"resume {B} o head {h}")
-            assert_close(o_part[:, h], ref_full["o"][B:, h], TOL[dtype], f"resume {B} o vs oracle")
+            assert_close(o_part[:, h], ref_full["o"][B:, h], TOL[dtype], f"resume {B} o vs oracle",
+                         name=f"prefill cases ({dtype})")
             assert_close(S_p[h], S_full[h], TOL[dtype], f"resume {B} S head {h}")
         assert np.array_equal(W_p, W_full)
         # checkpoints after B agree in position with the uninterrupted run
@@ -204,4 +205,4 @@ def test_scattered_pages_of_a_non_power_of_two_size(dtype, d):
     run = Prefill(pool, dev, cu, starts, init, act, stride=2, include_last=True)
     ck = oracle_positions(cu, starts, 2, True)
     ref = oracle_prefill(cpu, cu, starts, S0=S0, win0=W0, ckpt_abs=ck)
-    compare_prefill(pool, run, ref, cu, act, dtype, ck)
+    compare_prefill(pool, run, ref, cu, act, dtype, ck, name=f"prefill cases ({dtype})")

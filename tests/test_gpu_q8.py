@@ -124,11 +124,13 @@ def test_decode_continues_from_an_int8_restore():
         og = o.float().cpu().numpy()
         for b in range(B):
             for h in range(H):
-                assert_close(og[b, h], r["o"][b, h], TOL[dtype], f"step {step} o req {b} head {h}")
+                assert_close(og[b, h], r["o"][b, h], TOL[dtype], f"step {step} o req {b} head {h}",
+                             name=f"decode after INT8 restore ({dtype})")
     for b in range(B):
         Sg, Wg = read_object(pool, act[b], H, d, dtype)
         for h in range(H):
-            assert_close(Sg[h], S_ref[b, h], TOL[dtype], f"S req {b} head {h}")
+            assert_close(Sg[h], S_ref[b, h], TOL[dtype], f"S req {b} head {h}",
+                         name=f"decode after INT8 restore ({dtype})")
         assert np.array_equal(Wg, W_ref[b])
 
 

@@ -1,19 +1,27 @@
-"""Tensor-core building blocks of the prefill kernel, checked against a plain fp32 matmul:
+"""Tensor-core building blocks of the prefill kernels, checked against a plain fp32 matmul:
 operand layouts (K-major / MN-major, 128-byte swizzle), descriptors, negate-A,
 accumulation, TMEM readback and a TMA-loaded operand.  Products of bf16 values are exact
-in fp32, so the only difference is the fp32 summation order."""
+in fp32, so the only difference is the fp32 summation order.  The self-test kernel lives in
+the test-only library libkda_selftest.so, built beside libkda.so."""
 import ctypes
+import functools
 
 import pytest
 import torch
 
-import kda_state_chunked_gb300 as kda
+from kda_state_chunked_gb300 import build as kda_build
 
 pytestmark = pytest.mark.gpu
 
 
+@functools.lru_cache(maxsize=1)
+def _selftest_lib():
+    kda_build.build()
+    return ctypes.CDLL(kda_build.SELFTEST_SO)
+
+
 def _run(K, N, a_mn, b_mn, neg, use_tma, seed=0):
-    L = kda.lib()
+    L = _selftest_lib()
     f = L.kda_internal_mma_selftest
     f.restype = ctypes.c_int
     f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 6 + [ctypes.c_void_p, ctypes.c_void_p]

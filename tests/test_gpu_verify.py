@@ -52,10 +52,12 @@ def test_verify_intermediate_states_and_accept(dtype, d, page_bytes):
         S_ref, W_ref = r["S"], r["win"]
         for b in range(B):
             for h in range(H):
-                assert_close(og[j, b, h], r["o"][b, h], TOL[dtype], f"draft {j} o req {b} head {h}")
+                assert_close(og[j, b, h], r["o"][b, h], TOL[dtype], f"draft {j} o req {b} head {h}",
+                             name=f"speculative verify ({dtype})")
             Sg, Wg = read_object(pool, inter[j, b], H, d, dtype)
             for h in range(H):
-                assert_close(Sg[h], S_ref[b, h], TOL[dtype], f"draft {j} state req {b} head {h}")
+                assert_close(Sg[h], S_ref[b, h], TOL[dtype], f"draft {j} state req {b} head {h}",
+                             name=f"speculative verify ({dtype})")
             assert np.array_equal(Wg, W_ref[b])
     for b in range(B):
         assert read_object_bytes(pool, src[b], nb) == before[b]
