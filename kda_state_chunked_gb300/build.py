@@ -1,6 +1,7 @@
-"""Build libkda.so in-tree for sm_103a (nvcc for the kernels, g++ for the host code).
+"""Build libkda.so in-tree for sm_103a (nvcc for the kernels, g++ for the host code), and
+the test-only libkda_selftest.so (tensor-core descriptor self-test; only the GPU tests load it).
 
-Translation units compile in parallel; the result lands in kda_state_chunked_gb300/_build/.
+Translation units compile in parallel; the results land in kda_state_chunked_gb300/_build/.
 Usage: python -m kda_state_chunked_gb300.build [--force]
 """
 from __future__ import annotations
@@ -16,12 +17,14 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 SO = os.path.join(BUILD, "libkda.so")
+SELFTEST_SO = os.path.join(BUILD, "libkda_selftest.so")
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 CU_SOURCES = ["kernels/ckpt_copy.cu", "kernels/ckpt_q8.cu", "kernels/decode.cu", "kernels/prefill_simt.cu",
-              "kernels/tc_selftest.cu", "kernels/prefill_tc.cu", "kernels/prefill_split.cu",
+              "kernels/prefill_tc.cu", "kernels/prefill_split.cu", "host/tensor_map.cu",
               "host/prefill_noalloc.cu"]
+SELFTEST_CU = ["selftest/tc_selftest.cu"]
 CPP_SOURCES = ["host/pool.cpp", "host/split_plan.cpp", "host/api.cpp"]
 
 
@@ -51,14 +54,15 @@ def _run(cmd):
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and os.path.exists(SO) and os.path.getmtime(SO) >= _sources_mtime():
+    if (not force and os.path.exists(SO) and os.path.exists(SELFTEST_SO)
+            and min(os.path.getmtime(SO), os.path.getmtime(SELFTEST_SO)) >= _sources_mtime()):
         return SO
     cuda = _cuda_home()
     nvcc = os.path.join(cuda, "bin", "nvcc")
     os.makedirs(BUILD, exist_ok=True)
     inc = ["-I", INCLUDE, "-I", CSRC]
     jobs = []
-    for src in CU_SOURCES:
+    for src in CU_SOURCES + SELFTEST_CU:
         obj = os.path.join(BUILD, src.replace("/", "_") + ".o")
         jobs.append([nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xptxas", "-v" if verbose else "-O3", *inc, "-c", os.path.join(CSRC, src),
@@ -73,10 +77,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for o in outs:
             if o.strip():
                 print(o)
-    objs = [j[-1] for j in jobs]
-    tmp = SO + f".tmp{os.getpid()}"
-    _run([nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs])
-    os.replace(tmp, SO)
+    obj_of = {src: os.path.join(BUILD, src.replace("/", "_") + ".o") for src in CU_SOURCES + SELFTEST_CU + CPP_SOURCES}
+    for so, srcs in ((SO, CU_SOURCES + CPP_SOURCES), (SELFTEST_SO, SELFTEST_CU + ["host/tensor_map.cu"])):
+        tmp = so + f".tmp{os.getpid()}"
+        _run([nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *[obj_of[x] for x in srcs]])
+        os.replace(tmp, so)
     return SO
 
 

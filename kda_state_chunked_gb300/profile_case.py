@@ -13,7 +13,6 @@ Cases
   ckpt-restore        256 objects x 32 heads copied checkpoint -> private, 64 KiB pages
   ckpt-write-q8       the same objects quantised into INT8 checkpoints
   ckpt-restore-q8     INT8 checkpoints dequantised into the private objects
-  mma-issue           cycles per tcgen05.mma for the shapes the prefill kernels use (one CTA)
 """
 from __future__ import annotations
 
@@ -100,35 +99,10 @@ def ckpt_q8(launches, dev, n=256, restore=False):
     assert kda.kda_sync_status(st)[0] == kda.KDA_OK
 
 
-def mma_issue(dev):
-    """Cycles per tcgen05.mma (M = 128) for the shapes the prefill kernels issue: the median
-    over rounds of back-to-back groups, from issue of the first to completion of the last."""
-    import ctypes
-    import numpy as np
-    L = kda.lib()
-    f = L.kda_internal_mma_issue_probe
-    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
-    names = {0: "A, B smem, N = 64", 1: "A, B smem, N = 128", 2: "A, B smem, N = 256", 3: "A TMEM, N = 64",
-             4: "A TMEM, N = 128"}
-    reps = 16
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    print("| shape | MMAs | issue cycles | done cycles | cycles / MMA |")
-    print("|---|---:|---:|---:|---:|")
-    for mode in range(5):
-        for n in (1, 8, 64):
-            out = torch.zeros(2 * reps, dtype=torch.int64, device=dev)
-            assert f(out.data_ptr(), mode, n, reps, err.data_ptr(), None) == 0
-            torch.cuda.synchronize()
-            o = out.cpu().numpy().reshape(reps, 2)[4:]
-            print(f"| {names[mode]} | {n} | {int(np.median(o[:, 0]))} | {int(np.median(o[:, 1]))} | "
-                  f"{np.median(o[:, 1]) / n:.0f} |")
-    assert int(err.item()) == 0
-
-
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["prefill-batched", "prefill-long-slice", "decode", "ckpt-restore",
-                                     "ckpt-write-q8", "ckpt-restore-q8", "mma-issue"])
+                                     "ckpt-write-q8", "ckpt-restore-q8"])
     ap.add_argument("--launches", type=int, default=2)
     a = ap.parse_args()
     from kda_state_chunked_gb300.build import build
@@ -144,8 +118,6 @@ def main():
         ckpt_q8(a.launches, dev)
     elif a.case == "ckpt-restore-q8":
         ckpt_q8(a.launches, dev, restore=True)
-    elif a.case == "mma-issue":
-        mma_issue(dev)
     else:
         ckpt_restore(a.launches, dev)
     print("ok")
