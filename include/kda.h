@@ -231,7 +231,9 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
  *     state carries over between calls; calls whose GPU work may overlap (different streams
  *     without ordering between them) race on it.  Calls on one stream are ordered.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine: the metadata is built
- *     in a static host buffer and sent with one pageable cudaMemcpyAsync. */
+ *     in a static host buffer and sent with one cudaMemcpyAsync from that pageable buffer.
+ *     A copy from pageable memory is staged by the runtime before the call returns, and it
+ *     can make the host wait for work already queued on the stream. */
 int kda_prefill_varlen_noalloc(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t nseq,
                                const int32_t *cu_seqlens, const int64_t *start_pos,
                                const uint8_t *has_init, const void *q, const void *k,
@@ -297,8 +299,11 @@ int kda_verify_plan(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t
 /* kda_verify_step: q, k, v, alpha [K][B][H][d] and beta [K][B][H] (device, dtype; draft token
  * major), o [K][B][H][d] written.  src_pages (device int32 [B * P]) holds each request's state
  * before the drafts and is not modified; inter_pages (device int32 [K][B][P]) receives the
- * state after draft token j.  1 <= K <= 64.  Runs as K stream-ordered ping-pong decode steps
- * (kda_decode_step_pp): token j reads the object token j - 1 wrote. */
+ * state after draft token j.  1 <= K <= 64.  For bf16, d = 128, pages of at least 64 KiB and
+ * K <= 8 it is one kernel that reads each source record once and keeps the state on chip
+ * across the K tokens (traffic: one record read and K record writes per request-head);
+ * otherwise it runs as K stream-ordered ping-pong decode steps (kda_decode_step_pp), token j
+ * reading the object token j - 1 wrote. */
 int kda_verify_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32_t B, int32_t K,
                     const void *q, const void *k, const void *v, const void *alpha,
                     const void *beta, const float *conv_w, void *o, void *pool_base,

@@ -378,6 +378,20 @@ int kda_verify_step(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype, i
     if (!q || !k || !v || !alpha || !beta || !conv_w || !o || !pool_base || !src_pages || !inter_pages)
         return KDA_EINVAL;
     const int32_t P = kda_object_pages(pool, H, d, dtype);
+    {
+        // one fused kernel where it applies: each source record read once, the state kept on
+        // chip across the K draft tokens
+        kda::VerifyArgs a{};
+        a.H = H; a.d = d; a.dtype = dtype; a.B = B; a.K = K;
+        a.q = q; a.k = k; a.v = v; a.alpha = alpha; a.beta = beta; a.conv_w = conv_w; a.o = o;
+        a.pool = kda::pool_view(pool, pool_base, H, d, dtype);
+        a.src_pages = src_pages;
+        a.inter_pages = inter_pages;
+        a.status = status_dev;
+        if (kda::verify_fused_supported(a))
+            return kda::launch_verify_fused(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KDA_OK : KDA_ECUDA;
+    }
+    // otherwise K stream-ordered ping-pong decode steps
     const int64_t e = elem_size(dtype), tok = (int64_t)B * H * d * e, btok = (int64_t)B * H * e;
     for (int32_t j = 0; j < K; ++j) {
         // draft token j of every request: state from the previous token's object (or the

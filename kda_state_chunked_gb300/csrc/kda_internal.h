@@ -104,6 +104,20 @@ struct DecodeArgs {
     int32_t *status;
 };
 
+// Speculative verify: K draft tokens per request applied one after another; the state after
+// draft token j of request b goes to its own object.
+struct VerifyArgs {
+    int32_t H, d, dtype, B, K;
+    const void *q, *k, *v, *alpha;   // [K][B][H][d] (draft-token major)
+    const void *beta;                // [K][B][H]
+    const float *conv_w;
+    void *o;                         // [K][B][H][d]
+    PoolView pool;
+    const int32_t *src_pages;        // [B * P] read only
+    const int32_t *inter_pages;      // [K][B][P] written
+    int32_t *status;
+};
+
 struct CopyArgs {
     int32_t n;                    // objects
     int64_t object_bytes;
@@ -145,6 +159,11 @@ inline cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s) {
     return prefill_tc_supported(a) ? launch_prefill_tc(a, s) : launch_prefill_simt(a, s);
 }
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+// Fused verify kernel (bf16, d = 128, pages of at least 64 KiB, K <= kVerifyFusedMaxK): every
+// source record is read once and the state stays on chip across the K draft tokens.
+constexpr int kVerifyFusedMaxK = 8;
+bool verify_fused_supported(const VerifyArgs &a);
+cudaError_t launch_verify_fused(const VerifyArgs &a, cudaStream_t s);
 cudaError_t launch_copy_objects(const CopyArgs &a, cudaStream_t s);
 cudaError_t launch_host_copy(const HostCopyArgs &a, cudaStream_t s);
 cudaError_t launch_ckpt_quantize(const Q8Args &a, cudaStream_t s);

@@ -387,6 +387,246 @@ __global__ void __launch_bounds__(kDtThreads, 1) decode_tma_kernel(DecodeArgs a)
     if (*err && tid == 0) flag_status(a.status, KDA_DEV_TIMEOUT);
 }
 
+
+// ------------------------------------------------------------------------------------------
+// Fused speculative verify for bf16 records of d = 128 in pools of pages of at least 64 KiB:
+// K draft tokens per (request, head) applied one after another ("KIMI K3 경량 복제에서 본 KDA의
+// AI 인프라 과제", §0x06 6.4: the verify pass keeps the intermediate states).  One persistent
+// CTA per SM walks the (request, head) items.  The producer warp bulk-loads an item's source
+// record and its K draft tokens once; the sixteen compute warps move S into registers (thread
+// = one value column and 32 key rows) and the window and drafts into a token history, which
+// frees the input buffer for the next item's load.  For every draft token they run the same
+// step as decode (conv, S' = Diag(alpha) S, w = beta (v - S'^T k), S = S' + k w^T, o = S^T q)
+// and write the resulting record (S and the window after that token) into one of two output
+// buffers, which the producer bulk-stores into that token's object.  The source object is
+// only read.  Traffic per item: one record read and K record writes.
+constexpr int kVfMaxK = kVerifyFusedMaxK;
+constexpr uint32_t VF_IN = 0;                                  // record, then inputs [K][q|k|v|alpha]
+constexpr uint32_t VF_INPUTS = kDtRec;                         // 1 KiB per draft token
+constexpr uint32_t VF_OUT = kDtRec + kVfMaxK * kDtIn;          // two output records
+constexpr uint32_t VF_HIST = VF_OUT + 2 * kDtRec;              // bf16 window [3][384], drafts [K][512]
+constexpr uint32_t VF_HIST_DRAFT = VF_HIST + 3 * 768;
+constexpr uint32_t VF_RED = VF_HIST_DRAFT + kVfMaxK * 1024;    // float [4][128]
+constexpr uint32_t VF_XB = VF_RED + 2048;                      // float [384]
+constexpr uint32_t VF_MISC = VF_XB + 1536;                     // betas, flags, barriers
+constexpr uint32_t VF_SMEM = VF_MISC + 256;
+static_assert(VF_OUT % 128 == 0 && VF_HIST % 16 == 0 && VF_SMEM <= 227 * 1024, "verify shared memory layout");
+
+__global__ void __launch_bounds__(kDtThreads, 1) verify_tma_kernel(VerifyArgs a) {
+    using tcx::named_bar;
+    constexpr int D = 128, C3 = 3 * D;
+    extern __shared__ __align__(128) uint8_t sm[];
+    float *red = reinterpret_cast<float *>(sm + VF_RED);
+    float *xb = reinterpret_cast<float *>(sm + VF_XB);
+    float *beta_s = reinterpret_cast<float *>(sm + VF_MISC);                 // [K]
+    volatile int *valid = reinterpret_cast<volatile int *>(sm + VF_MISC + 32);
+    volatile int *err = reinterpret_cast<volatile int *>(sm + VF_MISC + 36);
+    volatile int *go = reinterpret_cast<volatile int *>(sm + VF_MISC + 40);
+    uint64_t *in_full = reinterpret_cast<uint64_t *>(sm + VF_MISC + 48);
+    uint64_t *in_free = in_full + 1;
+    uint64_t *out_full = in_full + 2;   // [2]
+    uint64_t *out_free = in_full + 4;   // [2]
+    const __nv_bfloat16 *hist_win = reinterpret_cast<const __nv_bfloat16 *>(sm + VF_HIST);
+    const __nv_bfloat16 *hist_draft = reinterpret_cast<const __nv_bfloat16 *>(sm + VF_HIST_DRAFT);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int total = a.B * a.H, K = a.K;
+    const int64_t PB = a.pool.page_bytes;
+    const int P = a.pool.pages_per_object;
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) ptx::mbar_init(&in_full[i], 1);
+        *err = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kDtCompute / 32) {
+        // ------------------------------------------------------------------ producer
+        const __nv_bfloat16 *src[4] = {static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k),
+                                      static_cast<const __nv_bfloat16 *>(a.v),
+                                      static_cast<const __nv_bfloat16 *>(a.alpha)};
+        // the record of head hh in the object whose page list is `pages`, piece by piece
+        // (at most one piece per page it touches)
+        auto record_pieces = [&](const int32_t *pages, int hh, auto &&fn) {
+            int64_t off = (int64_t)hh * a.pool.rec_bytes;
+            uint32_t done_b = 0;
+            while (done_b < kDtRec) {
+                const int64_t pi = off / PB, in = off - pi * PB;
+                const uint32_t len = (uint32_t)((int64_t)(kDtRec - done_b) < PB - in ? (kDtRec - done_b) : (PB - in));
+                fn(pages[pi], in, done_b, len);
+                off += len;
+                done_b += len;
+            }
+        };
+        // check the request's page ids (source and every draft object; the whole warp) and,
+        // when they are valid, load the item's record and draft tokens (lane 0)
+        auto issue_load = [&](int n) -> bool {
+            const int item = blockIdx.x + n * gridDim.x, r = item / a.H;
+            const int32_t *sp = a.src_pages + (int64_t)r * P;
+            bool ok = true;
+            for (int i = lane; i < P; i += 32) ok = ok && (uint32_t)sp[i] < (uint32_t)a.pool.num_pages;
+            for (int jd = 0; jd < K; ++jd) {
+                const int32_t *ip = a.inter_pages + ((int64_t)jd * a.B + r) * P;
+                for (int i = lane; i < P; i += 32) ok = ok && (uint32_t)ip[i] < (uint32_t)a.pool.num_pages;
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            if (lane == 0) {
+                *valid = ok ? 1 : 0;
+                if (!ok) {
+                    flag_status(a.status, KDA_DEV_BAD_PAGE);
+                    ptx::mbar_arrive(in_full);
+                } else {
+                    ptx::mbar_arrive_expect_tx(in_full, kDtRec + (uint32_t)K * kDtIn);
+                    record_pieces(sp, item % a.H, [&](int32_t page, int64_t in, uint32_t at, uint32_t len) {
+                        ptx::bulk_load(sm + VF_IN + at, a.pool.base + (int64_t)page * PB + in, len, in_full);
+                    });
+                    for (int jd = 0; jd < K; ++jd) {
+                        const int64_t tok = ((int64_t)jd * total + item) * D;
+                        for (int x = 0; x < 4; ++x)
+                            ptx::bulk_load(sm + VF_INPUTS + jd * kDtIn + x * 256, src[x] + tok, 256, in_full);
+                    }
+                }
+            }
+            __syncwarp();
+            return ok;
+        };
+        int issued = 0, gv = 0;
+        bool ok_cur = false;
+        if (blockIdx.x < total) {
+            ok_cur = issue_load(0);
+            issued = 1;
+        }
+        for (int n = 0;; ++n) {
+            const int item = blockIdx.x + n * gridDim.x;
+            if (item >= total) break;
+            int stop = 0;
+            // the compute warps have taken item n out of the input buffer
+            if (lane == 0 && (*err || !dt_wait(in_free, (uint32_t)(n & 1), err))) stop = 1;
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+            bool ok_next = false;
+            if (item + (int)gridDim.x < total) {
+                ok_next = issue_load(n + 1);
+                issued = n + 2;
+            }
+            if (ok_cur && lane == 0) {
+                const int r = item / a.H, hh = item % a.H;
+                for (int jd = 0; jd < K; ++jd, ++gv) {
+                    const int ob = gv & 1;
+                    if (!dt_wait(&out_full[ob], (uint32_t)((gv >> 1) & 1), err)) break;
+                    const int32_t *ip = a.inter_pages + ((int64_t)jd * a.B + r) * P;
+                    record_pieces(ip, hh, [&](int32_t page, int64_t in, uint32_t at, uint32_t len) {
+                        ptx::bulk_store(a.pool.base + (int64_t)page * PB + in, sm + VF_OUT + ob * kDtRec + at, len);
+                    });
+                    ptx::bulk_commit();
+                    ptx::bulk_wait_read0();
+                    ptx::mbar_arrive(&out_free[ob]);
+                }
+            }
+            ok_cur = ok_next;
+            __syncwarp();
+        }
+        if (lane == 0) {
+            ptx::bulk_wait0();
+            if (*err && issued > 0) {
+                // leave no load in flight: only the last issued one can be pending
+                uint32_t k = 0;
+                while (!ptx::mbar_try_wait(in_full, (uint32_t)((issued - 1) & 1)) && k < ptx::kSpinLimit) ++k;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ compute
+        const int j = tid & (D - 1), rq = tid >> 7;          // value channel, row quarter
+        // *go is written by thread 0 before a barrier and read by every thread right after it;
+        // the next write comes after at least one more barrier, so all threads agree on it
+        int gv = 0;
+        bool alive = true;
+        for (int n = 0; alive; ++n) {
+            const int item = blockIdx.x + n * gridDim.x;
+            if (item >= total) break;
+            const int hh = item % a.H;
+            if (tid == 0) *go = (dt_wait(in_full, (uint32_t)(n & 1), err) && !*err) ? 1 : 0;
+            named_bar(kDtBar, kDtCompute);
+            alive = *go != 0;
+            if (!alive) break;
+            const bool ok = *valid != 0;
+            float sv[32];
+            if (ok) {
+                const float *S = reinterpret_cast<const float *>(sm + VF_IN);
+#pragma unroll
+                for (int ii = 0; ii < 32; ++ii) sv[ii] = S[(rq * 32 + ii) * D + j];
+                // window rows and draft tokens into the history (16 bytes per thread and step)
+                const uint4 *win = reinterpret_cast<const uint4 *>(sm + VF_IN + D * D * 4);
+                for (int x = tid; x < 3 * C3 * 2 / 16; x += kDtCompute)
+                    reinterpret_cast<uint4 *>(sm + VF_HIST)[x] = win[x];
+                for (int x = tid; x < K * (int)kDtIn / 16; x += kDtCompute)
+                    reinterpret_cast<uint4 *>(sm + VF_HIST_DRAFT)[x] = reinterpret_cast<const uint4 *>(sm + VF_INPUTS)[x];
+                if (tid < K) beta_s[tid] = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.beta)[(int64_t)tid * total + item]);
+            }
+            named_bar(kDtBar, kDtCompute);
+            if (tid == 0) ptx::mbar_arrive(in_free);   // the input buffer may take the next item
+            if (!ok) continue;
+            // raw token r of the sequence window | drafts: r < 3 from the window, else draft r - 3
+            auto raw = [&](int r, int c) -> float {
+                return __bfloat162float(r < 3 ? hist_win[r * C3 + c] : hist_draft[(r - 3) * 512 + c]);
+            };
+            for (int jd = 0; jd < K; ++jd, ++gv) {
+                const int ob = gv & 1;
+                if (tid < C3) {
+                    const int c = tid;
+                    const float4 w = *reinterpret_cast<const float4 *>(a.conv_w + ((int64_t)hh * C3 + c) * 4);
+                    xb[c] = w.x * raw(jd, c) + w.y * raw(jd + 1, c) + w.z * raw(jd + 2, c) + w.w * raw(jd + 3, c);
+                }
+                // the output buffer's previous record has been read by its bulk store
+                if (tid == 0 && gv >= 2) *go = dt_wait(&out_free[ob], (uint32_t)(((gv >> 1) - 1) & 1), err) ? 1 : 0;
+                named_bar(kDtBar, kDtCompute);
+                alive = *go != 0;
+                if (!alive) break;
+                // S' = Diag(alpha) S; partial column sums of S'^T k over this thread's 32 rows
+                float acc = 0.f;
+#pragma unroll
+                for (int ii = 0; ii < 32; ++ii) {
+                    const int i = rq * 32 + ii;
+                    sv[ii] *= __bfloat162float(hist_draft[jd * 512 + C3 + i]);
+                    acc = fmaf(xb[D + i], sv[ii], acc);
+                }
+                red[rq * D + j] = acc;
+                named_bar(kDtBar, kDtCompute);
+                const float u = (red[j] + red[D + j]) + (red[2 * D + j] + red[3 * D + j]);
+                const float wj = beta_s[jd] * (xb[2 * D + j] - u);
+                named_bar(kDtBar, kDtCompute);   // red is reused below
+                // S = S' + k w^T into the output record, and the partial sums of S^T q
+                float *So = reinterpret_cast<float *>(sm + VF_OUT + ob * kDtRec);
+                float ao = 0.f;
+#pragma unroll
+                for (int ii = 0; ii < 32; ++ii) {
+                    const int i = rq * 32 + ii;
+                    sv[ii] = fmaf(xb[D + i], wj, sv[ii]);
+                    So[i * D + j] = sv[ii];
+                    ao = fmaf(xb[i], sv[ii], ao);
+                }
+                red[rq * D + j] = ao;
+                // the window after this token: raw tokens jd + 1 .. jd + 3
+                if (tid < 3 * C3 / 8) {
+                    const int u = tid / (C3 / 8), c = (tid % (C3 / 8)) * 8, r = jd + 1 + u;
+                    const uint4 v4 = r < 3 ? *reinterpret_cast<const uint4 *>(hist_win + r * C3 + c)
+                                           : *reinterpret_cast<const uint4 *>(hist_draft + (r - 3) * 512 + c);
+                    *reinterpret_cast<uint4 *>(sm + VF_OUT + ob * kDtRec + D * D * 4 + (u * C3 + c) * 2) = v4;
+                }
+                ptx::fence_proxy_async_smem();
+                named_bar(kDtBar, kDtCompute);
+                if (tid == 0) ptx::mbar_arrive(&out_full[ob]);
+                if (rq == 0) {
+                    const float o = (red[j] + red[D + j]) + (red[2 * D + j] + red[3 * D + j]);
+                    static_cast<__nv_bfloat16 *>(a.o)[((int64_t)jd * total + item) * D + j] = __float2bfloat16_rn(o);
+                }
+                named_bar(kDtBar, kDtCompute);   // red and xb are reused by the next token
+            }
+        }
+    }
+    __syncthreads();
+    if (*err && tid == 0) flag_status(a.status, KDA_DEV_TIMEOUT);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
@@ -407,6 +647,24 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     if (a.d == 64) return a.dtype == KDA_BF16 ? launch_decode_t<64, __nv_bfloat16>(a, s)
                                               : launch_decode_t<64, float>(a, s);
     return cudaErrorInvalidValue;
+}
+
+bool verify_fused_supported(const VerifyArgs &a) {
+    return a.d == 128 && a.dtype == KDA_BF16 && a.pool.rec_bytes == (int64_t)kDtRec && a.pool.page_bytes >= 65536 &&
+           a.K >= 1 && a.K <= kVfMaxK;
+}
+
+cudaError_t launch_verify_fused(const VerifyArgs &a, cudaStream_t s) {
+    if (a.B <= 0) return cudaSuccess;
+    if (!verify_fused_supported(a)) return cudaErrorInvalidValue;
+    int dev = 0, nsm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(verify_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)VF_SMEM);
+    if (e != cudaSuccess) return e;
+    const int total = a.B * a.H;
+    verify_tma_kernel<<<(unsigned)(total < nsm ? total : nsm), kDtThreads, VF_SMEM, s>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace kda
