@@ -5,8 +5,10 @@ tokens, H = 16, d = 128, bf16 inputs, fp32 state, chunk 64, checkpoints at every
 512-token hash-block end into a pool of 64 KiB pages): host checkpoint plan and page
 allocation, one prefill launch (conv, chunked recurrence, outputs, checkpoint streaming,
 final-state write), then the checkpoint pages are released for the next step.  The decode
-step (256 requests x 32 heads through a permuted page table) and checkpoint write/restore
-copies are measured in the same run and reported beside the headline number.
+step (256 requests x 32 heads through a permuted page table), checkpoint write/restore
+copies, the plain CPU-GPU link copy rate, the 1M-token long-context prefill and the
+varlen-resume prefill are measured in the same run and reported beside the headline number,
+and the oracle is timed on bounded samples of each workload on the host cores.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch under torch.distributed.run: each rank runs its own batch on its own GPU
@@ -413,22 +415,22 @@ def _prefill_algorithmic_bytes(token_heads: int, objects: int, H: int, rec: int)
     return token_heads * (4 * 256 + 2 + 256) + objects * H * rec
 
 
-def _long_phase(dev, steps=5, warmup=3):
-    """Long-context prefill: one sequence, H = 32, a 65,536-token slice of the 1M-token
-    workload (1,024 chunks per chain; the chain kernel dominates, so the per-token cost is
-    that of the full sequence), checkpoints at every 4th 512-token hash-block end."""
+def _long_phase(dev, steps=3, warmup=3):
+    """Long-context prefill at its full size: one sequence of 1,048,576 tokens, H = 32, chunk
+    64, checkpoints at every 4th 512-token hash-block end (512 checkpoints of 32 head records,
+    1.11 GB streamed to the pool during the prefill), final state into the active object."""
     import torch
     import kda_state_chunked_gb300 as kda
     from kda_state_chunked_gb300 import workloads
     w = workloads.WORKLOADS["long"]
-    T = 65536
+    T = w.T
     dt = kda.DTYPES[w.dtype]
     toks = workloads.make_tokens(T, w.H, w.d, w.dtype, w.seed, dev)
-    pool = kda.Pool(w.page_bytes, 64 + (T // 2048 + 2) * 34, dev)
+    n_ck = len(kda.kda_ckpt_positions(0, T, w.hash_block, w.stride, w.include_last))
+    pool = kda.Pool(w.page_bytes, 64 + (n_ck + 2) * 34, dev)
     P = pool.object_pages(w.H, w.d, dt)
     act = kda.kda_page_alloc(pool, P).reshape(1, P)
     cu, st0 = [0, T], [0]
-    n_ck = len(kda.kda_ckpt_positions(0, T, w.hash_block, w.stride, w.include_last))
     ws = kda.prefill_workspace(toks["q"], cu, st0, n_ck, P)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     o = torch.empty_like(toks["q"])
@@ -443,9 +445,14 @@ def _long_phase(dev, steps=5, warmup=3):
     assert kda.kda_sync_status(status)[0] == kda.KDA_OK
     ms = statistics.median(per)
     ab = _prefill_algorithmic_bytes(T * w.H, n_ck + 1, w.H, kda.kda_record_bytes(w.d, dt))
-    return {"workload": "long context: 1 sequence x 65,536 tokens (slice of the 1M-token workload), H=32, "
-                        "stride 4 checkpoints", "tokens": T, "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
-            "algorithmic_bytes": ab, "achieved_gbs": ab / (ms * 1e-3) / 1e9, "steps": steps}
+    launches = kda.kda_prefill_kernel_launches(w.H, w.d, dt, cu, st0)
+    del toks, o, ws, pool
+    torch.cuda.empty_cache()
+    return {"workload": f"long context: 1 sequence x {T:,} tokens, H={w.H}, d=128, bf16, chunk 64, "
+                        f"{n_ck} checkpoints (every 4th 512-token hash-block end), 64 KiB pages",
+            "tokens": T, "checkpoints": n_ck, "ms_per_step": ms, "tokens_per_s": T / (ms * 1e-3),
+            "algorithmic_bytes": ab, "achieved_gbs": ab / (ms * 1e-3) / 1e9, "steps": steps,
+            "launches_per_step": launches}
 
 
 def _varlen_phase(dev, steps=5, warmup=3):
@@ -525,6 +532,75 @@ def _oracle_sample(toks_cpu_fn, threads_note=True):
     return {"value": w.T / sec, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"sequence 0 of the batched workload: {w.T} tokens x {w.H} heads, conv + "
                       f"fp64 token recurrence + 4 checkpoints ({sec:.2f} s wall)"}
+
+
+def _oracle_workloads():
+    """The oracle (as it stands, on the host cores) on bounded samples of the other workloads:
+    one whole decode step (256 requests x 32 heads from random resident states), and 4,096-token
+    samples x 32 heads shaped like the varlen-resume suffixes (resumed from a state) and the
+    long-context sequence (checkpoints every 2,048 tokens)."""
+    import numpy as np
+    import oracle
+    from kda_state_chunked_gb300 import workloads
+    out = {}
+    w = workloads.WORKLOADS["decode"]
+    t = workloads.decode_step_tokens(w.nseq, w.H, w.d, w.dtype, w.seed, 0, "cpu")
+    cw = workloads.make_tokens(1, w.H, w.d, w.dtype, w.seed, "cpu")["conv_w"]
+    rng = np.random.default_rng(w.seed)
+    S0 = rng.standard_normal((w.nseq, w.H, w.d, w.d)) * 0.3
+    W0 = rng.standard_normal((w.nseq, w.H, 3, 3 * w.d))
+    t0 = time.perf_counter()
+    oracle.kda_run(t["q"], t["k"], t["v"], t["alpha"], t["beta"], cw, list(range(w.nseq + 1)), S0=S0, win0=W0)
+    sec = time.perf_counter() - t0
+    out["decode"] = {"value": sec * 1e6, "unit": "us per decode step", "kind": "oracle",
+                     "sample": f"one whole step: {w.nseq} requests x {w.H} heads, one token each, from resident "
+                               f"states ({sec:.3f} s wall)"}
+    del S0, W0
+    T = 4096
+    for name, seed, init, ck in (("varlen_resume", workloads.WORKLOADS["varlen_resume"].seed, True, []),
+                                  ("long", workloads.WORKLOADS["long"].seed, False, [2048, 4096])):
+        ww = workloads.WORKLOADS[name]
+        t = workloads.make_tokens(T, ww.H, ww.d, ww.dtype, seed, "cpu")
+        S0 = rng.standard_normal((1, ww.H, ww.d, ww.d)) * 0.3 if init else None
+        W0 = rng.standard_normal((1, ww.H, 3, 3 * ww.d)) if init else None
+        t0 = time.perf_counter()
+        oracle.kda_run(t["q"], t["k"], t["v"], t["alpha"], t["beta"], t["conv_w"], [0, T], S0=S0, win0=W0,
+                       ckpt_counts=[ck])
+        sec = time.perf_counter() - t0
+        out[name] = {"value": T / sec, "unit": "tokens/s", "kind": "oracle",
+                     "sample": f"{T} tokens x {ww.H} heads of a {'resumed suffix' if init else 'fresh sequence'}"
+                               f" ({sec:.2f} s wall)"}
+    return out
+
+
+def _link_phase(dev, nbytes=1 << 30, reps=5):
+    """Plain copy rate of the CPU-GPU link: one cudaMemcpyAsync of 1 GiB per call between
+    pinned host memory and the device, each direction timed over `reps` calls after two
+    untimed ones, CUDA events on the copying stream."""
+    import torch
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name in ("h2d", "d2h"):
+        for warm in (True, False):
+            count = 2 if warm else reps
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(count):
+                if name == "h2d":
+                    d.copy_(host, non_blocking=True)
+                else:
+                    host.copy_(d, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+        res[name + "_gbs"] = nbytes * reps / (ms * 1e-3) / 1e9
+    res["bytes_per_copy"] = nbytes
+    res["how"] = "pinned host <-> device cudaMemcpyAsync, 1 GiB per call, mean of 5 calls"
+    del host, d
+    return res
 
 
 # --------------------------------------------------------------------------- replicas
@@ -670,6 +746,13 @@ def run_ours(args, rank, world, dev):
         io = _ckpt_io_phase(dev)
         for k in ("write", "restore", "write_q8", "restore_q8"):
             io[k]["frac"] = io[k]["gbs"] / peaks["hbm_gbs"]
+        link = _link_phase(dev)
+        line["link"] = link
+        for k, direction in (("offload", "d2h_gbs"), ("prefetch", "h2d_gbs")):
+            io[k]["link_frac"] = io[k]["gbs"] / link[direction]
+        e2e_in_gbs = h2d / (e2e_ms / args.steps * 1e-3) / 1e9
+        line["e2e"]["h2d_gbs"] = e2e_in_gbs
+        line["e2e"]["link_frac"] = e2e_in_gbs / link["h2d_gbs"]
         line["ckpt_io"] = io
         for name, fn in (("long_prefill", _long_phase), ("varlen_resume", _varlen_phase)):
             r = fn(dev)
@@ -681,6 +764,8 @@ def run_ours(args, rank, world, dev):
         def cpu_toks():
             return {k: (v[:w.T] if k != "conv_w" else v).cpu() for k, v in bench.toks.items()}
         line["cpu_baseline"] = _oracle_sample(cpu_toks)
+        if not args.no_extras:
+            line["cpu_baseline"]["workloads"] = _oracle_workloads()
     return line
 
 

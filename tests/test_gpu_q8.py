@@ -152,3 +152,41 @@ def test_int8_restore_refuses_pages_outside_the_pool():
     assert e.value.code == kda.KDA_EINVAL
     assert pool.free_count() == free0
     assert kda.kda_sync_status(st) == (kda.KDA_OK, 0)
+
+
+def test_write_q8_near_rounding_ties_bit_for_bit():
+    """Rows built so that S[i][j] / scale_i lies exactly on, or one or two fp32 steps beside, a
+    half-integer, over scales from 1e-30 to 1e30: the quantiser's fast reciprocal path must take
+    the same integer decisions as the IEEE division of the oracle codec on every element."""
+    dtype, d, H, page_bytes = "bf16", 128, 4, 65536
+    dt = kda.DTYPES[dtype]
+    P = policy.object_pages(H, d, dtype, page_bytes)
+    Pq = q8.object_pages(H, d, dtype, page_bytes)
+    pool = kda.Pool(page_bytes, P + Pq + 8, DEV)
+    src = kda.kda_page_alloc(pool, P).reshape(1, P)
+    rng = np.random.default_rng(123)
+    f32 = np.float32
+    S = np.zeros((H, d, d), dtype=f32)
+    for h in range(H):
+        for i in range(d):
+            amax = f32(10.0 ** rng.uniform(-30, 30))
+            scale = f32(amax / f32(127))
+            row = np.empty(d, dtype=f32)
+            row[0] = amax
+            k = rng.integers(-126, 126, d - 1).astype(f32)
+            base = ((k + f32(0.5)) * scale).astype(f32)
+            steps = np.arange(d - 1) % 5 - 2                   # -2 .. 2 fp32 steps away
+            for u in range(1, 3):
+                base = np.where(steps >= u, np.nextafter(base, f32(np.inf)), base)
+                base = np.where(steps <= -u, np.nextafter(base, f32(-np.inf)), base)
+            row[1:] = np.clip(base, -amax, amax)
+            S[h, i] = rng.permutation(row)
+    g = torch.Generator().manual_seed(5)
+    _, W = random_state(H, d, dtype, g)
+    write_object(pool, src[0], S.astype(np.float64), W, dtype)
+    ws = torch.empty(kda.kda_copy_workspace_bytes(1, P), dtype=torch.uint8, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dst = kda.kda_ckpt_write_q8(pool, H, d, dt, src.reshape(-1), ws, st)
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+    got = read_object_bytes(pool, dst[0], q8.object_bytes(H, d, dtype))
+    assert got == q8.pack_object(S.astype(np.float64), W, dtype)
