@@ -21,6 +21,6 @@ def pytest_terminal_summary(terminalreporter):
         return
     terminalreporter.section("parity margins (max |x - ref| / max |ref|, worst block)")
     for name in sorted(margins):
-        err, tol, test = margins[name]
+        err, tol, test, what = margins[name]
         terminalreporter.write_line(f"{name:48s} {err:.3e}   limit {tol:.0e}   ({err / tol:5.1%} of limit)   "
-                                    f"worst in {test}")
+                                    f"worst: {test}, {what}")

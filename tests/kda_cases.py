@@ -19,12 +19,12 @@ TOL = {"f32": 1e-4, "bf16": 2e-2}
 MARGINS: dict = {}
 
 
-def record_margin(name: str, err: float, tol: float) -> float:
-    """Keep the worst error under `name`, with its limit and the test that produced it."""
-    old = MARGINS.get(name, (0.0, tol, ""))
+def record_margin(name: str, err: float, tol: float, what: str = "") -> float:
+    """Keep the worst error under `name`, with its limit, the test and the block it came from."""
+    old = MARGINS.get(name, (0.0, tol, "", ""))
     if float(err) >= old[0]:
         test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0].split("::")[-1]
-        MARGINS[name] = (float(err), tol, test)
+        MARGINS[name] = (float(err), tol, test, what)
     return err
 
 
@@ -44,7 +44,7 @@ def assert_close(x, ref, tol, what, name=None):
     assert np.all(np.isfinite(np.asarray(x, dtype=np.float64))), f"{what}: non-finite values"
     assert e <= tol, f"{what}: max relative error {e:.3e} > {tol:.1e}"
     if name:
-        record_margin(name, e, tol)
+        record_margin(name, e, tol, what)
     return e
 
 
@@ -76,10 +76,18 @@ def write_object(pool: kda.Pool, pages, S, win, dtype):
 
 
 def random_state(H, d, dtype, gen, scale=0.3):
-    """A random initial (S, window) whose values are exact in the storage types."""
+    """A random initial (S, window) whose values are exact in the storage types.  The window
+    holds three raw tokens drawn like the workload's: q and k parts unit-norm per token, v part
+    N(0, 1) (a window is the raw q | k | v of the last three tokens, and the input recipe
+    normalises q and k per token).  Un-normalised q, k rows would put beta |k_bar|^2 far above 2,
+    a regime no workload input reaches, where the recurrence amplifies every rounding."""
     S = (torch.randn(H, d, d, generator=gen) * scale).float().double().numpy()
     wdt = torch.bfloat16 if dtype == "bf16" else torch.float32
-    win = torch.randn(H, 3, 3 * d, generator=gen).to(wdt).double().numpy()
+    w = torch.randn(H, 3, 3 * d, generator=gen)
+    for part in (0, 1):
+        blk = w[:, :, part * d:(part + 1) * d]
+        w[:, :, part * d:(part + 1) * d] = blk / blk.norm(dim=-1, keepdim=True)
+    win = w.to(wdt).double().numpy()
     return S, win
 
 
@@ -141,20 +149,18 @@ def compare_prefill(pool, run: Prefill, ref, cu, active_pages, dtype, ck_abs, to
         a, b = int(cu[s]), int(cu[s + 1])
         for h in range(H):
             if b > a:
-                worst = max(worst, assert_close(o[a:b, h], ref["o"][a:b, h], tol, f"o seq {s} head {h}"))
+                worst = max(worst, assert_close(o[a:b, h], ref["o"][a:b, h], tol, f"o seq {s} head {h}", name))
         S, W = read_object(pool, active_pages[s], H, d, dtype)
         for h in range(H):
-            worst = max(worst, assert_close(S[h], ref["S"][s, h], tol, f"final S seq {s} head {h}"))
+            worst = max(worst, assert_close(S[h], ref["S"][s, h], tol, f"final S seq {s} head {h}", name))
         assert np.array_equal(W, ref["win"][s]), f"final window seq {s}"
     for n, (s, p) in enumerate(zip(run.seq, run.pos)):
         S, W = read_object(pool, run.pages[n], H, d, dtype)
         idx = _ck_index(run, n)
         for h in range(H):
             worst = max(worst, assert_close(S[h], ref["ck_S"][s][idx][h], tol,
-                                            f"checkpoint {p} seq {s} head {h}"))
+                                            f"checkpoint {p} seq {s} head {h}", name))
         assert np.array_equal(W, ref["ck_win"][s][idx]), f"checkpoint window {p} seq {s}"
-    if name:
-        record_margin(name, worst, tol)
     return worst
 
 

@@ -26,6 +26,10 @@ from kda_cases import (Prefill, TOL, assert_close, compare_prefill, ckpt_lists, 
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
+# names under which the worst errors are reported
+NM_VARLEN = "varlen resume workload prefill (bf16)"
+NM_DECODE = "decode workload, 64 steps (bf16)"
+NM_LONG = "long workload prefill, 4 heads (bf16)"
 
 
 def _cpu_heads(toks, rows, heads):
@@ -127,15 +131,14 @@ def test_varlen_resume_workload():
         mine = [i for i, q in enumerate(run.seq) if int(q) == s]
         cks = [read_object(pool, run.pages[i], H, d, w.dtype) for i in mine]
         for h in range(H):
-            worst = max(worst, assert_close(got_o[:, h], ref["o"][B[s]:, h], tol, f"o seq {s} head {h}"))
-            worst = max(worst, assert_close(S[h], ref["S"][0, h], tol, f"final S seq {s} head {h}"))
+            worst = max(worst, assert_close(got_o[:, h], ref["o"][B[s]:, h], tol, f"o seq {s} head {h}", name=NM_VARLEN))
+            worst = max(worst, assert_close(S[h], ref["S"][0, h], tol, f"final S seq {s} head {h}", name=NM_VARLEN))
             for n, i in enumerate(mine):
                 worst = max(worst, assert_close(cks[n][0][h], ref["ck_S"][0][n][h], tol,
-                                                f"ckpt {run.pos[i]} seq {s} head {h}"))
+                                                f"ckpt {run.pos[i]} seq {s} head {h}", name=NM_VARLEN))
         assert np.array_equal(W, ref["win"][0]), f"final window seq {s}"
         for n in range(len(mine)):
             assert np.array_equal(cks[n][1], ref["ck_win"][0][n]), f"checkpoint window seq {s}"
-    record_margin("varlen resume workload prefill (bf16)", worst, tol)
 
 
 def test_decode_workload():
@@ -183,10 +186,9 @@ def test_decode_workload():
             want = ref["o"][i * n_tok + setup_T:(i + 1) * n_tok]
             S, W = read_object(pool, table[r], H, d, w.dtype)
             for h in range(H):
-                worst = max(worst, assert_close(got[:, h], want[:, h], tol, f"decode o req {r} head {h}"))
-                worst = max(worst, assert_close(S[h], ref["S"][i, h], tol, f"decode state req {r} head {h}"))
+                worst = max(worst, assert_close(got[:, h], want[:, h], tol, f"decode o req {r} head {h}", name=NM_DECODE))
+                worst = max(worst, assert_close(S[h], ref["S"][i, h], tol, f"decode state req {r} head {h}", name=NM_DECODE))
             assert np.array_equal(W, ref["win"][i]), f"decode window req {r}"
-    record_margin("decode workload, 64 steps (bf16)", worst, tol)
 
 
 @pytest.mark.slow
@@ -218,12 +220,11 @@ def test_long_workload_four_heads():
     worst = 0.0
     for i, h in enumerate(heads):
         worst = max(worst, assert_close(run.o[:, h].float().cpu().numpy(), refs[i]["o"][:, 0], tol,
-                                        f"long o head {h}"))
-        worst = max(worst, assert_close(S[h], refs[i]["S"][0, 0], tol, f"long final S head {h}"))
+                                        f"long o head {h}", name=NM_LONG))
+        worst = max(worst, assert_close(S[h], refs[i]["S"][0, 0], tol, f"long final S head {h}", name=NM_LONG))
         assert np.array_equal(W[h], refs[i]["win"][0, 0])
     for n in range(512):
         Sc, Wc = read_object(pool, run.pages[n], H, d, w.dtype)
         for i, h in enumerate(heads):
-            worst = max(worst, assert_close(Sc[h], refs[i]["ck_S"][0][n][0], tol, f"long ckpt {n} head {h}"))
+            worst = max(worst, assert_close(Sc[h], refs[i]["ck_S"][0][n][0], tol, f"long ckpt {n} head {h}", name=NM_LONG))
             assert np.array_equal(Wc[h], refs[i]["ck_win"][0][n][0])
-    record_margin("long workload prefill, 4 heads (bf16)", worst, tol)
