@@ -292,6 +292,17 @@ int kda_prefill_varlen(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int3
         m.ckpt_count = ci - m.ckpt_begin;
     }
     if (ci != n_ckpt) return KDA_EINVAL;   // sequence ids not ascending or out of range
+    if (split) {
+        // each chunk-prep item learns here whether a checkpoint ends its chunk (its window is
+        // written then), instead of searching the checkpoint table on the device
+        for (kda::SplitItem &it : plan.items) {
+            const SeqMeta &m = seqs[it.seq];
+            const int64_t c_end = std::min<int64_t>(m.start_pos + m.len, (m.start_pos / kda::kChunk + it.lc + 1) * kda::kChunk);
+            const auto b = cks.begin() + m.ckpt_begin, e = b + m.ckpt_count;   // positions ascend
+            const auto f = std::lower_bound(b, e, c_end, [](const CkptMeta &c, int64_t p) { return c.pos < p; });
+            it.ckpt = (f != e && f->pos == c_end) ? (int32_t)(f - cks.begin()) : -1;
+        }
+    }
 
     // One upload of the metadata part of the workspace layout.
     std::vector<uint8_t> blob((size_t)L.meta, 0);

@@ -153,7 +153,7 @@ void make_split_plan(int32_t H, int32_t nseq, const int32_t *cu, const int64_t *
             if (l0 >= l1) continue;
             pl.wave_seq_off[(size_t)w * nseq + s] = (int32_t)pl.items.size() - b;
             for (int32_t lc = l0; lc < l1; ++lc)
-                pl.items.push_back(SplitItem{s, lc, (int32_t)(cu[s] + (start[s] / kChunk + lc) * kChunk - start[s]), 0});
+                pl.items.push_back(SplitItem{s, lc, (int32_t)(cu[s] + (start[s] / kChunk + lc) * kChunk - start[s]), -1});
         }
         pl.slot_items = std::max<int64_t>(pl.slot_items, (int64_t)pl.items.size() - b);
     }

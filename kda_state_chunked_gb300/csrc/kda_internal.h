@@ -69,7 +69,7 @@ struct SplitItem {
     int32_t lc;    // chunk index within the sequence's chain
     int32_t row0;  // packed-token row of the chunk's first position (below the sequence's first
                    // row for a chunk that starts before start_pos)
-    int32_t pad;
+    int32_t ckpt;  // index in the checkpoint table of the checkpoint at the chunk's end, or -1
 };
 
 struct SplitArgs {

@@ -14,12 +14,14 @@
 //     conv, decay factors, Kt' = k gamma_r/gamma_C, Qt' = q gamma_r/gamma_C, Kb = k gamma_C/gamma_r,
 //     G | P = [Kt'; Qt'] Kb^T (tcgen05), T = (I + Diag(beta) strict_lower(G))^{-1} Diag(beta)
 //     (CUDA cores + tf32 mma.sync), WK'^T = Kt'^T T^T (tcgen05), and writes one operand image
-//     per item, bf16 and 128-byte swizzled as the chain kernel's MMAs read it: [-WK' | Qt'], Kb,
-//     P, V, T, and gamma_C (fp32).  Conv windows of checkpoints are written here.
+//     per item, bf16 and 128-byte swizzled as the chain kernel's MMAs read it:
+//     Gamma_C [-WK' | Qt'] = [-WK' Gamma_C | q gamma_r], Kb, P, V, T, and gamma_C (fp32).  Conv
+//     windows of checkpoints are written here.
 //
 //   chain_kernel (one CTA per (sequence, head), 512 threads)
 //     S^T resident in TMEM; per chunk: U^T = V^T T^T, then [W^T | O^T] = [U^T | 0] +
-//     (Gamma_C S)^T [-WK' | Qt']^T in one MMA group, S^T <- Gamma_C S^T + W^T Kb,
+//     S^T (Gamma_C [-WK' | Qt'])^T in one MMA group (the decay is in the image, so the state
+//     operand is S itself), S^T <- Gamma_C S^T + W^T Kb,
 //     O^T += W^T P^T; checkpoint states and outputs.  Images arrive by bulk copies,
 //     double-buffered.
 //
@@ -54,7 +56,7 @@ constexpr int D = 128;
 constexpr int C = kChunk;   // 64
 
 // Operand image of one (chunk, head) item (byte offsets; every operand 1024-byte aligned).
-constexpr uint32_t IMG_WQ = 0;       // [2 kb][128 rows: -WK' 0-63 | Qt' 64-127][128 B]  K-major B
+constexpr uint32_t IMG_WQ = 0;       // [2 kb][128 rows: -WK' Gamma_C 0-63 | q gamma_r 64-127][128 B]  K-major B
 constexpr uint32_t IMG_PK = 32768;   // [3 N blocks: P^T | Kb keys 0-63 | Kb keys 64-127][64 rows j][128 B]  MN-major B
 constexpr uint32_t IMG_V = 57344;    // V     [2 kb][64 rows][128 B]   MN-major A operand
 constexpr uint32_t IMG_T = 73728;    // T     [64 rows][128 B]         K-major B operand
@@ -64,17 +66,6 @@ static_assert(IMG_GC + 512 == kImageBytes, "image layout");
 __device__ __forceinline__ uint8_t *image_addr(const SplitArgs &a, int wave, int64_t idx_in_wave, int h) {
     const int64_t slot = wave & 1;
     return a.images + ((slot * a.slot_items + idx_in_wave) * a.p.H + h) * kImageBytes;
-}
-
-// Index of the checkpoint of sequence m at absolute position pos, or -1 (positions ascend).
-__device__ __forceinline__ int find_ckpt(const PrefillArgs &a, const SeqMeta &m, int64_t pos) {
-    int lo = 0, hi = m.ckpt_count;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (a.ckpts[m.ckpt_begin + mid].pos < pos) lo = mid + 1;
-        else hi = mid;
-    }
-    return (lo < m.ckpt_count && a.ckpts[m.ckpt_begin + lo].pos == pos) ? m.ckpt_begin + lo : -1;
 }
 
 // ============================================================================ chunk prep
@@ -224,8 +215,6 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 // reused later, for T and P^T (QVF)
                 ptx::bulk_store(img + IMG_PK + 8192, sm + A_AL, 16384);
                 ptx::bulk_commit();
-                ptx::bulk_store(img + IMG_WQ + 8192, sm + A_KQ + 8192, 8192);
-                ptx::bulk_store(img + IMG_WQ + 16384 + 8192, sm + A_KQ + 16384 + 8192, 8192);
                 ptx::bulk_store(img + IMG_V, sm + A_V, 16384);
                 ptx::bulk_commit();
                 ptx::bulk_wait_read1();
@@ -341,7 +330,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
             // One row: conv, running decay, bf16 operands written in place (Kb over the alpha
             // tile); the pair-summed share of the diagonal q.k of the row goes to `diag`.
             auto row_proc = [&](int r, uint32_t off, float2 xq, float2 xk, float2 xv, float2 al, bool valid) {
-                uint32_t oq = 0, ok = 0, okb = 0, ov = 0;
+                uint32_t oq = 0, ok = 0, okb = 0, ov = 0, oqg = 0;
                 float dpart = 0.f;
                 if (valid) {
                     float2 qb = fmul2(wq[0], wqv[0]), kbv = fmul2(wk[0], wkv[0]), vb = fmul2(wv[0], wvv[0]);
@@ -364,6 +353,8 @@ __global__ void __launch_bounds__(kAThreads, 3)
                     const float2 qs = fmul2(qb, s2), ks = fmul2(kbv, s2);
                     const float2 kr = fmul2(kbv, make_float2(rcp_approx(s2.x), rcp_approx(s2.y)));
                     oq = pack_bf16x2(qs.x, qs.y);
+                    const float2 qg = fmul2(qb, g2);                  // q gamma_r: the image's operand
+                    oqg = pack_bf16x2(qg.x, qg.y);
                     ok = pack_bf16x2(ks.x, ks.y);
                     okb = pack_bf16x2(kr.x, kr.y);
                     ov = pack_bf16x2(vb.x, vb.y);
@@ -373,6 +364,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
                 if ((lane & 3) == 0) diag[r * 16 + (p >> 2)] = dsum;
                 *reinterpret_cast<uint32_t *>(qrow + off) = oq;
+                *reinterpret_cast<uint32_t *>(img + IMG_WQ + kb * 16384 + 8192 + off) = oqg;
                 *reinterpret_cast<uint32_t *>(krow + off) = ok;
                 *reinterpret_cast<uint32_t *>(arow + off) = okb;
                 *reinterpret_cast<uint32_t *>(vrow + off) = ov;
@@ -433,7 +425,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
             named_bar(kAWg, 128);
             {
                 // window of a checkpoint ending here; the final window goes to the scratch
-                const int ck = find_ckpt(pa, m, abs0 + r_end);
+                const int ck = it.ckpt;
                 const uint4 *src = reinterpret_cast<const uint4 *>(halo);
                 if (ck >= 0) {
                     const int32_t *pg = pa.pages + pa.ckpts[ck].pages_off;
@@ -564,7 +556,6 @@ __global__ void __launch_bounds__(kAThreads, 3)
             named_bar(kAWg, 128);
             {
                 // T = inverse * Diag(beta) as the bf16 operand; two threads per row (32 columns each)
-                (void)warp_wait(S, AB_QVF, 0);   // T goes over the first Qt' half: read by then
                 const int r = t & 63, c8 = (t >> 6) * 4;
                 const float4 *row = reinterpret_cast<const float4 *>(Msc + r * 64);
                 const float4 *b4 = reinterpret_cast<const float4 *>(bs);
@@ -604,10 +595,11 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 // t / 64 gets it at position t % 64, negated (the chain accumulates -(Gamma S)^T WK'^T)
                 uint8_t *const wk = sm + A_AL + (t >> 6) * 8192;
                 const uint32_t cb2 = (uint32_t)(t & 63) * 2;
+                const float gt = gC[t];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    *reinterpret_cast<__nv_bfloat16 *>(wk + ptx::sw128_off(c, cb2)) = __float2bfloat16_rn(-w0[c]);
-                    *reinterpret_cast<__nv_bfloat16 *>(wk + ptx::sw128_off(32 + c, cb2)) = __float2bfloat16_rn(-w1[c]);
+                    *reinterpret_cast<__nv_bfloat16 *>(wk + ptx::sw128_off(c, cb2)) = __float2bfloat16_rn(-w0[c] * gt);
+                    *reinterpret_cast<__nv_bfloat16 *>(wk + ptx::sw128_off(32 + c, cb2)) = __float2bfloat16_rn(-w1[c] * gt);
                 }
                 reinterpret_cast<float *>(img + IMG_GC)[t] = gC[t];
             }
@@ -774,7 +766,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
             const uint32_t id_u = ptx::idesc_bf16(128, 64, 1, 0);
             const uint32_t sbase = ptx::smem_u32(sm), wt = sbase + B_WT;
             // Per chunk, in this order, each group after a blocking (bounded) wait on what it
-            // needs: [W^T | O^T] += (Gamma S)^T [-WK' | Qt']^T (needs the scaled state and the
+            // needs: [W^T | O^T] += S^T (Gamma_C [-WK' | Qt'])^T (needs the bf16 state and the
             // emptied O^T; W^T accumulates onto U^T, O^T onto zeros), then [O^T | S^T] +=
             // W^T [P^T | Kb] (needs W^T), then U^T = V^T T^T of the next chunk into the W columns
             // (which E2 has read).  Every MMA holds the tensor pipe about the same time whatever
@@ -794,7 +786,7 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                     issue_u(0);
                 }
                 if (!wait_bar(S, BB_DO, (uint32_t)(n & 1)) || !wait_bar(S, BB_SB + b, par(n))) break;
-                // [W^T | O^T] += (Gamma S)^T [-WK' | Qt']^T
+                // [W^T | O^T] += S^T (Gamma_C [-WK' | Qt'])^T
                 ptx::tc_fence_after();
                 for (int s = 0; s < 8; ++s) {
                     const uint64_t bq = ptx::sdesc_sw128(im + IMG_WQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
@@ -906,9 +898,10 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
         bool ok = true;
         for (int n = 0; n < cnt; ++n) {
             const int b = n & 1;
-            // ---------------- E1: checkpoint S, Gamma_C S in TMEM, bf16 operand
-            // A checkpoint at this chunk boundary is stored from the registers E1 loads S into,
-            // before the decay scaling: no separate pass over S on the chain's critical path.
+            // ---------------- E1: checkpoint S, bf16 operand S^T, then Gamma_C S in TMEM
+            // A checkpoint at this chunk boundary is stored from the registers E1 loads S into: no
+            // separate pass over S on the chain's critical path.  The decay Gamma_C is folded
+            // into the image's first operand, so this part needs nothing from the image.
             const int32_t *ckpg = nullptr;
             if (n >= 1) {
                 if (!(ok = warp_wait(S, BB_M4S + ((n - 1) & 1), par(n - 1)))) break;
@@ -919,8 +912,6 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                     ck_pos = ck_i < m.ckpt_count ? pa.ckpts[m.ckpt_begin + ck_i].pos : INT64_MAX;
                 }
             }
-            if (!(ok = warp_wait(S, BB_FULL + b, par(n)))) break;
-            const float *gcb = reinterpret_cast<const float *>(sm + b * B_SLOT + IMG_GC);
 #pragma unroll 1
             for (int i0 = 0; i0 < 64; i0 += 32) {
                 float v[32], pk[16];
@@ -941,14 +932,14 @@ __global__ void __launch_bounds__(kBThreads, 1) chain_kernel(const SplitArgs a, 
                     }
                 }
 #pragma unroll
-                for (int ii = 0; ii < 32; ++ii) v[ii] *= gcb[ib + i0 + ii];
-#pragma unroll
                 for (int q2 = 0; q2 < 16; ++q2) pk[q2] = __uint_as_float(pack_bf16x2(v[2 * q2], v[2 * q2 + 1]));
                 ptx::tmem_st16(tbase + lanes + COL_SA + b * 64 + ((ib + i0) >> 1), pk);
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             warp_arrive(&S.bar[BB_SB + b]);
+            if (!(ok = warp_wait(S, BB_FULL + b, par(n)))) break;
+            const float *gcb = reinterpret_cast<const float *>(sm + b * B_SLOT + IMG_GC);
             // S <- Gamma_C S in fp32 while the MMAs form W: the state update reads it only after
             // E2 below, which these stores precede
 #pragma unroll 1

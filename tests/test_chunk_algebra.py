@@ -1,10 +1,11 @@
 """The chunk algebra of the tensor-core prefill, written out in fp64 the way the kernels group
 it, checked against the oracle's token recurrence.
 
-Chunk preparation builds one operand image per chunk: [-WK' | Qt'], [P^T | Kb], V, T and
-gamma_C. The chain then applies four steps per chunk:
+Chunk preparation builds one operand image per chunk: Gamma_C [-WK' | Qt'] (the decay of the
+chunk folded into the first operand: [-WK' Gamma_C | q gamma_r]), [P^T | Kb], V, T and gamma_C.
+The chain then applies four steps per chunk:
   1. U^T = V^T T^T;
-  2. [W^T | O^T] = [U^T | 0] + (Gamma_C S)^T [-WK' | Qt']^T;
+  2. [W^T | O^T] = [U^T | 0] + S^T (Gamma_C [-WK' | Qt'])^T;
   3. [O^T | S^T] = [O^T | (Gamma_C S)^T] + W^T [P^T | Kb];
   4. the output of the chunk is O.
 A sign, transpose or grouping error in that design fails here on the CPU. The GPU tests check
@@ -32,7 +33,8 @@ def _image(qb, kb, vb, al, beta):
     A = np.diag(beta) @ np.tril(G, -1)
     T = np.linalg.inv(np.eye(C) + A) @ np.diag(beta)
     WK = T @ Kt                                  # WK' = T Kt'  (C x d)
-    return {"WQ": np.concatenate([-WK, Qt]),     # N rows of the first group's B operand
+    # N rows of the first group's B operand, key columns scaled by gamma_C
+    return {"WQ": np.concatenate([-WK, Qt]) * gC[None, :],
             "PK": np.concatenate([P.T, Kb], axis=1),   # [j][i | key]: the second group's B
             "V": vb, "T": T, "gC": gC}
 
@@ -42,7 +44,7 @@ def _chain_step(ST, img):
     C = img["T"].shape[0]
     GST = ST * img["gC"][None, :]                # (Gamma_C S)^T, keys scaled
     UT = img["V"].T @ img["T"].T                 # U^T = V^T T^T
-    WO = np.concatenate([UT, np.zeros_like(UT)], axis=1) + GST @ img["WQ"].T
+    WO = np.concatenate([UT, np.zeros_like(UT)], axis=1) + ST @ img["WQ"].T
     WT, OT = WO[:, :C], WO[:, C:]
     OS = np.concatenate([OT, GST], axis=1) + WT @ img["PK"]
     return OS[:, :C].T, OS[:, C:]
