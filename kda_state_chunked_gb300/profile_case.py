@@ -82,7 +82,8 @@ def ckpt_q8(launches, dev, n=256, restore=False):
     P = pool.object_pages(H, d, dt)
     Pq = kda.kda_object_pages_q8(pool, H, d, dt)
     src = kda.kda_page_alloc(pool, n * P)
-    pool.base.zero_()
+    torch.manual_seed(7)
+    pool.base.view(torch.float32).normal_(0.0, 0.3)     # every row has a nonzero scale
     ws = torch.empty(kda.kda_copy_workspace_bytes(n, P), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     ck = kda.kda_ckpt_write_q8(pool, H, d, dt, src, ws, st).reshape(-1)
