@@ -13,6 +13,7 @@ Cases
   ckpt-restore        256 objects x 32 heads copied checkpoint -> private, 64 KiB pages
   ckpt-write-q8       the same objects quantised into INT8 checkpoints
   ckpt-restore-q8     INT8 checkpoints dequantised into the private objects
+  verify              speculative verify, 4 draft tokens for 256 requests x 32 heads
 """
 from __future__ import annotations
 
@@ -61,6 +62,28 @@ def decode(launches, dev):
     assert kda.kda_sync_status(st)[0] == kda.KDA_OK
 
 
+def verify(launches, dev, K=4):
+    """Speculative verify: K = 4 draft tokens for 256 requests x 32 heads (256 KiB pages)."""
+    w = workloads.WORKLOADS["decode"]
+    dt = kda.DTYPES[w.dtype]
+    P = 9
+    pool = kda.Pool(w.page_bytes, (K + 1) * w.nseq * P + 8, dev)
+    assert pool.object_pages(w.H, w.d, dt) == P
+    torch.manual_seed(7)
+    pool.base.view(torch.float32).normal_(0.0, 0.3)
+    src = torch.from_numpy(kda.kda_page_alloc(pool, w.nseq * P).reshape(w.nseq, P)).to(dev)
+    inter = torch.from_numpy(kda.kda_verify_plan(pool, w.H, w.d, dt, w.nseq, K)).to(dev)
+    conv_w = workloads.make_tokens(1, w.H, w.d, w.dtype, w.seed, dev)["conv_w"]
+    steps = [workloads.decode_step_tokens(w.nseq, w.H, w.d, w.dtype, w.seed, j, dev) for j in range(K)]
+    dr = {k: torch.stack([x[k] for x in steps]) for k in steps[0]}
+    o = torch.empty_like(dr["q"])
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(launches):
+        kda.kda_verify_step(pool, dr["q"], dr["k"], dr["v"], dr["alpha"], dr["beta"], conv_w, o, src, inter, st)
+    torch.cuda.synchronize()
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+
+
 def ckpt_restore(launches, dev, n=256):
     H, d, dt = 32, 128, kda.KDA_BF16
     pool = kda.Pool(65536, 2 * n * 34 + 64, dev)
@@ -103,7 +126,7 @@ def ckpt_q8(launches, dev, n=256, restore=False):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["prefill-batched", "prefill-long-slice", "decode", "ckpt-restore",
-                                     "ckpt-write-q8", "ckpt-restore-q8"])
+                                     "ckpt-write-q8", "ckpt-restore-q8", "verify"])
     ap.add_argument("--launches", type=int, default=2)
     a = ap.parse_args()
     from kda_state_chunked_gb300.build import build
@@ -119,6 +142,8 @@ def main():
         ckpt_q8(a.launches, dev)
     elif a.case == "ckpt-restore-q8":
         ckpt_q8(a.launches, dev, restore=True)
+    elif a.case == "verify":
+        verify(a.launches, dev)
     else:
         ckpt_restore(a.launches, dev)
     print("ok")
