@@ -88,7 +88,12 @@ constexpr uint32_t A_SMEM = A_BAR + 128 + 1024;
 static_assert(3 * (A_SMEM + 1024) <= 228 * 1024, "three chunk-prep CTAs per SM");
 constexpr int kAWg = 1, kAHalf = 2;   // named barriers (128 and 64 threads)
 
-enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_QVF, AB_PT, AB_T, AB_M2, AB_WK, A_NBARS };
+enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_QVF, AB_PT, AB_T, AB_M2, AB_WK, AB_SO, A_NBARS };
+// bf16 64 x 64 tiles of the tensor-core solve (8 KiB each, row-major, 128-byte swizzle): Binv over
+// the second Qt' half and N over the second V half (both read out by then), E over the first
+// Qt' half; E^2 then takes N's place and G E's place, and T finally G's (A_T).  Round 2 reads
+// [E | Binv] as one N = 128 operand: Binv lies A_SB - A_SE bytes after E.
+constexpr uint32_t A_SB = A_KQ + 16384 + 8192, A_SN = A_V + 8192, A_SE = A_T, A_SE2 = A_SN, A_SG = A_SE;
 constexpr uint32_t A_ERR = 96;   // error flag, TMEM address and wait flag after the mbarriers
 static_assert(A_NBARS * 8 <= A_ERR && A_ERR + 24 <= 128, "prep barrier block");
 
@@ -262,6 +267,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
         const int p = t & 63, hf = t >> 6;              // channel pair (2p, 2p+1), row half
         const int c0 = 2 * p, kb = c0 >> 6, cb = (c0 & 63) * 2;
         const uint32_t lanes = (uint32_t)(warp * 32) << 16;
+        int solve_rounds = 0;   // rounds of the tensor-core solve issued (by thread 0)
         do {
             // conv weights of the channel pair, tap by tap: (channel c0, channel c0 + 1)
             float2 wq[4], wk[4], wv[4];
@@ -485,6 +491,48 @@ __global__ void __launch_bounds__(kAThreads, 3)
             ptx::tc_fence_before();
             named_bar(kAWg, 128);
             if (t == 0) ptx::mbar_arrive(&S.bar[AB_PT]);
+            // Each round: the compute warps write its operands, meet at a barrier, and thread 0
+            // issues the round's MMAs and its commit; the round's completion is polled by
+            // thread 0 and handed to the warpgroup through a flag word of its own (one barrier).
+            volatile int *solve_flag = reinterpret_cast<volatile int *>(sm + A_RED);   // free after the conv
+            auto solve_issue = [&](int rd) {
+                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                named_bar(kAWg, 128);
+                if (t == 0) {
+                    ptx::tc_fence_after();
+                    const uint32_t sbase = ptx::smem_u32(sm);
+                    const uint32_t a_t = rd == 0 ? A_SB : (rd == 1 ? A_SE : A_SE2);
+                    const uint32_t b_t = rd == 0 ? A_SN : (rd == 1 ? A_SE : A_SG);
+                    const uint32_t idr = ptx::idesc_bf16(128, rd == 1 ? 128 : 64, 0, 1);
+                    // K-steps (16-row blocks of the shared dimension) whose products are all zero
+                    // are skipped: N has no entries in its first row block, E none in its last
+                    // column block, E^2 none in its last two
+                    const int s0 = rd == 0 ? 1 : 0, s1 = rd == 2 ? 2 : (rd == 1 ? 3 : 4);
+                    for (int s = s0; s < s1; ++s)
+                        ptx::mma_bf16(tbase, ptx::sdesc_sw128(sbase + a_t + s * 32, 16, 1024),
+                                      ptx::sdesc_sw128(sbase + b_t + s * 2048, A_SB - A_SE, 1024), idr,
+                                      s > s0 ? 1u : 0u);
+                    ptx::mma_commit(&S.bar[AB_SO]);
+                }
+                solve_rounds = rd + 1;
+            };
+            auto solve_wait = [&](int rd) -> bool {
+                if (t == 0) solve_flag[rd] = ptx::mbar_wait(&S.bar[AB_SO], (uint32_t)(rd & 1), S.err) ? 1 : 0;
+                named_bar(kAWg, 128);
+                return solve_flag[rd] != 0;
+            };
+            auto put_row_bf16 = [&](uint32_t tile, int r, int ch0, const float *v8x4) {   // 4 units of 8
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 pk;
+                    pk.x = pack_bf16x2(v8x4[j * 8 + 0], v8x4[j * 8 + 1]);
+                    pk.y = pack_bf16x2(v8x4[j * 8 + 2], v8x4[j * 8 + 3]);
+                    pk.z = pack_bf16x2(v8x4[j * 8 + 4], v8x4[j * 8 + 5]);
+                    pk.w = pack_bf16x2(v8x4[j * 8 + 6], v8x4[j * 8 + 7]);
+                    *reinterpret_cast<uint4 *>(sm + tile + ptx::sw128_off(r, (ch0 + j) * 16)) = pk;
+                }
+            };
             // ---------------- T = (I + A)^{-1} Diag(beta)
             // level 0: the four 16 x 16 diagonal blocks, one row per thread (from the last row up)
             if (t < C) {
@@ -513,74 +561,113 @@ __global__ void __launch_bounds__(kAThreads, 3)
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     row[(bb * 4 + q) ^ (r & 7)] = make_float4(x[q * 4], x[q * 4 + 1], x[q * 4 + 2], x[q * 4 + 3]);
+                // the row of Binv as bf16 (its 16-column block, zeros elsewhere)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 pk = make_uint4(0, 0, 0, 0);
+                    if ((ch >> 1) == bb) {
+                        const float *xs = x + (ch & 1) * 8;
+                        pk.x = pack_bf16x2(xs[0], xs[1]);
+                        pk.y = pack_bf16x2(xs[2], xs[3]);
+                        pk.z = pack_bf16x2(xs[4], xs[5]);
+                        pk.w = pack_bf16x2(xs[6], xs[7]);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + A_SB + ptx::sw128_off(r, ch * 16)) = pk;
+                }
+            } else {
+                // meanwhile: N, the strictly block-lower part of A (untouched by level 0), as bf16
+                const int r = t - C, rb = r >> 4;
+                const float4 *row = reinterpret_cast<const float4 *>(Msc + r * 64);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 pk = make_uint4(0, 0, 0, 0);
+                    if ((ch >> 1) < rb) {
+                        const float4 m0 = row[(ch * 2) ^ (r & 7)], m1 = row[(ch * 2 + 1) ^ (r & 7)];
+                        pk.x = pack_bf16x2(m0.x, m0.y);
+                        pk.y = pack_bf16x2(m0.z, m0.w);
+                        pk.z = pack_bf16x2(m1.x, m1.y);
+                        pk.w = pack_bf16x2(m1.z, m1.w);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + A_SN + ptx::sw128_off(r, ch * 16)) = pk;
+                }
             }
-            named_bar(kAWg, 128);
-            // Off-diagonal blocks in 32 x 32 halves (tf32 mma.sync, one warp per 16 x 16 block):
-            //   J0 = [[I00, 0], [-I11 A10 I00, I11]], J1 likewise, lower-left of the inverse -J1 (B J0).
-            {
-                const int pw = warp;
-                if (pw < 2) {
-                    const int i = pw == 0 ? 1 : 3, j = i - 1;
-                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    blk_mma(acc, Msc, i, j, j, lane);
-                    __syncwarp();
-                    blk_store(Msc, i, j, acc, 1.f, lane);
-                    __syncwarp();
-                    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    blk_mma(acc2, Msc, i, i, j, lane);
-                    __syncwarp();
-                    blk_store(Msc, i, j, acc2, -1.f, lane);
-                }
-                named_bar(kAWg, 128);
-                const int bi = 2 + (pw >> 1), bj = pw & 1;
-                float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                if (bj == 0) {
-                    blk_mma(y, Msc, bi, 0, 0, lane);
-                    blk_mma(y, Msc, bi, 1, 0, lane);
-                } else {
-                    blk_mma(y, Msc, bi, 1, 1, lane);
-                }
-                named_bar(kAWg, 128);
-                blk_store(Msc, bi, bj, y, 1.f, lane);
-                named_bar(kAWg, 128);
-                float z[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                if (bi == 2) {
-                    blk_mma(z, Msc, 2, 2, bj, lane);
-                } else {
-                    blk_mma(z, Msc, 3, 2, bj, lane);
-                    blk_mma(z, Msc, 3, 3, bj, lane);
-                }
-                named_bar(kAWg, 128);
-                blk_store(Msc, bi, bj, z, -1.f, lane);
+            // Off-diagonal part on the tensor cores: with Binv = the block-diagonal inverse and N
+            // the strictly block-lower part of A, L = I + A has L^{-1} = (I - E)(I + E^2) Binv =
+            // G + E^2 G, E = Binv N, G = Binv - E Binv (E^4 = 0).  Three bf16 MMA rounds with
+            // fp32 accumulation: E = Binv N; [E^2 | E Binv] = E [E | Binv]; E^2 G (8 MMAs: the
+            // block structure leaves some 16-deep steps of each product zero).  Every
+            // operand is a 64 x 64 bf16 tile, row-major and 128-byte swizzled, which serves as a
+            // K-major A and as an MN-major B alike.  Rows 0-63 of each M = 128 product are used.
+            solve_issue(0);
+            // round 1 done: E -> bf16 tile (rows 0-63 of the product, lanes of warps 0 and 1)
+            if (!solve_wait(0)) break;
+            ptx::tc_fence_after();
+            if (t < C) {
+                float e0[32], e1[32];
+                ptx::tmem_ld32(tbase + lanes, e0);
+                ptx::tmem_ld32(tbase + lanes + 32, e1);
+                ptx::tmem_wait_ld();
+                put_row_bf16(A_SE, t, 0, e0);
+                put_row_bf16(A_SE, t, 4, e1);
             }
-            named_bar(kAWg, 128);
-            {
-                // T = inverse * Diag(beta) as the bf16 operand; two threads per row (32 columns each)
-                const int r = t & 63, c8 = (t >> 6) * 4;
+            solve_issue(1);
+            // round 2 done: E^2 -> bf16 tile; G = Binv - E Binv -> bf16 tile and fp32 row of Msc
+            if (!solve_wait(1)) break;
+            ptx::tc_fence_after();
+            if (t < C) {
+                const int r = t, rb = r >> 4;
+                float4 *row = reinterpret_cast<float4 *>(Msc + r * 64);
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    float e2[32], eb[32];
+                    ptx::tmem_ld32(tbase + lanes + hh * 32, e2);
+                    ptx::tmem_ld32(tbase + lanes + 64 + hh * 32, eb);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const int cc = hh * 8 + c4;
+                        float4 g4 = make_float4(-eb[c4 * 4], -eb[c4 * 4 + 1], -eb[c4 * 4 + 2], -eb[c4 * 4 + 3]);
+                        if ((cc >> 2) == rb) {
+                            const float4 b4 = row[cc ^ (r & 7)];
+                            g4.x += b4.x; g4.y += b4.y; g4.z += b4.z; g4.w += b4.w;
+                        }
+                        eb[c4 * 4] = g4.x; eb[c4 * 4 + 1] = g4.y; eb[c4 * 4 + 2] = g4.z; eb[c4 * 4 + 3] = g4.w;
+                    }
+                    // Binv of this half read above; G overwrites it (only this thread uses row r)
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4)
+                        row[(hh * 8 + c4) ^ (r & 7)] = make_float4(eb[c4 * 4], eb[c4 * 4 + 1], eb[c4 * 4 + 2], eb[c4 * 4 + 3]);
+                    put_row_bf16(A_SE2, r, hh * 4, e2);
+                    put_row_bf16(A_SG, r, hh * 4, eb);
+                }
+            }
+            solve_issue(2);
+            // round 3 done: T = (G + E^2 G) Diag(beta), lower triangle, as the bf16 operand
+            if (!solve_wait(2)) break;
+            ptx::tc_fence_after();
+            if (t < C) {
+                const int r = t;
                 const float4 *row = reinterpret_cast<const float4 *>(Msc + r * 64);
                 const float4 *b4 = reinterpret_cast<const float4 *>(bs);
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    float d[32];
+                    ptx::tmem_ld32(tbase + lanes + hh * 32, d);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-                for (int ch = c8; ch < c8 + 4; ++ch) {
-                    float ev[8];
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int c4 = ch * 2 + h2;
-                        const float4 mv = row[c4 ^ (r & 7)];
-                        const float4 bv = b4[c4];
-                        ev[h2 * 4 + 0] = c4 * 4 + 0 <= r ? mv.x * bv.x : 0.f;
-                        ev[h2 * 4 + 1] = c4 * 4 + 1 <= r ? mv.y * bv.y : 0.f;
-                        ev[h2 * 4 + 2] = c4 * 4 + 2 <= r ? mv.z * bv.z : 0.f;
-                        ev[h2 * 4 + 3] = c4 * 4 + 3 <= r ? mv.w * bv.w : 0.f;
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const int cc = hh * 8 + c4;
+                        const float4 g4 = row[cc ^ (r & 7)], bv = b4[cc];
+                        d[c4 * 4 + 0] = cc * 4 + 0 <= r ? (g4.x + d[c4 * 4 + 0]) * bv.x : 0.f;
+                        d[c4 * 4 + 1] = cc * 4 + 1 <= r ? (g4.y + d[c4 * 4 + 1]) * bv.y : 0.f;
+                        d[c4 * 4 + 2] = cc * 4 + 2 <= r ? (g4.z + d[c4 * 4 + 2]) * bv.z : 0.f;
+                        d[c4 * 4 + 3] = cc * 4 + 3 <= r ? (g4.w + d[c4 * 4 + 3]) * bv.w : 0.f;
                     }
-                    uint4 v;
-                    v.x = pack_bf16x2(ev[0], ev[1]);
-                    v.y = pack_bf16x2(ev[2], ev[3]);
-                    v.z = pack_bf16x2(ev[4], ev[5]);
-                    v.w = pack_bf16x2(ev[6], ev[7]);
-                    *reinterpret_cast<uint4 *>(sm + A_T + ptx::sw128_off(r, ch * 16)) = v;
+                    put_row_bf16(A_T, r, hh * 4, d);
                 }
             }
             ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
             named_bar(kAWg, 128);
             if (t == 0) ptx::mbar_arrive(&S.bar[AB_T]);
             // ---------------- -WK' (K-major bf16 operand rows, staged for bulk copies) and gamma_C
@@ -608,6 +695,11 @@ __global__ void __launch_bounds__(kAThreads, 3)
             named_bar(kAWg, 128);
             if (t == 0) ptx::mbar_arrive(&S.bar[AB_WK]);
         } while (false);
+        // on a timeout, leave no solve MMA in flight: its commit tracks every MMA before it
+        if (t == 0 && *S.err && solve_rounds > 0) {
+            uint32_t k = 0;
+            while (!ptx::mbar_try_wait(&S.bar[AB_SO], (uint32_t)((solve_rounds - 1) & 1)) && k < ptx::kSpinLimit) ++k;
+        }
     }
     // ---------------------------------------------------------------------- teardown
     ptx::tc_fence_before();
