@@ -581,32 +581,34 @@ def _oracle_workloads():
     return out
 
 
-def _link_phase(dev, nbytes=1 << 30, reps=5):
-    """Plain copy rate of the CPU-GPU link: one cudaMemcpyAsync of 1 GiB per call between
-    pinned host memory and the device, each direction timed over `reps` calls after two
-    untimed ones, CUDA events on the copying stream."""
+def _link_phase(dev, nbytes=1 << 29, reps=9):
+    """Plain copy rate of the CPU-GPU link: one cudaMemcpyAsync of 512 MiB per call between
+    pinned host memory and the device, each direction timed call by call (CUDA events on the
+    copying stream) over `reps` calls after two untimed ones; the median call gives the rate."""
     import torch
     host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     res = {}
     for name in ("h2d", "d2h"):
-        for warm in (True, False):
-            count = 2 if warm else reps
+        times = []
+        for i in range(2 + reps):
             torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for _ in range(count):
-                if name == "h2d":
-                    d.copy_(host, non_blocking=True)
-                else:
-                    host.copy_(d, non_blocking=True)
+            if name == "h2d":
+                d.copy_(host, non_blocking=True)
+            else:
+                host.copy_(d, non_blocking=True)
             b.record(stream)
             torch.cuda.synchronize()
-            ms = a.elapsed_time(b)
-        res[name + "_gbs"] = nbytes * reps / (ms * 1e-3) / 1e9
+            if i >= 2:
+                times.append(a.elapsed_time(b))
+        times.sort()
+        res[name + "_gbs"] = nbytes / (times[len(times) // 2] * 1e-3) / 1e9
+        res[name + "_gbs_range"] = [nbytes / (times[-1] * 1e-3) / 1e9, nbytes / (times[0] * 1e-3) / 1e9]
     res["bytes_per_copy"] = nbytes
-    res["how"] = "pinned host <-> device cudaMemcpyAsync, 1 GiB per call, mean of 5 calls"
+    res["how"] = f"pinned host <-> device cudaMemcpyAsync, 512 MiB per call, median of {reps} calls"
     del host, d
     return res
 

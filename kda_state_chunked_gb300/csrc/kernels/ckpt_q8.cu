@@ -188,26 +188,30 @@ __global__ void __launch_bounds__(kQThreads) dequantize_kernel(Q8Args a) {
 // Bulk-copy pipeline for bf16 records of d = 128 (full record 67,840 B: S fp32 [128][128] and
 // the window; INT8 record 19,200 B: scales, codes, window; neither needs padding) in pools of
 // pages of at least 4 KiB.  One persistent CTA per SM walks the head records.
-//   - A producer warp bulk-loads source records (split at page boundaries) into a ring of
-//     source slots and bulk-stores converted records from a ring of destination slots.  The
-//     page ids of the next item are read into registers one step ahead, so their global
-//     reads overlap the current step.  A store's read-out of shared memory is waited for only
-//     when its destination slot is needed again, two items later.
+//   - A load warp bulk-loads source records (split at page boundaries) into a ring of source
+//     slots, as far ahead as the ring allows: a slot is refilled as soon as the compute warps
+//     have taken its record into registers.
+//   - A store warp bulk-stores converted records from a ring of destination slots; a slot is
+//     released once its store has read it out.
+//   - Both read an item's page ids into registers one step ahead, so those global reads
+//     overlap the current step.
 //   - Sixteen compute warps convert one item at a time from its source slot into its
 //     destination slot: four threads per row of S, 32 consecutive values each (a row's
 //     max-abs is a reduction over its four threads).
-// Quantising: 2 source slots (67,840 B) and 2 destination slots (19,200 B); dequantising: 3
-// source slots (19,200 B) and 2 destination slots (67,840 B).  The codes are those of the
-// per-record kernels above, bit for bit: the division goes through the reciprocal where that
-// provably gives the same integer (see below), through the IEEE division elsewhere.
+// Quantising: 3 source slots (67,840 B) and 1 destination slot (19,200 B); dequantising: 3
+// source slots (19,200 B) and 2 destination slots (67,840 B), with up to two stores in flight.
+// The codes are those of the per-record kernels above, bit for bit: the division goes through
+// the reciprocal where that provably gives the same integer (see below), through the IEEE
+// division elsewhere.
 constexpr int kQtCompute = 512;
-constexpr int kQtThreads = kQtCompute + 32;
+constexpr int kQtThreads = kQtCompute + 64;   // + load warp + store warp
 constexpr uint32_t kQtFull = 67840, kQtQ8 = 19200;
 template <bool QUANT> struct QtGeom {
-    static constexpr int NS = QUANT ? 2 : 3, ND = 2;
+    static constexpr int NS = 3, ND = QUANT ? 1 : 2;
     static constexpr uint32_t SB = QUANT ? kQtFull : kQtQ8, DB = QUANT ? kQtQ8 : kQtFull;
     static constexpr uint32_t DST0 = NS * SB, MISC = DST0 + ND * DB, SMEM = MISC + 256;
     static_assert(SB % 128 == 0 && DB % 128 == 0 && SMEM <= 227 * 1024, "INT8 pipeline shared memory");
+    static_assert(NS <= 4 && ND <= 4, "slot flags: valid[4] at +0, dvalid[4] at +64, barriers from +128");
 };
 
 // Page index of in-object byte offset `off` (below 4 GiB): a shift for power-of-two page
@@ -232,20 +236,22 @@ __device__ __forceinline__ void load_quarter(const float *row, int qq, int rot, 
     for (int k = 0; k < 8; ++k) x[k] = reinterpret_cast<const float4 *>(row)[qq * 8 + ((k + rot) & 7)];
 }
 
-__device__ __forceinline__ void quant_quarter(const float4 (&x)[8], uint8_t *crow, int qq, int rot, float *scale_out) {
+// Codes of the quarter into registers; returns the row's scale.
+__device__ __forceinline__ float quant_quarter(const float4 (&x)[8], uint32_t (&w)[8]) {
     float m = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) m = fmaxf(m, fmaxf(fmaxf(fabsf(x[k].x), fabsf(x[k].y)), fmaxf(fabsf(x[k].z), fabsf(x[k].w))));
     m = quad_max(m);
     const float sc = __fdiv_rn(m, 127.f);
     // code = rint(RN(x / sc)) through the correctly rounded reciprocal, with Ziv's rounding
-    // test: y = RN(x RN(1/sc)) lies within 127 * 2^-23 + 2^-18 < 2^-14 of RN(x / sc)
-    // (|x / sc| <= 127), so rint(y) is that integer unless y is within 2^-14 of a
-    // half-integer.  Such values, and rows whose reciprocal is not finite, take the IEEE
-    // division; the branch is taken per warp and only when a lane needs it.
+    // test.  With rs = RN(1/sc) and y = RN(x rs): |x rs - x/sc| <= |x/sc| 2^-24 < 2^-17
+    // (|x/sc| <= 127 (1 + 2^-23)), and y and RN(x/sc) each lie within half an ulp of 64..128,
+    // 2^-18, of x rs and x/sc.  So |y - RN(x/sc)| < 2^-16, and rint(y) is rint(RN(x/sc))
+    // unless y is within 2^-16 of a half-integer.  Such values, and rows whose reciprocal is
+    // not finite, take the IEEE division; the branch is taken per warp and only when a lane
+    // needs it.
     const float rs = __frcp_rn(sc);
     const bool fast_row = sc > 0.f && isfinite(rs);
-    bool near = !fast_row && sc > 0.f;
     auto pack4 = [](int q0, int q1, int q2, int q3) {
         auto c = [](int q) { return (uint32_t)((q > 127 ? 127 : (q < -127 ? -127 : q)) & 0xff); };
         return c(q0) | (c(q1) << 8) | (c(q2) << 16) | (c(q3) << 24);
@@ -253,34 +259,37 @@ __device__ __forceinline__ void quant_quarter(const float4 (&x)[8], uint8_t *cro
     // Rounding by the magic number 1.5 * 2^23: for |y| < 2^22, t = RN(y + 1.5 * 2^23) is y
     // rounded to the nearest integer (ties to even) plus 1.5 * 2^23, so the low byte of t's bits
     // is that integer's two's complement byte and t - 1.5 * 2^23 is the integer itself (exact).
-    // Here |y| <= 127 (1 + 2^-23), so the code needs no clamp.
+    // Here |y| <= 127 (1 + 2^-23), so the code needs no clamp.  The arithmetic runs on value
+    // pairs (one f32x2 instruction, each lane correctly rounded as the scalar one).
     constexpr float kMagic = 12582912.f;
-    uint32_t w[8];
+    const float2 rs2 = make_float2(rs, rs), mg2 = make_float2(kMagic, kMagic);
+    float dmax = 0.f;   // largest |y - rint(y)| of the quarter
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        const float xs[4] = {x[k].x, x[k].y, x[k].z, x[k].w};
-        uint32_t word = 0;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float y = __fmul_rn(xs[u], rs);
-            const float t = __fadd_rn(y, kMagic);
-            const float d = __fsub_rn(y, __fsub_rn(t, kMagic));   // y - rint(y), in [-0.5, 0.5]
-            near = near || fabsf(d) > 0.5f - 0x1p-14f;
-            word |= (__float_as_uint(t) & 0xffu) << (8 * u);
-        }
-        w[k] = fast_row ? word : 0u;
+        const float2 ya = tcx::fmul2(make_float2(x[k].x, x[k].y), rs2);
+        const float2 yb = tcx::fmul2(make_float2(x[k].z, x[k].w), rs2);
+        const float2 ta = tcx::fadd2(ya, mg2), tb = tcx::fadd2(yb, mg2);
+        const float2 da = tcx::fsub2(ya, tcx::fsub2(ta, mg2)), db = tcx::fsub2(yb, tcx::fsub2(tb, mg2));
+        dmax = fmaxf(dmax, fmaxf(fmaxf(fabsf(da.x), fabsf(da.y)), fmaxf(fabsf(db.x), fabsf(db.y))));
+        const uint32_t lo = __byte_perm(__float_as_uint(ta.x), __float_as_uint(ta.y), 0x5140);
+        const uint32_t hi = __byte_perm(__float_as_uint(tb.x), __float_as_uint(tb.y), 0x5140);
+        w[k] = fast_row ? __byte_perm(lo, hi, 0x5410) : 0u;
     }
+    const bool near = sc > 0.f && (!fast_row || dmax > 0.5f - 0x1p-16f);
     if (__any_sync(0xffffffffu, near) && sc > 0.f) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             w[k] = pack4(__float2int_rn(__fdiv_rn(x[k].x, sc)), __float2int_rn(__fdiv_rn(x[k].y, sc)),
                          __float2int_rn(__fdiv_rn(x[k].z, sc)), __float2int_rn(__fdiv_rn(x[k].w, sc)));
     }
-    // element k * 4 + u of the quarter goes to byte qq * 32 + k * 4 + u of the row, in the same
-    // rotated order as the loads
+    return sc;
+}
+
+// Element k * 4 + u of the quarter goes to byte qq * 32 + k * 4 + u of the row, in the same
+// rotated order as the loads.
+__device__ __forceinline__ void store_codes(const uint32_t (&w)[8], uint8_t *crow, int qq, int rot) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) reinterpret_cast<uint32_t *>(crow)[qq * 8 + ((k + rot) & 7)] = w[k];
-    if (scale_out) *scale_out = sc;
 }
 
 // One row quarter back: 32 codes (read first, rotated order) and the row's scale -> 32 fp32
@@ -312,7 +321,8 @@ __global__ void __launch_bounds__(kQtThreads, 1) q8_tma_kernel(Q8Args a) {
     volatile int *valid = reinterpret_cast<volatile int *>(sm + G::MISC);        // [NS] per source slot
     volatile int *err = reinterpret_cast<volatile int *>(sm + G::MISC + 16);
     volatile int *go = reinterpret_cast<volatile int *>(sm + G::MISC + 20);
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + G::MISC + 32);            // [NS] source loaded (tx)
+    volatile int *dvalid = reinterpret_cast<volatile int *>(sm + G::MISC + 64);  // [ND] per destination slot
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + G::MISC + 128);           // [NS] source loaded (tx)
     uint64_t *sfree = full + NS;                                                 // [NS] source read by compute
     uint64_t *dfull = sfree + NS;                                                // [ND] destination written
     uint64_t *dfree = dfull + ND;                                                // [ND] destination read by its store
@@ -327,125 +337,104 @@ __global__ void __launch_bounds__(kQtThreads, 1) q8_tma_kernel(Q8Args a) {
     }
     __syncthreads();
 
-    if (warp == kQtCompute / 32) {
-        // ------------------------------------------------------------------ producer
-        // Page ids of an item's two lists live in the warp's registers (lane i: ids i and
-        // i + 32); ids from 64 on are read from global memory where needed.
+    if (warp >= kQtCompute / 32) {
+        // ------------------------------------------------------------------ load and store warps
+        // Page ids of an item's list live in the warp's registers (lane i: ids i and i + 32);
+        // ids from 64 on are read from global memory where needed.
+        const bool loader = warp == kQtCompute / 32;
+        const PoolView &v = loader ? sv : dv;
+        const int32_t *pl = loader ? spl : dpl;
         constexpr int kIds = 2;
-        struct Ids { int32_t s[kIds], d[kIds]; };
-        auto lists = [&](int m, const int32_t *&sp, const int32_t *&dp) {
-            const int obj = (blockIdx.x + m * gridDim.x) / a.H;
-            sp = spl + (int64_t)obj * sv.pages_per_object;
-            dp = dpl + (int64_t)obj * dv.pages_per_object;
+        struct Ids { int32_t id[kIds]; };
+        auto list_of = [&](int m) {
+            return pl + (int64_t)((blockIdx.x + m * gridDim.x) / a.H) * v.pages_per_object;
         };
         auto fetch_ids = [&](int m, Ids &x) {
-            const int32_t *sp, *dp;
-            lists(m, sp, dp);
+            const int32_t *l = list_of(m);
 #pragma unroll
             for (int u = 0; u < kIds; ++u) {
                 const int i = lane + 32 * u;
-                x.s[u] = i < sv.pages_per_object ? sp[i] : 0;
-                x.d[u] = i < dv.pages_per_object ? dp[i] : 0;
+                x.id[u] = i < v.pages_per_object ? l[i] : 0;
             }
-        };
-        auto ids_ok = [&](int m, const Ids &x) {
-            bool ok = true;
-#pragma unroll
-            for (int u = 0; u < kIds; ++u)
-                ok = ok && (uint32_t)x.s[u] < (uint32_t)sv.num_pages && (uint32_t)x.d[u] < (uint32_t)dv.num_pages;
-            const int32_t *sp, *dp;
-            lists(m, sp, dp);
-            for (int i = lane + 32 * kIds; i < sv.pages_per_object; i += 32) ok = ok && (uint32_t)sp[i] < (uint32_t)sv.num_pages;
-            for (int i = lane + 32 * kIds; i < dv.pages_per_object; i += 32) ok = ok && (uint32_t)dp[i] < (uint32_t)dv.num_pages;
-            return __all_sync(0xffffffffu, ok);
         };
         // The record of head hh, piece by piece (at most one piece per page it touches): the whole
         // warp walks the pieces, the page id comes from the registers, lane 0 issues the copy.
-        auto pieces = [&](const PoolView &v, const int32_t (&ids)[kIds], const int32_t *list, int hh, uint32_t bytes,
-                          auto &&fn) {
+        auto pieces = [&](const Ids &x, const int32_t *list, int hh, uint32_t bytes, auto &&fn) {
             const uint32_t PB = (uint32_t)v.page_bytes;
             uint32_t off = (uint32_t)(hh * v.rec_bytes), at = 0;
             while (at < bytes) {
                 const uint32_t pi = qt_page_of(v, off), in = off - pi * PB;
                 const uint32_t len = bytes - at < PB - in ? bytes - at : PB - in;
-                int32_t id = __shfl_sync(0xffffffffu, pi < 32 ? ids[0] : ids[1], pi & 31);
+                int32_t id = __shfl_sync(0xffffffffu, pi < 32 ? x.id[0] : x.id[1], pi & 31);
                 if (pi >= 64) id = list[pi];
                 if (lane == 0) fn(v.base + (uint64_t)id * v.page_bytes + in, at, len);
                 off += len;
                 at += len;
             }
         };
-        Ids cur, nxt, prev;
-        int dmask = 0;   // bit b: destination slot b holds a converted record to store
+        Ids cur, nxt;
         int n = 0;
         if (blockIdx.x < total) fetch_ids(0, cur);
         for (;; ++n) {
             const int item = blockIdx.x + n * gridDim.x;
             if (item >= total) break;
-            const int bs = n % NS;
             if (item + (int)gridDim.x < total) fetch_ids(n + 1, nxt);   // overlaps this step
-            const bool ok = ids_ok(n, cur);
-            // load item n once compute has read the item that used its source slot
+            const int32_t *l = list_of(n);
             int stop = 0;
-            if (lane == 0 && (*err || (n >= NS && !ptx::mbar_wait(&sfree[bs], (uint32_t)(((n - NS) / NS) & 1), err))))
-                stop = 1;
-            if (__shfl_sync(0xffffffffu, stop, 0)) break;
-            const int32_t *sp, *dp;
-            lists(n, sp, dp);
-            if (lane == 0) {
-                valid[bs] = ok ? 1 : 0;
-                if (!ok) {
-                    flag_status(a.status, KDA_DEV_BAD_PAGE);
-                    ptx::mbar_arrive(&full[bs]);
-                } else {
-                    ptx::mbar_arrive_expect_tx(&full[bs], G::SB);
-                }
-            }
-            if (ok)
-                pieces(sv, cur.s, sp, item % a.H, G::SB, [&](uint8_t *g, uint32_t at, uint32_t len) {
-                    ptx::bulk_load(sm + bs * G::SB + at, g, len, &full[bs]);
-                });
-            // store item n - 1 once compute has written it; then the destination slot of item
-            // n - 2 is free as soon as that older store has read it out
-            if (n >= 1) {
-                const int m = n - 1, bd = m % ND;
-                if (lane == 0 && !ptx::mbar_wait(&dfull[bd], (uint32_t)((m / ND) & 1), err)) stop = 1;
+            if (loader) {
+                // every page id of both lists in range, or the item is skipped and flagged
+                const int32_t *dl = dpl + (int64_t)(item / a.H) * dv.pages_per_object;
+                bool ok = true;
+#pragma unroll
+                for (int u = 0; u < kIds; ++u) ok = ok && (uint32_t)cur.id[u] < (uint32_t)sv.num_pages;
+                for (int i = lane + 32 * kIds; i < sv.pages_per_object; i += 32) ok = ok && (uint32_t)l[i] < (uint32_t)sv.num_pages;
+                for (int i = lane; i < dv.pages_per_object; i += 32) ok = ok && (uint32_t)dl[i] < (uint32_t)dv.num_pages;
+                ok = __all_sync(0xffffffffu, ok);
+                // load item n once compute has taken the item that used its source slot
+                const int bs = n % NS;
+                if (lane == 0 && (*err || (n >= NS && !ptx::mbar_wait(&sfree[bs], (uint32_t)(((n - NS) / NS) & 1), err))))
+                    stop = 1;
                 if (__shfl_sync(0xffffffffu, stop, 0)) break;
-                const int32_t *psp, *pdp;
-                lists(m, psp, pdp);
-                if ((dmask >> bd) & 1)
-                    pieces(dv, prev.d, pdp, (blockIdx.x + m * gridDim.x) % a.H, G::DB, [&](uint8_t *g, uint32_t at, uint32_t len) {
+                if (lane == 0) {
+                    valid[bs] = ok ? 1 : 0;
+                    if (!ok) {
+                        flag_status(a.status, KDA_DEV_BAD_PAGE);
+                        ptx::mbar_arrive(&full[bs]);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(&full[bs], G::SB);
+                    }
+                }
+                if (ok)
+                    pieces(cur, l, item % a.H, G::SB, [&](uint8_t *g, uint32_t at, uint32_t len) {
+                        ptx::bulk_load(sm + bs * G::SB + at, g, len, &full[bs]);
+                    });
+            } else {
+                // store item n once compute has written it; its slot is free when read out
+                const int bd = n % ND;
+                if (lane == 0 && !ptx::mbar_wait(&dfull[bd], (uint32_t)((n / ND) & 1), err)) stop = 1;
+                if (__shfl_sync(0xffffffffu, stop, 0)) break;
+                if (dvalid[bd])
+                    pieces(cur, l, item % a.H, G::DB, [&](uint8_t *g, uint32_t at, uint32_t len) {
                         ptx::bulk_store(g, sm + G::DST0 + bd * G::DB + at, len);
                     });
                 if (lane == 0) {
                     ptx::bulk_commit();
-                    ptx::bulk_wait_read1();
-                    if (m >= 1) ptx::mbar_arrive(&dfree[(m - 1) % ND]);
+                    if constexpr (ND == 1) {
+                        ptx::bulk_wait_read0();
+                        ptx::mbar_arrive(&dfree[bd]);
+                    } else {
+                        // up to two stores in flight: the older one has read its slot out
+                        ptx::bulk_wait_read1();
+                        if (n >= 1) ptx::mbar_arrive(&dfree[(n - 1) % ND]);
+                    }
                 }
             }
             __syncwarp();
-            dmask = ok ? (dmask | (1 << (n % ND))) : (dmask & ~(1 << (n % ND)));
-            prev = cur;
             cur = nxt;
-        }
-        if (!*err && n >= 1) {
-            // the last item goes out
-            const int m = n - 1, bd = m % ND;
-            int stop = 0;
-            if (lane == 0 && !ptx::mbar_wait(&dfull[bd], (uint32_t)((m / ND) & 1), err)) stop = 1;
-            if (!__shfl_sync(0xffffffffu, stop, 0)) {
-                const int32_t *psp, *pdp;
-                lists(m, psp, pdp);
-                if ((dmask >> bd) & 1)
-                    pieces(dv, prev.d, pdp, (blockIdx.x + m * gridDim.x) % a.H, G::DB, [&](uint8_t *g, uint32_t at, uint32_t len) {
-                        ptx::bulk_store(g, sm + G::DST0 + bd * G::DB + at, len);
-                    });
-                if (lane == 0) ptx::bulk_commit();
-            }
         }
         if (lane == 0) {
             ptx::bulk_wait0();
-            if (*err) {
+            if (loader && *err) {
                 // leave no load in flight
                 for (int m = n - NS < 0 ? 0 : n - NS; m < n; ++m) {
                     uint32_t k = 0;
@@ -464,8 +453,7 @@ __global__ void __launch_bounds__(kQtThreads, 1) q8_tma_kernel(Q8Args a) {
             if (item >= total) break;
             const int bs = n % NS, bd = n % ND;
             if (tid == 0) {
-                bool okw = ptx::mbar_wait(&full[bs], (uint32_t)((n / NS) & 1), err);
-                if (okw && n >= ND) okw = ptx::mbar_wait(&dfree[bd], (uint32_t)(((n - ND) / ND) & 1), err);
+                const bool okw = ptx::mbar_wait(&full[bs], (uint32_t)((n / NS) & 1), err);
                 *go = (okw && !*err) ? 1 : 0;
             }
             tcx::named_bar(1, kQtCompute);
@@ -490,10 +478,20 @@ __global__ void __launch_bounds__(kQtThreads, 1) q8_tma_kernel(Q8Args a) {
                 }
             }
             tcx::named_bar(1, kQtCompute);
-            if (tid == 0) ptx::mbar_arrive(&sfree[bs]);
+            if (tid == 0) {
+                ptx::mbar_arrive(&sfree[bs]);
+                // the destination slot is free once the store of item n - ND has read it out
+                const bool okw = n < ND || ptx::mbar_wait(&dfree[bd], (uint32_t)(((n - ND) / ND) & 1), err);
+                *go = okw ? 1 : 0;
+            }
             if (vld) {
+                // codes in registers first; the destination is written once its slot is free
+                uint32_t w[8];
+                if (QUANT) sc = quant_quarter(x, w);
+                tcx::named_bar(1, kQtCompute);
+                if (!*go) break;
                 if (QUANT) {
-                    quant_quarter(x, dst + 4 * D + r * D, qq, rot, qq == 0 ? &sc : nullptr);
+                    store_codes(w, dst + 4 * D + r * D, qq, rot);
                     if (qq == 0) reinterpret_cast<float *>(dst)[r] = sc;
                     if (tid < WBYTES / 16) reinterpret_cast<uint4 *>(dst + WQ)[tid] = win;
                 } else {
@@ -503,7 +501,10 @@ __global__ void __launch_bounds__(kQtThreads, 1) q8_tma_kernel(Q8Args a) {
                 ptx::fence_proxy_async_smem();
             }
             tcx::named_bar(1, kQtCompute);
-            if (tid == 0) ptx::mbar_arrive(&dfull[bd]);
+            if (tid == 0) {
+                dvalid[bd] = vld ? 1 : 0;
+                ptx::mbar_arrive(&dfull[bd]);
+            }
         }
     }
     __syncthreads();

@@ -155,9 +155,10 @@ def test_int8_restore_refuses_pages_outside_the_pool():
 
 
 def test_write_q8_near_rounding_ties_bit_for_bit():
-    """Rows built so that S[i][j] / scale_i lies exactly on, or one or two fp32 steps beside, a
-    half-integer, over scales from 1e-30 to 1e30: the quantiser's fast reciprocal path must take
-    the same integer decisions as the IEEE division of the oracle codec on every element."""
+    """Rows built so that S[i][j] / scale_i lies exactly on, or up to six fp32 steps beside, a
+    half-integer, over scales from 1e-30 to 1e30 (the steps straddle the quantiser's 2^-16
+    rounding-test band): its fast reciprocal path must take the same integer decisions as the
+    IEEE division of the oracle codec on every element."""
     dtype, d, H, page_bytes = "bf16", 128, 4, 65536
     dt = kda.DTYPES[dtype]
     P = policy.object_pages(H, d, dtype, page_bytes)
@@ -175,8 +176,8 @@ def test_write_q8_near_rounding_ties_bit_for_bit():
             row[0] = amax
             k = rng.integers(-126, 126, d - 1).astype(f32)
             base = ((k + f32(0.5)) * scale).astype(f32)
-            steps = np.arange(d - 1) % 5 - 2                   # -2 .. 2 fp32 steps away
-            for u in range(1, 3):
+            steps = np.arange(d - 1) % 13 - 6                  # -6 .. 6 fp32 steps away
+            for u in range(1, 7):
                 base = np.where(steps >= u, np.nextafter(base, f32(np.inf)), base)
                 base = np.where(steps <= -u, np.nextafter(base, f32(-np.inf)), base)
             row[1:] = np.clip(base, -amax, amax)
