@@ -127,36 +127,45 @@ __global__ void __launch_bounds__(kSimtThreads, 1) prefill_simt_kernel(PrefillAr
         const int r_end = end - abs0 < C ? (int)(end - abs0) : C;
         const int64_t row0 = (int64_t)m.tok_begin + (abs0 - start);   // packed row of chunk row 0
 
-        // 1. conv over the q | k | v channels, each thread walking its channels down the chunk.
-        for (int ch = tid; ch < C3; ch += kSimtThreads) {
-            const int which = ch / D, cc = ch % D;
+        // 1. The chunk's raw rows into the tiles in one coalesced pass (rows outside the
+        //    sequence read as zeros, their alpha as one), then the conv in place, each thread
+        //    walking a channel down the chunk with the last three raw values in registers, and
+        //    the cumulative decay in place over the alpha tile.
+        for (int e = tid; e < C * C3; e += kSimtThreads) {
+            const int r = e / C3, ch = e % C3, which = ch / D, cc = ch % D;
             const T *src = which == 0 ? qg : (which == 1 ? kg : vg);
-            const float4 w = *reinterpret_cast<const float4 *>(a.conv_w + ((int64_t)h * C3 + ch) * 4);
-            float p0 = halo[ch], p1 = halo[C3 + ch], p2 = halo[2 * C3 + ch];
             float *dst = which == 0 ? qs : (which == 1 ? ks : vs);
             const int ld = which == 2 ? D : LD;
-            for (int r = 0; r < C; ++r) {
-                float y = 0.f;
-                if (r >= r_first && r < r_end) {
-                    const float x = ld_elem(src + ((row0 + r) * H + h) * D + cc);
-                    y = w.x * p0 + w.y * p1 + w.z * p2 + w.w * x;
+            dst[r * ld + cc] = (r >= r_first && r < r_end) ? ld_elem(src + ((row0 + r) * H + h) * D + cc) : 0.f;
+        }
+        for (int e = tid; e < C * D; e += kSimtThreads) {
+            const int r = e / D, i = e % D;
+            gs[r * D + i] = (r >= r_first && r < r_end) ? ld_elem(ag + ((row0 + r) * H + h) * D + i) : 1.f;
+        }
+        if (tid < C) bs[tid] = (tid >= r_first && tid < r_end) ? ld_elem(bg + (row0 + tid) * H + h) : 0.f;
+        __syncthreads();
+        for (int col = tid; col < C3 + D; col += kSimtThreads) {
+            if (col < C3) {
+                const int ch = col, which = ch / D, cc = ch % D;
+                const float4 w = *reinterpret_cast<const float4 *>(a.conv_w + ((int64_t)h * C3 + ch) * 4);
+                float p0 = halo[ch], p1 = halo[C3 + ch], p2 = halo[2 * C3 + ch];
+                float *dst = which == 0 ? qs : (which == 1 ? ks : vs);
+                const int ld = which == 2 ? D : LD;
+                for (int r = r_first; r < r_end; ++r) {
+                    const float x = dst[r * ld + cc];
+                    dst[r * ld + cc] = w.x * p0 + w.y * p1 + w.z * p2 + w.w * x;
                     p0 = p1; p1 = p2; p2 = x;
                 }
-                dst[r * ld + cc] = y;
+                halo[ch] = p0; halo[C3 + ch] = p1; halo[2 * C3 + ch] = p2;
+            } else {
+                const int i = col - C3;
+                float g = 1.f;
+                for (int r = 0; r < C; ++r) {
+                    g *= gs[r * D + i];
+                    gs[r * D + i] = g;
+                }
+                gC[i] = g;
             }
-            halo[ch] = p0; halo[C3 + ch] = p1; halo[2 * C3 + ch] = p2;
-        }
-        // 2. cumulative decay per key channel, and beta.
-        if (tid < D) {
-            float g = 1.f;
-            for (int r = 0; r < C; ++r) {
-                if (r >= r_first && r < r_end) g *= ld_elem(ag + ((row0 + r) * H + h) * D + tid);
-                gs[r * D + tid] = g;
-            }
-            gC[tid] = g;
-        } else if (tid < D + C) {
-            const int r = tid - D;
-            bs[r] = (r >= r_first && r < r_end) ? ld_elem(bg + (row0 + r) * H + h) : 0.f;
         }
         __syncthreads();
         // 3. decay-scaled copies.
@@ -233,15 +242,40 @@ __global__ void __launch_bounds__(kSimtThreads, 1) prefill_simt_kernel(PrefillAr
             }
             __syncthreads();
         }
-        // 7. forward substitution (I + A) W = R, one column per thread, in place.
-        if (part == 0) {
-            for (int r = 1; r < C; ++r) {
-                float w = vs[r * D + j];
-                for (int s = 0; s < r; ++s) w = fmaf(-As[r * CP + s], vs[s * D + j], w);
-                vs[r * D + j] = w;
+        // 7. forward substitution (I + A) W = R, in place, in blocks of RB rows: a block's rows
+        //    first take the terms of all earlier rows (split over the NI parts, summed through
+        //    `red`), then part 0 solves within the block, one column per thread.
+        for (int rb = 0; rb < C; rb += RB) {
+            if (rb > 0) {
+                float pr[RB];
+#pragma unroll
+                for (int x = 0; x < RB; ++x) pr[x] = 0.f;
+                for (int s2 = part; s2 < rb; s2 += NI) {
+                    const float w = vs[s2 * D + j];
+#pragma unroll
+                    for (int x = 0; x < RB; ++x) pr[x] = fmaf(As[(rb + x) * CP + s2], w, pr[x]);
+                }
+#pragma unroll
+                for (int x = 0; x < RB; ++x) red[(part * RB + x) * D + j] = pr[x];
+                __syncthreads();
+                for (int e = tid; e < RB * D; e += kSimtThreads) {
+                    const int x = e / D, jj = e % D;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int pp = 0; pp < NI; ++pp) acc += red[(pp * RB + x) * D + jj];
+                    vs[(rb + x) * D + jj] -= acc;
+                }
+                __syncthreads();
             }
+            if (part == 0) {
+                for (int r = rb + 1; r < rb + RB; ++r) {
+                    float w = vs[r * D + j];
+                    for (int s2 = rb; s2 < r; ++s2) w = fmaf(-As[r * CP + s2], vs[s2 * D + j], w);
+                    vs[r * D + j] = w;
+                }
+            }
+            __syncthreads();
         }
-        __syncthreads();
         // 8. Y = Qt S into gs, 16 rows at a time.
         for (int rb = 0; rb < C; rb += RB) {
             float pr[RB];

@@ -9,6 +9,7 @@ python -m kda_state_chunked_gb300.profile_case prefill-long-slice --launches 1
 Cases
   prefill-batched     4 x 8192 tokens, H = 16, d = 128, bf16, checkpoints every 2048
   prefill-long-slice  one 65536-token slice of the long workload (H = 32), same layout
+  prefill-tiny        the tiny fp32 workload: 1 x 1024 tokens, H = 2, d = 64 (CUDA-core kernel)
   decode              256 requests x 32 heads, 256 KiB pages, permuted page table
   ckpt-restore        256 objects x 32 heads copied checkpoint -> private, 64 KiB pages
   ckpt-write-q8       the same objects quantised into INT8 checkpoints
@@ -38,6 +39,27 @@ def prefill(T_seq, nseq, H, seed, launches, dev):
         seq, pos, pages = kda.kda_ckpt_plan(pool, H, d, dt, cu, [0] * nseq, 512, 4, True)
         ws = kda.prefill_workspace(toks["q"], cu, [0] * nseq, len(seq), P)
         kda.kda_prefill_varlen(pool, cu, [0] * nseq, [0] * nseq, toks["q"], toks["k"], toks["v"],
+                               toks["alpha"], toks["beta"], toks["conv_w"], o, act, seq, pos, pages, ws, st)
+        torch.cuda.synchronize()
+        kda.kda_page_decref(pool, pages.reshape(-1))
+    assert kda.kda_sync_status(st)[0] == kda.KDA_OK
+
+
+def prefill_tiny(launches, dev):
+    """The tiny fp32 workload: 1 sequence x 1024 tokens, H = 2, d = 64, checkpoints every 512."""
+    w = workloads.WORKLOADS["tiny"]
+    dt = kda.DTYPES[w.dtype]
+    toks = workloads.make_tokens(w.nseq * w.T, w.H, w.d, w.dtype, w.seed, dev)
+    pool = kda.Pool(w.page_bytes, 256, dev)
+    P = pool.object_pages(w.H, w.d, dt)
+    act = kda.kda_page_alloc(pool, w.nseq * P).reshape(w.nseq, P)
+    cu = [i * w.T for i in range(w.nseq + 1)]
+    o = torch.empty_like(toks["q"])
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(launches):
+        seq, pos, pages = kda.kda_ckpt_plan(pool, w.H, w.d, dt, cu, [0] * w.nseq, 512, w.stride, w.include_last)
+        ws = kda.prefill_workspace(toks["q"], cu, [0] * w.nseq, len(seq), P)
+        kda.kda_prefill_varlen(pool, cu, [0] * w.nseq, [0] * w.nseq, toks["q"], toks["k"], toks["v"],
                                toks["alpha"], toks["beta"], toks["conv_w"], o, act, seq, pos, pages, ws, st)
         torch.cuda.synchronize()
         kda.kda_page_decref(pool, pages.reshape(-1))
@@ -125,7 +147,7 @@ def ckpt_q8(launches, dev, n=256, restore=False):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill-batched", "prefill-long-slice", "decode", "ckpt-restore",
+    ap.add_argument("case", choices=["prefill-batched", "prefill-long-slice", "prefill-tiny", "decode", "ckpt-restore",
                                      "ckpt-write-q8", "ckpt-restore-q8", "verify"])
     ap.add_argument("--launches", type=int, default=2)
     a = ap.parse_args()
@@ -136,6 +158,8 @@ def main():
         prefill(8192, 4, 16, 1, a.launches, dev)
     elif a.case == "prefill-long-slice":
         prefill(65536, 1, 32, 4, a.launches, dev)
+    elif a.case == "prefill-tiny":
+        prefill_tiny(a.launches, dev)
     elif a.case == "decode":
         decode(a.launches, dev)
     elif a.case == "ckpt-write-q8":
