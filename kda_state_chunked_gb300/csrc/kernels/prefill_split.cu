@@ -13,7 +13,8 @@
 //   chunk_prep_kernel (one CTA per (item, head), 160 threads, three CTAs per SM)
 //     conv, decay factors, Kt' = k gamma_r/gamma_C, Qt' = q gamma_r/gamma_C, Kb = k gamma_C/gamma_r,
 //     G | P = [Kt'; Qt'] Kb^T (tcgen05), T = (I + Diag(beta) strict_lower(G))^{-1} Diag(beta)
-//     (CUDA cores + tf32 mma.sync), WK'^T = Kt'^T T^T (tcgen05), and writes one operand image
+//     (16 x 16 diagonal inverses on CUDA cores, the rest in three tcgen05 rounds),
+//     WK'^T = Kt'^T T^T (tcgen05), and writes one operand image
 //     per item, bf16 and 128-byte swizzled as the chain kernel's MMAs read it:
 //     Gamma_C [-WK' | Qt'] = [-WK' Gamma_C | q gamma_r], Kb, P, V, T, and gamma_C (fp32).  Conv
 //     windows of checkpoints are written here.
@@ -71,11 +72,11 @@ __device__ __forceinline__ uint8_t *image_addr(const SplitArgs &a, int wave, int
 // ============================================================================ chunk prep
 constexpr int kAThreads = 160;   // warps 0-3 compute, warp 4 TMA + MMA + bulk stores
 
-// Shared memory (73 KiB: three CTAs per SM).  P^T is staged over the V tile.
+// Shared memory (73 KiB: three CTAs per SM).
 constexpr uint32_t A_KQ = 0;        // [2 kb][128 rows: k 0-63 | q 64-127][128 B] -> Kt' | Qt'
-constexpr uint32_t A_T = 8192;      // T [64][128 B], over the first Qt' half once that is stored
-constexpr uint32_t A_V = 32768;     // [2 kb][64][128 B]  raw v -> V
-constexpr uint32_t A_AL = 49152;    // [2 kb][64][128 B]  raw alpha -> Kb -> fp32 solve scratch -> WK'^T
+constexpr uint32_t A_T = 8192;      // T [64][128 B], over the first Qt' half once M1 has read it
+constexpr uint32_t A_V = 32768;     // [2 kb][64][128 B]  raw v (V goes to the image) -> solve tiles
+constexpr uint32_t A_AL = 49152;    // [2 kb][64][128 B]  raw alpha -> Kb -> fp32 solve scratch
 constexpr uint32_t A_DG = 65536;    // float [64][16]     partial sums of the diagonal q.k
 constexpr uint32_t A_GC = 69632;    // float [128]  gamma_C
 constexpr uint32_t A_BS = 70144;    // float [64]   beta
@@ -88,9 +89,9 @@ constexpr uint32_t A_SMEM = A_BAR + 128 + 1024;
 static_assert(3 * (A_SMEM + 1024) <= 228 * 1024, "three chunk-prep CTAs per SM");
 constexpr int kAWg = 1, kAHalf = 2;   // named barriers (128 and 64 threads)
 
-enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_QVF, AB_PT, AB_T, AB_M2, AB_WK, AB_SO, A_NBARS };
+enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_T, AB_M2, AB_SO, A_NBARS };
 // bf16 64 x 64 tiles of the tensor-core solve (8 KiB each, row-major, 128-byte swizzle): Binv over
-// the second Qt' half and N over the second V half (both read out by then), E over the first
+// the second Qt' half (read by M1 by then) and N over the second raw v half, E over the first
 // Qt' half; E^2 then takes N's place and G E's place, and T finally G's (A_T).  Round 2 reads
 // [E | Binv] as one N = 128 operand: Binv lies A_SB - A_SE bytes after E.
 constexpr uint32_t A_SB = A_KQ + 16384 + 8192, A_SN = A_V + 8192, A_SE = A_T, A_SE2 = A_SN, A_SG = A_SE;
@@ -215,21 +216,13 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 }
                 ptx::mma_commit(&S.bar[AB_GP]);
                 m1 = true;
-                // Kb, Qt' and V to the image, Kb in a group of its own: its tile becomes the solve
-                // scratch once M1 and this copy have read it (KBF); the Qt' and V tiles are
-                // reused later, for T and P^T (QVF)
+                // Kb to the image: its tile becomes the solve scratch once M1 and this copy have
+                // read it (KBF).  (V, q gamma_r and P^T go to the image from the compute
+                // warps' registers.)
                 ptx::bulk_store(img + IMG_PK + 8192, sm + A_AL, 16384);
                 ptx::bulk_commit();
-                ptx::bulk_store(img + IMG_V, sm + A_V, 16384);
-                ptx::bulk_commit();
-                ptx::bulk_wait_read1();
-                if (wait_bar(S, AB_GP, 0)) ptx::mbar_arrive(&S.bar[AB_KBF]);
                 ptx::bulk_wait_read0();
-                ptx::mbar_arrive(&S.bar[AB_QVF]);
-            }
-            if (!*S.err && wait_bar(S, AB_PT, 0)) {
-                ptx::bulk_store(img + IMG_PK, sm + A_V, 8192);
-                ptx::bulk_commit();
+                if (wait_bar(S, AB_GP, 0)) ptx::mbar_arrive(&S.bar[AB_KBF]);
             }
             if (!*S.err && wait_bar(S, AB_T, 0)) {
                 // M2: WK'^T = Kt'^T T^T (the chain forms U^T = V^T T^T itself, from V and T)
@@ -245,12 +238,9 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 ptx::bulk_store(img + IMG_T, sm + A_T, 8192);
                 ptx::bulk_commit();
             }
-            if (!*S.err && wait_bar(S, AB_WK, 0)) {
-                ptx::bulk_store(img + IMG_WQ, sm + A_AL, 8192);
-                ptx::bulk_store(img + IMG_WQ + 16384, sm + A_AL + 8192, 8192);
-                ptx::bulk_commit();
-            }
-            ptx::bulk_wait0();
+            // the image stores need only have read their shared memory before the CTA exits:
+            // the grid's completion, which the chains wait for, covers their global writes
+            ptx::bulk_wait_read0();
             if (*S.err) {
                 // leave nothing in flight: the tile loads and any issued MMA
                 uint32_t n = 0;
@@ -373,7 +363,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 *reinterpret_cast<uint32_t *>(img + IMG_WQ + kb * 16384 + 8192 + off) = oqg;
                 *reinterpret_cast<uint32_t *>(krow + off) = ok;
                 *reinterpret_cast<uint32_t *>(arow + off) = okb;
-                *reinterpret_cast<uint32_t *>(vrow + off) = ov;
+                *reinterpret_cast<uint32_t *>(img + IMG_V + kb * 8192 + off) = ov;   // V: image only
             };
             if (r_first == 0 && r_end == C) {
 #pragma unroll 1
@@ -472,13 +462,12 @@ __global__ void __launch_bounds__(kAThreads, 3)
                         row[c4 ^ (r & 7)] = make_float4(ev[0], ev[1], ev[2], ev[3]);
                     }
                 } else {
-                    // P^T staged MN-major over the V tile (free once its bulk copy has read it):
-                    // row j holds P[0..63][j]; thread r writes column r.  (A timeout of this
-                    // warp-level wait is recorded; the warps carry on together to the barriers.)
-                    (void)warp_wait(S, AB_QVF, 0);
+                    // P^T straight from the registers into the image, MN-major and swizzled as
+                    // the chain reads it: row j holds P[0..63][j]; thread r writes column r
+                    // (a warp's store fills whole 32-byte sectors of one row)
                     const int r = t - C;
                     const float pdr = pd[r];
-                    uint8_t *const pt = sm + A_V;
+                    uint8_t *const pt = img + IMG_PK;
 #pragma unroll
                     for (int s0 = 0; s0 < 64; ++s0) {
                         const float gv = s0 < 32 ? g0[s0 & 31] : g1[s0 & 31];
@@ -490,7 +479,6 @@ __global__ void __launch_bounds__(kAThreads, 3)
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             named_bar(kAWg, 128);
-            if (t == 0) ptx::mbar_arrive(&S.bar[AB_PT]);
             // Each round: the compute warps write its operands, meet at a barrier, and thread 0
             // issues the round's MMAs and its commit; the round's completion is polled by
             // thread 0 and handed to the warpgroup through a flag word of its own (one barrier).
@@ -575,7 +563,8 @@ __global__ void __launch_bounds__(kAThreads, 3)
                     *reinterpret_cast<uint4 *>(sm + A_SB + ptx::sw128_off(r, ch * 16)) = pk;
                 }
             } else {
-                // meanwhile: N, the strictly block-lower part of A (untouched by level 0), as bf16
+                // meanwhile: N, the strictly block-lower part of A (untouched by level 0), as bf16,
+                // over the second half of the raw v tile
                 const int r = t - C, rb = r >> 4;
                 const float4 *row = reinterpret_cast<const float4 *>(Msc + r * 64);
 #pragma unroll
@@ -670,7 +659,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
             ptx::tc_fence_before();
             named_bar(kAWg, 128);
             if (t == 0) ptx::mbar_arrive(&S.bar[AB_T]);
-            // ---------------- -WK' (K-major bf16 operand rows, staged for bulk copies) and gamma_C
+            // ---------------- -WK' Gamma_C (K-major bf16 operand rows) and gamma_C, straight into the image
             if (!wg_wait(S, AB_M2, 0, t, kAWg, wflag)) break;
             ptx::tc_fence_after();
             {
@@ -680,7 +669,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 ptx::tmem_wait_ld();
                 // thread t holds column t (key t) of WK'; row c of the K-major tile of key block
                 // t / 64 gets it at position t % 64, negated (the chain accumulates -(Gamma S)^T WK'^T)
-                uint8_t *const wk = sm + A_AL + (t >> 6) * 8192;
+                uint8_t *const wk = img + IMG_WQ + (t >> 6) * 16384;
                 const uint32_t cb2 = (uint32_t)(t & 63) * 2;
                 const float gt = gC[t];
 #pragma unroll
@@ -690,10 +679,6 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 }
                 reinterpret_cast<float *>(img + IMG_GC)[t] = gC[t];
             }
-            ptx::fence_proxy_async_smem();
-            ptx::tc_fence_before();
-            named_bar(kAWg, 128);
-            if (t == 0) ptx::mbar_arrive(&S.bar[AB_WK]);
         } while (false);
         // on a timeout, leave no solve MMA in flight: its commit tracks every MMA before it
         if (t == 0 && *S.err && solve_rounds > 0) {
