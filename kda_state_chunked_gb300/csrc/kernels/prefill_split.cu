@@ -90,11 +90,15 @@ static_assert(3 * (A_SMEM + 1024) <= 228 * 1024, "three chunk-prep CTAs per SM")
 constexpr int kAWg = 1, kAHalf = 2;   // named barriers (128 and 64 threads)
 
 enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_T, AB_M2, AB_SO, A_NBARS };
-// bf16 64 x 64 tiles of the tensor-core solve (8 KiB each, row-major, 128-byte swizzle): Binv over
-// the second Qt' half (read by M1 by then) and N over the second raw v half, E over the first
-// Qt' half; E^2 then takes N's place and G E's place, and T finally G's (A_T).  Round 2 reads
-// [E | Binv] as one N = 128 operand: Binv lies A_SB - A_SE bytes after E.
-constexpr uint32_t A_SB = A_KQ + 16384 + 8192, A_SN = A_V + 8192, A_SE = A_T, A_SE2 = A_SN, A_SG = A_SE;
+// bf16 64 x 64 tiles of the tensor-core solve (8 KiB each, row-major, 128-byte swizzle).  The A
+// operand of an M = 128 product reads its rows 64-127 8 KiB after rows 0-63, and each A tile has
+// a copy there, so TMEM lanes 64-127 hold the product's rows 0-63 once more and all four compute
+// warps share an epilogue, each thread half a row.  Binv over the second Qt' half (read by M1),
+// its copy over the first raw v half; N over the second raw v half; E, then E^2, over the raw v
+// tile with its copy in the second half (each once the previous round has read that tile); G
+// over Binv once round 2 has read it; T at A_T.
+constexpr uint32_t A_SB = A_KQ + 16384 + 8192, A_SN = A_V + 8192, A_SE = A_V, A_SE2 = A_V, A_SG = A_SB;
+static_assert(A_SB + 8192 == A_V && A_SE + 8192 == A_SN, "solve tiles and their row copies");
 constexpr uint32_t A_ERR = 96;   // error flag, TMEM address and wait flag after the mbarriers
 static_assert(A_NBARS * 8 <= A_ERR && A_ERR + 24 <= 128, "prep barrier block");
 
@@ -490,17 +494,24 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 if (t == 0) {
                     ptx::tc_fence_after();
                     const uint32_t sbase = ptx::smem_u32(sm);
-                    const uint32_t a_t = rd == 0 ? A_SB : (rd == 1 ? A_SE : A_SE2);
-                    const uint32_t b_t = rd == 0 ? A_SN : (rd == 1 ? A_SE : A_SG);
-                    const uint32_t idr = ptx::idesc_bf16(128, rd == 1 ? 128 : 64, 0, 1);
-                    // K-steps (16-row blocks of the shared dimension) whose products are all zero
-                    // are skipped: N has no entries in its first row block, E none in its last
-                    // column block, E^2 none in its last two
-                    const int s0 = rd == 0 ? 1 : 0, s1 = rd == 2 ? 2 : (rd == 1 ? 3 : 4);
-                    for (int s = s0; s < s1; ++s)
-                        ptx::mma_bf16(tbase, ptx::sdesc_sw128(sbase + a_t + s * 32, 16, 1024),
-                                      ptx::sdesc_sw128(sbase + b_t + s * 2048, A_SB - A_SE, 1024), idr,
-                                      s > s0 ? 1u : 0u);
+                    const uint32_t id64 = ptx::idesc_bf16(128, 64, 0, 1);
+                    // one N = 64 product into TMEM columns d_col..+63; K-steps (16-row blocks of
+                    // the shared dimension) whose products are all zero are skipped: N and E have
+                    // no entries in their first row block, E none in its last column block, E^2
+                    // none in its last two
+                    auto product = [&](uint32_t d_col, uint32_t a_t, uint32_t b_t, int s0, int s1) {
+                        for (int s = s0; s < s1; ++s)
+                            ptx::mma_bf16(tbase + d_col, ptx::sdesc_sw128(sbase + a_t + s * 32, 16, 1024),
+                                          ptx::sdesc_sw128(sbase + b_t + s * 2048, 8192, 1024), id64, s > s0 ? 1u : 0u);
+                    };
+                    if (rd == 0) {
+                        product(0, A_SB, A_SN, 1, 4);        // E = Binv N
+                    } else if (rd == 1) {
+                        product(0, A_SE, A_SE, 1, 3);        // E^2
+                        product(64, A_SE, A_SB, 0, 3);       // E Binv
+                    } else {
+                        product(0, A_SE2, A_SG, 0, 2);       // E^2 G
+                    }
                     ptx::mma_commit(&S.bar[AB_SO]);
                 }
                 solve_rounds = rd + 1;
@@ -561,6 +572,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
                         pk.w = pack_bf16x2(xs[6], xs[7]);
                     }
                     *reinterpret_cast<uint4 *>(sm + A_SB + ptx::sw128_off(r, ch * 16)) = pk;
+                    *reinterpret_cast<uint4 *>(sm + A_SB + 8192 + ptx::sw128_off(r, ch * 16)) = pk;   // rows 64-127
                 }
             } else {
                 // meanwhile: N, the strictly block-lower part of A (untouched by level 0), as bf16,
@@ -583,77 +595,73 @@ __global__ void __launch_bounds__(kAThreads, 3)
             // Off-diagonal part on the tensor cores: with Binv = the block-diagonal inverse and N
             // the strictly block-lower part of A, L = I + A has L^{-1} = (I - E)(I + E^2) Binv =
             // G + E^2 G, E = Binv N, G = Binv - E Binv (E^4 = 0).  Three bf16 MMA rounds with
-            // fp32 accumulation: E = Binv N; [E^2 | E Binv] = E [E | Binv]; E^2 G (8 MMAs: the
-            // block structure leaves some 16-deep steps of each product zero).  Every
-            // operand is a 64 x 64 bf16 tile, row-major and 128-byte swizzled, which serves as a
-            // K-major A and as an MN-major B alike.  Rows 0-63 of each M = 128 product are used.
+            // fp32 accumulation: E = Binv N; E^2 and E Binv; E^2 G (10 MMAs: the block structure
+            // leaves some 16-deep steps of each product zero).  Every operand is a 64 x 64 bf16
+            // tile, row-major and 128-byte swizzled, which serves as a K-major A and as an
+            // MN-major B alike.  Thread t takes row t % 64 and column half t / 64 of each
+            // product, from the TMEM lanes of its warp (lanes 64-127 repeat rows 0-63).
+            const int sr = t & 63, shf = t >> 6;
             solve_issue(0);
-            // round 1 done: E -> bf16 tile (rows 0-63 of the product, lanes of warps 0 and 1)
+            // round 1 done: E -> bf16 tile and its row copy
             if (!solve_wait(0)) break;
             ptx::tc_fence_after();
-            if (t < C) {
-                float e0[32], e1[32];
-                ptx::tmem_ld32(tbase + lanes, e0);
-                ptx::tmem_ld32(tbase + lanes + 32, e1);
+            {
+                float e[32];
+                ptx::tmem_ld32(tbase + lanes + shf * 32, e);
                 ptx::tmem_wait_ld();
-                put_row_bf16(A_SE, t, 0, e0);
-                put_row_bf16(A_SE, t, 4, e1);
+                put_row_bf16(A_SE, sr, shf * 4, e);
+                put_row_bf16(A_SE + 8192, sr, shf * 4, e);
             }
             solve_issue(1);
-            // round 2 done: E^2 -> bf16 tile; G = Binv - E Binv -> bf16 tile and fp32 row of Msc
+            // round 2 done: E^2 -> bf16 tile and copy; G = Binv - E Binv -> bf16 tile and fp32 row of Msc
             if (!solve_wait(1)) break;
             ptx::tc_fence_after();
-            if (t < C) {
-                const int r = t, rb = r >> 4;
+            {
+                const int r = sr, rb = r >> 4;
                 float4 *row = reinterpret_cast<float4 *>(Msc + r * 64);
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    float e2[32], eb[32];
-                    ptx::tmem_ld32(tbase + lanes + hh * 32, e2);
-                    ptx::tmem_ld32(tbase + lanes + 64 + hh * 32, eb);
-                    ptx::tmem_wait_ld();
+                float e2[32], eb[32];
+                ptx::tmem_ld32(tbase + lanes + shf * 32, e2);
+                ptx::tmem_ld32(tbase + lanes + 64 + shf * 32, eb);
+                ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const int cc = hh * 8 + c4;
-                        float4 g4 = make_float4(-eb[c4 * 4], -eb[c4 * 4 + 1], -eb[c4 * 4 + 2], -eb[c4 * 4 + 3]);
-                        if ((cc >> 2) == rb) {
-                            const float4 b4 = row[cc ^ (r & 7)];
-                            g4.x += b4.x; g4.y += b4.y; g4.z += b4.z; g4.w += b4.w;
-                        }
-                        eb[c4 * 4] = g4.x; eb[c4 * 4 + 1] = g4.y; eb[c4 * 4 + 2] = g4.z; eb[c4 * 4 + 3] = g4.w;
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const int cc = shf * 8 + c4;
+                    float4 g4 = make_float4(-eb[c4 * 4], -eb[c4 * 4 + 1], -eb[c4 * 4 + 2], -eb[c4 * 4 + 3]);
+                    if ((cc >> 2) == rb) {
+                        const float4 b4 = row[cc ^ (r & 7)];
+                        g4.x += b4.x; g4.y += b4.y; g4.z += b4.z; g4.w += b4.w;
                     }
-                    // Binv of this half read above; G overwrites it (only this thread uses row r)
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4)
-                        row[(hh * 8 + c4) ^ (r & 7)] = make_float4(eb[c4 * 4], eb[c4 * 4 + 1], eb[c4 * 4 + 2], eb[c4 * 4 + 3]);
-                    put_row_bf16(A_SE2, r, hh * 4, e2);
-                    put_row_bf16(A_SG, r, hh * 4, eb);
+                    eb[c4 * 4] = g4.x; eb[c4 * 4 + 1] = g4.y; eb[c4 * 4 + 2] = g4.z; eb[c4 * 4 + 3] = g4.w;
                 }
+                // Binv of this half read above; G overwrites it (only this thread uses it)
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                    row[(shf * 8 + c4) ^ (r & 7)] = make_float4(eb[c4 * 4], eb[c4 * 4 + 1], eb[c4 * 4 + 2], eb[c4 * 4 + 3]);
+                put_row_bf16(A_SE2, r, shf * 4, e2);
+                put_row_bf16(A_SE2 + 8192, r, shf * 4, e2);
+                put_row_bf16(A_SG, r, shf * 4, eb);
             }
             solve_issue(2);
             // round 3 done: T = (G + E^2 G) Diag(beta), lower triangle, as the bf16 operand
             if (!solve_wait(2)) break;
             ptx::tc_fence_after();
-            if (t < C) {
-                const int r = t;
+            {
+                const int r = sr;
                 const float4 *row = reinterpret_cast<const float4 *>(Msc + r * 64);
                 const float4 *b4 = reinterpret_cast<const float4 *>(bs);
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    float d[32];
-                    ptx::tmem_ld32(tbase + lanes + hh * 32, d);
-                    ptx::tmem_wait_ld();
+                float d[32];
+                ptx::tmem_ld32(tbase + lanes + shf * 32, d);
+                ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const int cc = hh * 8 + c4;
-                        const float4 g4 = row[cc ^ (r & 7)], bv = b4[cc];
-                        d[c4 * 4 + 0] = cc * 4 + 0 <= r ? (g4.x + d[c4 * 4 + 0]) * bv.x : 0.f;
-                        d[c4 * 4 + 1] = cc * 4 + 1 <= r ? (g4.y + d[c4 * 4 + 1]) * bv.y : 0.f;
-                        d[c4 * 4 + 2] = cc * 4 + 2 <= r ? (g4.z + d[c4 * 4 + 2]) * bv.z : 0.f;
-                        d[c4 * 4 + 3] = cc * 4 + 3 <= r ? (g4.w + d[c4 * 4 + 3]) * bv.w : 0.f;
-                    }
-                    put_row_bf16(A_T, r, hh * 4, d);
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const int cc = shf * 8 + c4;
+                    const float4 g4 = row[cc ^ (r & 7)], bv = b4[cc];
+                    d[c4 * 4 + 0] = cc * 4 + 0 <= r ? (g4.x + d[c4 * 4 + 0]) * bv.x : 0.f;
+                    d[c4 * 4 + 1] = cc * 4 + 1 <= r ? (g4.y + d[c4 * 4 + 1]) * bv.y : 0.f;
+                    d[c4 * 4 + 2] = cc * 4 + 2 <= r ? (g4.z + d[c4 * 4 + 2]) * bv.z : 0.f;
+                    d[c4 * 4 + 3] = cc * 4 + 3 <= r ? (g4.w + d[c4 * 4 + 3]) * bv.w : 0.f;
                 }
+                put_row_bf16(A_T, r, shf * 4, d);
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();

@@ -102,3 +102,59 @@ def test_a_wrong_sign_in_the_first_group_is_caught():
     img["WQ"] = np.concatenate([-img["WQ"][:C], img["WQ"][C:]])
     o, _ = _chain_step(S0.T.copy(), img)
     assert np.max(np.abs(o - o_ref[:C])) > 1e-3
+
+
+def _series_solve(A, beta, skip=True):
+    """T = (I + A)^{-1} Diag(beta) as chunk prep forms it: 16 x 16 diagonal block inverses
+    (Binv), E = Binv N with N the strictly block-lower part of I + A, then the products
+    E^2, E Binv and E^2 G (G = Binv - E Binv) over 16-deep K-steps, skipping the steps the
+    block structure makes zero (E = Binv N: K-blocks 1-3; E^2: 1-2; E Binv: 0-2; E^2 G: 0-1)."""
+    C = A.shape[0]
+    L = np.eye(C) + A
+    blk = [slice(i, i + 16) for i in range(0, C, 16)]
+    Binv = np.zeros_like(L)
+    for s in blk:
+        Binv[s, s] = np.linalg.inv(L[s, s])
+    N = L - sum(np.pad(L[s, s], ((s.start, C - s.stop), (s.start, C - s.stop))) for s in blk)
+
+    def prod(X, Y, ks):
+        ks = ks if skip else range(len(blk))
+        return sum(X[:, blk[k]] @ Y[blk[k], :] for k in ks)
+
+    E = prod(Binv, N, (1, 2, 3))
+    E2 = prod(E, E, (1, 2))
+    G = Binv - prod(E, Binv, (0, 1, 2))
+    return np.tril(G + prod(E2, G, (0, 1))) @ np.diag(beta)
+
+
+def test_block_series_solve_equals_the_inverse():
+    rng = np.random.default_rng(11)
+    for _ in range(5):
+        C = 64
+        K = rng.standard_normal((C, 32)) / np.sqrt(32)
+        beta = 1 / (1 + np.exp(-rng.standard_normal(C)))
+        A = np.diag(beta) @ np.tril(K @ K.T, -1)
+        ref = np.linalg.inv(np.eye(C) + A) @ np.diag(beta)
+        got = _series_solve(A, beta)
+        assert np.allclose(got, ref, rtol=0, atol=1e-11)
+        # the skipped K-steps contribute nothing
+        assert np.allclose(got, _series_solve(A, beta, skip=False), rtol=0, atol=1e-14)
+
+
+def test_a_dropped_series_term_is_caught():
+    """Without the E^2 G term (or with E^2 summed over too few K-steps) the result is wrong."""
+    rng = np.random.default_rng(12)
+    C = 64
+    K = rng.standard_normal((C, 32)) / np.sqrt(32)
+    beta = np.full(C, 0.9)
+    A = np.diag(beta) @ np.tril(K @ K.T, -1)
+    ref = np.linalg.inv(np.eye(C) + A) @ np.diag(beta)
+    L = np.eye(C) + A
+    mask = np.kron(np.eye(4), np.ones((16, 16)))
+    Binv = np.linalg.inv(L * mask)
+    E = Binv @ (L * (1 - mask))
+    G = Binv - E @ Binv
+    assert not np.allclose(np.tril(G) @ np.diag(beta), ref, atol=1e-6)
+    E2_short = E[:, 16:32] @ E[16:32, :]           # K-block 2 dropped
+    assert not np.allclose(np.tril(G + E2_short @ G) @ np.diag(beta), ref, atol=1e-6)
+    assert np.allclose(np.tril(G + E @ E @ G) @ np.diag(beta), ref, atol=1e-11)
