@@ -398,8 +398,9 @@ __global__ void __launch_bounds__(kDtThreads, 1) decode_tma_kernel(DecodeArgs a)
 // frees the input buffer for the next item's load.  For every draft token they run the same
 // step as decode (conv, S' = Diag(alpha) S, w = beta (v - S'^T k), S = S' + k w^T, o = S^T q)
 // and write the resulting record (S and the window after that token) into one of two output
-// buffers, which the producer bulk-stores into that token's object.  The source object is
-// only read.  Traffic per item: one record read and K record writes.
+// buffers; compute thread 0 bulk-stores it into that token's object right away, so two
+// record stores can be in flight while the next draft runs.  The source object is only read.
+// Traffic per item: one record read and K record writes.
 constexpr int kVfMaxK = kVerifyFusedMaxK;
 constexpr uint32_t VF_IN = 0;                                  // record, then inputs [K][q|k|v|alpha]
 constexpr uint32_t VF_INPUTS = kDtRec;                         // 1 KiB per draft token
@@ -424,8 +425,6 @@ __global__ void __launch_bounds__(kDtThreads, 1) verify_tma_kernel(VerifyArgs a)
     volatile int *go = reinterpret_cast<volatile int *>(sm + VF_MISC + 40);
     uint64_t *in_full = reinterpret_cast<uint64_t *>(sm + VF_MISC + 48);
     uint64_t *in_free = in_full + 1;
-    uint64_t *out_full = in_full + 2;   // [2]
-    uint64_t *out_free = in_full + 4;   // [2]
     const __nv_bfloat16 *hist_win = reinterpret_cast<const __nv_bfloat16 *>(sm + VF_HIST);
     const __nv_bfloat16 *hist_draft = reinterpret_cast<const __nv_bfloat16 *>(sm + VF_HIST_DRAFT);
 
@@ -434,7 +433,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) verify_tma_kernel(VerifyArgs a)
     const int64_t PB = a.pool.page_bytes;
     const int P = a.pool.pages_per_object;
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) ptx::mbar_init(&in_full[i], 1);
+        for (int i = 0; i < 2; ++i) ptx::mbar_init(&in_full[i], 1);
         *err = 0;
         ptx::fence_mbar_init();
     }
@@ -490,10 +489,9 @@ __global__ void __launch_bounds__(kDtThreads, 1) verify_tma_kernel(VerifyArgs a)
             __syncwarp();
             return ok;
         };
-        int issued = 0, gv = 0;
-        bool ok_cur = false;
+        int issued = 0;
         if (blockIdx.x < total) {
-            ok_cur = issue_load(0);
+            (void)issue_load(0);
             issued = 1;
         }
         for (int n = 0;; ++n) {
@@ -503,30 +501,13 @@ __global__ void __launch_bounds__(kDtThreads, 1) verify_tma_kernel(VerifyArgs a)
             // the compute warps have taken item n out of the input buffer
             if (lane == 0 && (*err || !dt_wait(in_free, (uint32_t)(n & 1), err))) stop = 1;
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
-            bool ok_next = false;
             if (item + (int)gridDim.x < total) {
-                ok_next = issue_load(n + 1);
+                (void)issue_load(n + 1);
                 issued = n + 2;
             }
-            if (ok_cur && lane == 0) {
-                const int r = item / a.H, hh = item % a.H;
-                for (int jd = 0; jd < K; ++jd, ++gv) {
-                    const int ob = gv & 1;
-                    if (!dt_wait(&out_full[ob], (uint32_t)((gv >> 1) & 1), err)) break;
-                    const int32_t *ip = a.inter_pages + ((int64_t)jd * a.B + r) * P;
-                    record_pieces(ip, hh, [&](int32_t page, int64_t in, uint32_t at, uint32_t len) {
-                        ptx::bulk_store(a.pool.base + (int64_t)page * PB + in, sm + VF_OUT + ob * kDtRec + at, len);
-                    });
-                    ptx::bulk_commit();
-                    ptx::bulk_wait_read0();
-                    ptx::mbar_arrive(&out_free[ob]);
-                }
-            }
-            ok_cur = ok_next;
             __syncwarp();
         }
         if (lane == 0) {
-            ptx::bulk_wait0();
             if (*err && issued > 0) {
                 // leave no load in flight: only the last issued one can be pending
                 uint32_t k = 0;
@@ -576,11 +557,10 @@ __global__ void __launch_bounds__(kDtThreads, 1) verify_tma_kernel(VerifyArgs a)
                     const float4 w = *reinterpret_cast<const float4 *>(a.conv_w + ((int64_t)hh * C3 + c) * 4);
                     xb[c] = w.x * raw(jd, c) + w.y * raw(jd + 1, c) + w.z * raw(jd + 2, c) + w.w * raw(jd + 3, c);
                 }
-                // the output buffer's previous record has been read by its bulk store
-                if (tid == 0 && gv >= 2) *go = dt_wait(&out_free[ob], (uint32_t)(((gv >> 1) - 1) & 1), err) ? 1 : 0;
+                // the output buffer's previous record has been read by its bulk store (thread 0
+                // issued both stores since: at most the newer one may still be reading)
+                if (tid == 0 && gv >= 2) ptx::bulk_wait_read1();
                 named_bar(kDtBar, kDtCompute);
-                alive = *go != 0;
-                if (!alive) break;
                 // S' = Diag(alpha) S; partial column sums of S'^T k over this thread's 32 rows
                 float acc = 0.f;
 #pragma unroll
@@ -614,7 +594,21 @@ __global__ void __launch_bounds__(kDtThreads, 1) verify_tma_kernel(VerifyArgs a)
                 }
                 ptx::fence_proxy_async_smem();
                 named_bar(kDtBar, kDtCompute);
-                if (tid == 0) ptx::mbar_arrive(&out_full[ob]);
+                if (tid == 0) {
+                    // the record after draft jd into its object, piece by piece (at most one piece
+                    // per page it touches), from the buffer just written
+                    const int32_t *ip = a.inter_pages + ((int64_t)jd * a.B + item / a.H) * P;
+                    int64_t off = (int64_t)hh * a.pool.rec_bytes;
+                    uint32_t at = 0;
+                    while (at < kDtRec) {
+                        const int64_t pi = off / PB, in = off - pi * PB;
+                        const uint32_t len = (uint32_t)((int64_t)(kDtRec - at) < PB - in ? (kDtRec - at) : (PB - in));
+                        ptx::bulk_store(a.pool.base + (int64_t)ip[pi] * PB + in, sm + VF_OUT + ob * kDtRec + at, len);
+                        off += len;
+                        at += len;
+                    }
+                    ptx::bulk_commit();
+                }
                 if (rq == 0) {
                     const float o = (red[j] + red[D + j]) + (red[2 * D + j] + red[3 * D + j]);
                     static_cast<__nv_bfloat16 *>(a.o)[((int64_t)jd * total + item) * D + j] = __float2bfloat16_rn(o);
@@ -622,6 +616,7 @@ __global__ void __launch_bounds__(kDtThreads, 1) verify_tma_kernel(VerifyArgs a)
                 named_bar(kDtBar, kDtCompute);   // red and xb are reused by the next token
             }
         }
+        if (tid == 0) ptx::bulk_wait_read0();   // the last records have left their buffers
     }
     __syncthreads();
     if (*err && tid == 0) flag_status(a.status, KDA_DEV_TIMEOUT);
