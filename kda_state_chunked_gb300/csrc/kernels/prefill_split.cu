@@ -13,7 +13,7 @@
 //   chunk_prep_kernel (one CTA per (item, head), 160 threads, three CTAs per SM)
 //     conv, decay factors, Kt' = k gamma_r/gamma_C, Qt' = q gamma_r/gamma_C, Kb = k gamma_C/gamma_r,
 //     G | P = [Kt'; Qt'] Kb^T (tcgen05), T = (I + Diag(beta) strict_lower(G))^{-1} Diag(beta)
-//     (16 x 16 diagonal inverses on CUDA cores, the rest in three tcgen05 rounds),
+//     (16 x 16 diagonal inverses on CUDA cores, the rest in three tcgen05 stages),
 //     WK'^T = Kt'^T T^T (tcgen05), and writes one operand image
 //     per item, bf16 and 128-byte swizzled as the chain kernel's MMAs read it:
 //     Gamma_C [-WK' | Qt'] = [-WK' Gamma_C | q gamma_r], Kb, P, V, T, and gamma_C (fp32).  Conv
@@ -95,8 +95,8 @@ enum { AB_FULL = 0, AB_P1, AB_GP, AB_KBF, AB_T, AB_M2, AB_SO, A_NBARS };
 // a copy there, so TMEM lanes 64-127 hold the product's rows 0-63 once more and all four compute
 // warps share an epilogue, each thread half a row.  Binv over the second Qt' half (read by M1),
 // its copy over the first raw v half; N over the second raw v half; E, then E^2, over the raw v
-// tile with its copy in the second half (each once the previous round has read that tile); G
-// over Binv once round 2 has read it; T at A_T.
+// tile with its copy in the second half (each once the previous stage has read that tile); G
+// over Binv once stage 2 has read it; T at A_T.
 constexpr uint32_t A_SB = A_KQ + 16384 + 8192, A_SN = A_V + 8192, A_SE = A_V, A_SE2 = A_V, A_SG = A_SB;
 static_assert(A_SB + 8192 == A_V && A_SE + 8192 == A_SN, "solve tiles and their row copies");
 constexpr uint32_t A_ERR = 96;   // error flag, TMEM address and wait flag after the mbarriers
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
         const int p = t & 63, hf = t >> 6;              // channel pair (2p, 2p+1), row half
         const int c0 = 2 * p, kb = c0 >> 6, cb = (c0 & 63) * 2;
         const uint32_t lanes = (uint32_t)(warp * 32) << 16;
-        int solve_rounds = 0;   // rounds of the tensor-core solve issued (by thread 0)
+        int solve_stages = 0;   // stages of the tensor-core solve issued (by thread 0)
         do {
             // conv weights of the channel pair, tap by tap: (channel c0, channel c0 + 1)
             float2 wq[4], wk[4], wv[4];
@@ -483,8 +483,8 @@ __global__ void __launch_bounds__(kAThreads, 3)
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             named_bar(kAWg, 128);
-            // Each round: the compute warps write its operands, meet at a barrier, and thread 0
-            // issues the round's MMAs and its commit; the round's completion is polled by
+            // Each stage: the compute warps write its operands, meet at a barrier, and thread 0
+            // issues the stage's MMAs and its commit; the stage's completion is polled by
             // thread 0 and handed to the warpgroup through a flag word of its own (one barrier).
             volatile int *solve_flag = reinterpret_cast<volatile int *>(sm + A_RED);   // free after the conv
             auto solve_issue = [&](int rd) {
@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
                     }
                     ptx::mma_commit(&S.bar[AB_SO]);
                 }
-                solve_rounds = rd + 1;
+                solve_stages = rd + 1;
             };
             auto solve_wait = [&](int rd) -> bool {
                 if (t == 0) solve_flag[rd] = ptx::mbar_wait(&S.bar[AB_SO], (uint32_t)(rd & 1), S.err) ? 1 : 0;
@@ -594,7 +594,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
             }
             // Off-diagonal part on the tensor cores: with Binv = the block-diagonal inverse and N
             // the strictly block-lower part of A, L = I + A has L^{-1} = (I - E)(I + E^2) Binv =
-            // G + E^2 G, E = Binv N, G = Binv - E Binv (E^4 = 0).  Three bf16 MMA rounds with
+            // G + E^2 G, E = Binv N, G = Binv - E Binv (E^4 = 0).  Three bf16 MMA stages with
             // fp32 accumulation: E = Binv N; E^2 and E Binv; E^2 G (10 MMAs: the block structure
             // leaves some 16-deep steps of each product zero).  Every operand is a 64 x 64 bf16
             // tile, row-major and 128-byte swizzled, which serves as a K-major A and as an
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
             // product, from the TMEM lanes of its warp (lanes 64-127 repeat rows 0-63).
             const int sr = t & 63, shf = t >> 6;
             solve_issue(0);
-            // round 1 done: E -> bf16 tile and its row copy
+            // stage 1 done: E -> bf16 tile and its row copy
             if (!solve_wait(0)) break;
             ptx::tc_fence_after();
             {
@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 put_row_bf16(A_SE + 8192, sr, shf * 4, e);
             }
             solve_issue(1);
-            // round 2 done: E^2 -> bf16 tile and copy; G = Binv - E Binv -> bf16 tile and fp32 row of Msc
+            // stage 2 done: E^2 -> bf16 tile and copy; G = Binv - E Binv -> bf16 tile and fp32 row of Msc
             if (!solve_wait(1)) break;
             ptx::tc_fence_after();
             {
@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(kAThreads, 3)
                 put_row_bf16(A_SG, r, shf * 4, eb);
             }
             solve_issue(2);
-            // round 3 done: T = (G + E^2 G) Diag(beta), lower triangle, as the bf16 operand
+            // stage 3 done: T = (G + E^2 G) Diag(beta), lower triangle, as the bf16 operand
             if (!solve_wait(2)) break;
             ptx::tc_fence_after();
             {
@@ -689,9 +689,9 @@ __global__ void __launch_bounds__(kAThreads, 3)
             }
         } while (false);
         // on a timeout, leave no solve MMA in flight: its commit tracks every MMA before it
-        if (t == 0 && *S.err && solve_rounds > 0) {
+        if (t == 0 && *S.err && solve_stages > 0) {
             uint32_t k = 0;
-            while (!ptx::mbar_try_wait(&S.bar[AB_SO], (uint32_t)((solve_rounds - 1) & 1)) && k < ptx::kSpinLimit) ++k;
+            while (!ptx::mbar_try_wait(&S.bar[AB_SO], (uint32_t)((solve_stages - 1) & 1)) && k < ptx::kSpinLimit) ++k;
         }
     }
     // ---------------------------------------------------------------------- teardown
