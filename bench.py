@@ -635,8 +635,9 @@ def _aggregate(units_per_rank_step: int, steps: int, total_ms_max: float, world:
 def _e2e_pipelined(bench, steps: int, warmup: int, stream, world: int):
     """End-to-end steps through the public API from pinned host memory: every step copies its
     inputs host -> device, runs the prefill, and copies its output device -> host.  Steps are
-    pipelined the way a serving loop would run them: the input copies of step i + 1 (two copy
-    streams) and the output copy of step i - 1 (a third stream) overlap the prefill of step i,
+    pipelined the way a serving loop would run them: the input copies of step i + 1 (four copy
+    streams, one per large input: concurrent copies keep more of the link busy than one or two
+    streams do) and the output copy of step i - 1 (a fifth stream) overlap the prefill of step i,
     with double-buffered device inputs and outputs ordered by events.  Returns (h2d bytes per
     step, d2h bytes per step, total ms of the `steps` timed steps, every copy included)."""
     import torch
@@ -645,7 +646,7 @@ def _e2e_pipelined(bench, steps: int, warmup: int, stream, world: int):
     o_host = [torch.empty(bench.o.shape, dtype=bench.o.dtype).pin_memory() for _ in range(2)]
     dtoks = [{k: torch.empty_like(v) for k, v in bench.toks.items()} for _ in range(2)]
     dout = [torch.empty_like(bench.o) for _ in range(2)]
-    s_in = [torch.cuda.Stream(), torch.cuda.Stream()]
+    s_in = [torch.cuda.Stream() for _ in range(4)]
     s_out = torch.cuda.Stream()
     ev_in = [[torch.cuda.Event() for _ in s_in] for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
