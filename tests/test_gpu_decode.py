@@ -58,8 +58,8 @@ def _decode_case(dtype, d, B, H, steps, page_bytes, seed):
 
 
 @pytest.mark.parametrize("dtype,d,page_bytes", [("f32", 64, 65536), ("bf16", 128, 262144),
-                                                ("bf16", 128, 65536), ("f32", 128, 4096),
-                                                ("bf16", 128, 19 * 256)])
+                                                ("bf16", 128, 65536), ("bf16", 128, 260 * 256),
+                                                ("f32", 128, 4096), ("bf16", 128, 19 * 256)])
 def test_decode_steps_match_oracle(dtype, d, page_bytes):
     _decode_case(dtype, d, B=6, H=3, steps=5, page_bytes=page_bytes, seed=70 + d)
 

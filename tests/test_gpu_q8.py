@@ -32,6 +32,7 @@ def _objects(pool, n, H, d, dtype, seed, scale=0.3):
 
 
 @pytest.mark.parametrize("dtype,d,H,page_bytes", [("bf16", 128, 3, 65536), ("bf16", 128, 32, 65536),
+                                                  ("bf16", 128, 5, 19 * 256),   # pipeline, 70-page lists
                                                   ("f32", 64, 2, 4096), ("bf16", 64, 5, 768)])
 def test_write_q8_is_the_oracle_codec_bit_for_bit(dtype, d, H, page_bytes):
     dt = kda.DTYPES[dtype]
@@ -56,8 +57,8 @@ def test_write_q8_is_the_oracle_codec_bit_for_bit(dtype, d, H, page_bytes):
         assert np.array_equal(Si, S[i]) and np.array_equal(Wi, W[i])
 
 
-@pytest.mark.parametrize("dtype,d,H,page_bytes", [("bf16", 128, 4, 65536), ("f32", 64, 3, 4096),
-                                                  ("bf16", 64, 5, 768)])
+@pytest.mark.parametrize("dtype,d,H,page_bytes", [("bf16", 128, 4, 65536), ("bf16", 128, 5, 19 * 256),
+                                                  ("f32", 64, 3, 4096), ("bf16", 64, 5, 768)])
 def test_restore_q8_dequantises_bit_for_bit(dtype, d, H, page_bytes):
     dt = kda.DTYPES[dtype]
     n = 2

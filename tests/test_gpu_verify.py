@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.mark.parametrize("dtype,d,page_bytes", [("bf16", 128, 65536), ("f32", 64, 4096)])
+@pytest.mark.parametrize("dtype,d,page_bytes", [("bf16", 128, 65536), ("bf16", 128, 260 * 256), ("f32", 64, 4096)])
 def test_verify_intermediate_states_and_accept(dtype, d, page_bytes):
     dt = kda.DTYPES[dtype]
     B, H, K = 3, 2, 4
