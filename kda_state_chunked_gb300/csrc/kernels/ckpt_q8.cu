@@ -193,8 +193,8 @@ __global__ void __launch_bounds__(kQThreads) dequantize_kernel(Q8Args a) {
 //     have taken its record into registers.
 //   - A store warp bulk-stores converted records from a ring of destination slots; a slot is
 //     released once its store has read it out.
-//   - Both read an item's page ids into registers one step ahead, so those global reads
-//     overlap the current step.
+//   - Both read an item's page ids into registers two steps ahead, so those global reads
+//     overlap the steps in between, and each checks its own list before using it.
 //   - Sixteen compute warps convert one item at a time from its source slot into its
 //     destination slot: four threads per row of S, 32 consecutive values each (a row's
 //     max-abs is a reduction over its four threads).
@@ -372,24 +372,27 @@ __global__ void __launch_bounds__(kQtThreads, 1) q8_tma_kernel(Q8Args a) {
                 at += len;
             }
         };
-        Ids cur, nxt;
+        Ids cur, nxt, nxt2;   // page ids of items n, n + 1, n + 2
         int n = 0;
         if (blockIdx.x < total) fetch_ids(0, cur);
+        if (blockIdx.x + (int)gridDim.x < total) fetch_ids(1, nxt);
         for (;; ++n) {
             const int item = blockIdx.x + n * gridDim.x;
             if (item >= total) break;
-            if (item + (int)gridDim.x < total) fetch_ids(n + 1, nxt);   // overlaps this step
+            // two items ahead, so that the global reads overlap two steps even when the warp runs
+            // ahead of the compute warps
+            if (item + 2 * (int)gridDim.x < total) fetch_ids(n + 2, nxt2);
             const int32_t *l = list_of(n);
             int stop = 0;
-            if (loader) {
-                // every page id of both lists in range, or the item is skipped and flagged
-                const int32_t *dl = dpl + (int64_t)(item / a.H) * dv.pages_per_object;
-                bool ok = true;
+            // every page id of this warp's list in range (ids from 64 on read from the list), or
+            // the item is skipped and flagged: the loader does not load it, the store warp does
+            // not store it
+            bool ok = true;
 #pragma unroll
-                for (int u = 0; u < kIds; ++u) ok = ok && (uint32_t)cur.id[u] < (uint32_t)sv.num_pages;
-                for (int i = lane + 32 * kIds; i < sv.pages_per_object; i += 32) ok = ok && (uint32_t)l[i] < (uint32_t)sv.num_pages;
-                for (int i = lane; i < dv.pages_per_object; i += 32) ok = ok && (uint32_t)dl[i] < (uint32_t)dv.num_pages;
-                ok = __all_sync(0xffffffffu, ok);
+            for (int u = 0; u < kIds; ++u) ok = ok && (uint32_t)cur.id[u] < (uint32_t)v.num_pages;
+            for (int i = lane + 32 * kIds; i < v.pages_per_object; i += 32) ok = ok && (uint32_t)l[i] < (uint32_t)v.num_pages;
+            ok = __all_sync(0xffffffffu, ok);
+            if (loader) {
                 // load item n once compute has taken the item that used its source slot
                 const int bs = n % NS;
                 if (lane == 0 && (*err || (n >= NS && !ptx::mbar_wait(&sfree[bs], (uint32_t)(((n - NS) / NS) & 1), err))))
@@ -413,10 +416,12 @@ __global__ void __launch_bounds__(kQtThreads, 1) q8_tma_kernel(Q8Args a) {
                 const int bd = n % ND;
                 if (lane == 0 && !ptx::mbar_wait(&dfull[bd], (uint32_t)((n / ND) & 1), err)) stop = 1;
                 if (__shfl_sync(0xffffffffu, stop, 0)) break;
-                if (dvalid[bd])
+                if (dvalid[bd] && ok)
                     pieces(cur, l, item % a.H, G::DB, [&](uint8_t *g, uint32_t at, uint32_t len) {
                         ptx::bulk_store(g, sm + G::DST0 + bd * G::DB + at, len);
                     });
+                else if (!ok && lane == 0)
+                    flag_status(a.status, KDA_DEV_BAD_PAGE);
                 if (lane == 0) {
                     ptx::bulk_commit();
                     if constexpr (ND == 1) {
@@ -431,6 +436,7 @@ __global__ void __launch_bounds__(kQtThreads, 1) q8_tma_kernel(Q8Args a) {
             }
             __syncwarp();
             cur = nxt;
+            nxt = nxt2;
         }
         if (lane == 0) {
             ptx::bulk_wait0();
