@@ -8,7 +8,13 @@
 
 namespace kda {
 
-constexpr int64_t kWaveBytes = (int64_t)512 << 20;
+// Cap on one wave's operand images (one of two workspace slots): 512 MiB while every chain of
+// a wave has an SM of its own, 2 GiB when there are more chains than SMs.  Then the chains of a
+// wave run in several rounds and every extra wave repeats each round's launch and state
+// hand-off, so fewer, larger waves pay (varlen resume, 1024 chains: 65 waves -> 18, 7.15 ms ->
+// 5.84 ms); with few chains, smaller waves let them start sooner (no gain measured from larger
+// ones for 32 or 64 chains).
+constexpr int64_t kWaveBytes = (int64_t)512 << 20, kWaveBytesManyChains = (int64_t)2048 << 20;
 
 bool split_applies(int32_t d, int32_t dtype) { return dtype == KDA_BF16 && d == 128; }
 
@@ -115,14 +121,15 @@ void make_split_plan(int32_t H, int32_t nseq, const int32_t *cu, const int64_t *
     // Fewest waves whose images fit a slot if every wave were equal; candidates from there up
     // to six more waves, sizes geometric in the wave index (decreasing when chunk preparation
     // dominates, increasing when the chains do); the modelled fastest split that keeps every
-    // slot under kWaveBytes wins.  The equal split is always a candidate.
+    // slot under the cap wins.  The equal split is always a candidate.
     const int64_t unit_bytes = (int64_t)H * kImageBytes;
     const int64_t per_chunk = (int64_t)hs.n.size() * unit_bytes;
-    const int64_t cw_max = std::max<int64_t>(1, kWaveBytes / per_chunk);
+    const int64_t wave_bytes = (int64_t)hs.n.size() * H > (int64_t)kSMs ? kWaveBytesManyChains : kWaveBytes;
+    const int64_t cw_max = std::max<int64_t>(1, wave_bytes / per_chunk);
     const int W0 = (int)((maxc + cw_max - 1) / cw_max);
     auto fits = [&](const std::vector<int32_t> &b) {
         for (size_t w = 0; w + 1 < b.size(); ++w)
-            if (b[w + 1] <= b[w] || hs.chunks_in(b[w], b[w + 1]) * unit_bytes > kWaveBytes) return false;
+            if (b[w + 1] <= b[w] || hs.chunks_in(b[w], b[w + 1]) * unit_bytes > wave_bytes) return false;
         return true;
     };
     std::vector<int32_t> best, cand;
