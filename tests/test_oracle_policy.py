@@ -71,6 +71,17 @@ def test_rollback_6000_to_4096():
     assert B == g["resume"] and g["matched"] - B == g["replay"]
 
 
+def test_hit_exactly_at_a_stored_position_replays_nothing():
+    """A checkpoint at p holds the state after tokens [0, p) (the oracle's resume test shows
+    that state continues the uninterrupted run), so a match of exactly p tokens resumes at p
+    with nothing to replay; one token fewer falls back to the previous checkpoint.  Stored
+    positions as in the 6000-token rollback example."""
+    g = GOLDEN["rollback_6000"]
+    assert policy.hit_boundary(g["stored"], 4096) == 4096
+    assert policy.hit_boundary(g["stored"], 8192) == 8192
+    assert policy.hit_boundary(g["stored"], 4095) == 0
+
+
 def test_rollback_15k_to_10k():
     g = GOLDEN["rollback_15k"]
     stored = list(range(g["interval"], 10 * g["interval"], g["interval"]))

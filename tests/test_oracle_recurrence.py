@@ -343,3 +343,35 @@ def test_varlen_batch_equals_separate_runs():
                              S0=S0[s:s + 1], win0=win0[s:s + 1])
         assert np.array_equal(one["o"], batch["o"][sl])
         assert np.array_equal(one["S"][0], batch["S"][s])
+
+
+def test_full_path_is_conv_then_recurrence_per_head():
+    """The full path is the conv followed by the recurrence, each (sequence, head) on its own
+    slices: its outputs, final states and checkpoints equal the plain scan (pinned above) run
+    on that pair's post-conv values (pinned against numpy's convolution above) with that
+    pair's own decay and beta, from that pair's initial state.  This pins the packed
+    [T][H][d] indexing of every input and the token count at which a checkpoint is taken."""
+    rng = np.random.default_rng(RNG_SEED + 19)
+    H, d = 3, 5
+    lens = [7, 12, 3]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    q, k, v = (rng.standard_normal((T, H, d)) for _ in range(3))
+    a = rng.uniform(0.3, 1.0, (T, H, d))
+    b = rng.uniform(0.05, 1.0, (T, H))
+    w = rng.standard_normal((H, 3 * d, 4)) * 0.5
+    S0 = rng.standard_normal((len(lens), H, d, d))
+    win0 = rng.standard_normal((len(lens), H, 3, 3 * d))
+    cks = [[2, 7], [1, 5, 12], [3]]
+    r = oracle.kda_run(q, k, v, a, b, w, cu, S0=S0, win0=win0, ckpt_counts=cks, want_xbar=True)
+    xb = r["xbar"]
+    for s in range(len(lens)):
+        sl = slice(cu[s], cu[s + 1])
+        for h in range(H):
+            qb, kb, vb = xb[sl, h, :d], xb[sl, h, d:2 * d], xb[sl, h, 2 * d:]
+            o, S = oracle.scan(qb, kb, vb, a[sl, h], b[sl, h], S0[s, h])
+            assert _rel(r["o"][sl, h], o) < 1e-13
+            assert _rel(r["S"][s, h], S) < 1e-13
+            for n, p in enumerate(cks[s]):
+                _, Sp = oracle.scan(qb[:p], kb[:p], vb[:p], a[sl, h][:p], b[sl, h][:p], S0[s, h])
+                assert _rel(r["ck_S"][s][n][h], Sp) < 1e-13
