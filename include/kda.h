@@ -61,7 +61,8 @@ typedef enum kda_status_code {
     KDA_ENOPAGES = -2,  /* pool exhausted: nothing was allocated */
     KDA_EREF = -3,      /* reference-count misuse (freeing a free page, claiming a used one) */
     KDA_ECUDA = -4,     /* CUDA launch / runtime error */
-    KDA_EDEVICE = -5    /* a kernel found a bad page id or metadata (see kda_sync_status) */
+    KDA_EDEVICE = -5    /* a kernel found a bad page id, bad metadata or an out-of-range decay
+                           (see kda_sync_status) */
 } kda_status_code;
 
 typedef enum kda_dtype { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -70,6 +71,8 @@ typedef enum kda_dtype { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 #define KDA_DEV_BAD_PAGE 1   /* a page id outside [0, num_pages) was met; access skipped */
 #define KDA_DEV_BAD_META 2   /* inconsistent metadata in the workspace; work skipped */
 #define KDA_DEV_TIMEOUT 4    /* an internal pipeline wait gave up; that sequence is incomplete */
+#define KDA_DEV_RANGE 8      /* prefill: a chunk's decay product fell below the supported range
+                                (see alpha in kda_prefill_varlen); that sequence's results are undefined */
 
 typedef struct kda_pool kda_pool;
 
@@ -185,6 +188,14 @@ int32_t kda_prefill_waves(int32_t H, int32_t d, int32_t dtype, int32_t nseq, con
  *                    object, 0 = start from zeros
  *   q, k, v, alpha   device [T_tot][H][d] dtype (q, k as given: any normalisation is the
  *                    caller's; the conv runs here)
+ *                    alpha is the forget gate, in [0, 1] per key channel.  The chunked
+ *                    kernels factor a chunk's decay through its running product per channel,
+ *                    so the product of alpha over each 64-token chunk must stay at or above
+ *                    2^-100 in every channel (a geometric-mean gate above 0.34 over a full
+ *                    chunk; a gate of exactly 0 is below it).  A chunk below that sets
+ *                    KDA_DEV_RANGE, and the outputs, states and checkpoints of its
+ *                    (sequence, head) from that chunk on are undefined.  kda_decode_step
+ *                    steps token by token and has no such limit.
  *   beta             device [T_tot][H] dtype
  *   conv_w           device fp32 [H][3d][4]; tap j multiplies raw token t-3+j
  *   o                device [T_tot][H][d] dtype, written

@@ -24,7 +24,7 @@ _lib = None
 
 KDA_OK, KDA_EINVAL, KDA_ENOPAGES, KDA_EREF, KDA_ECUDA, KDA_EDEVICE = 0, -1, -2, -3, -4, -5
 KDA_F32, KDA_BF16 = 0, 1
-KDA_DEV_BAD_PAGE, KDA_DEV_BAD_META, KDA_DEV_TIMEOUT = 1, 2, 4
+KDA_DEV_BAD_PAGE, KDA_DEV_BAD_META, KDA_DEV_TIMEOUT, KDA_DEV_RANGE = 1, 2, 4, 8
 DTYPES = {"f32": KDA_F32, "bf16": KDA_BF16}
 
 # Every symbol include/kda.h declares, with (restype, argtypes).

@@ -13,6 +13,10 @@ namespace kda {
 constexpr int kChunk = 64;   // tokens per chunk; chunks are aligned to absolute positions
 constexpr int kConvW = 4;    // short causal conv width (taps on t-3 .. t)
 constexpr int kWin = kConvW - 1;
+// Smallest product of alpha over one chunk, per key channel, that the chunked prefill kernels
+// accept: they scale rows by gamma_r / gamma_C (up to 1 / gamma_C) and by its inverse, which
+// must stay far inside the fp32 / bf16 exponent range.  Below it a kernel sets KDA_DEV_RANGE.
+constexpr float kMinChunkDecay = 0x1p-100f;
 
 // Per-sequence metadata of one prefill call (device copy in the workspace).
 struct SeqMeta {
@@ -62,7 +66,8 @@ struct PrefillArgs {
 // (chunk, head) item, a sequential chain consumes the images in chunk order.  The chunks of
 // every chain are processed in waves (wave w = local chunks [wave_c0[w], wave_c0[w + 1]));
 // wave w's images live in slot w % 2 of the image buffer.
-constexpr int64_t kImageBytes = 82432;   // Qt' 16 KiB | Kb 16 KiB | P 8 KiB | WK'^T 16 KiB | V 16 KiB | T 8 KiB | gamma_C 512 B
+constexpr int64_t kImageBytes = 82432;   // [-WK' Gamma_C | q gamma_r] 32 KiB | [P^T | Kb] 24 KiB | V 16 KiB |
+                                         // T 8 KiB | gamma_C 512 B
 
 struct SplitItem {
     int32_t seq;   // sequence

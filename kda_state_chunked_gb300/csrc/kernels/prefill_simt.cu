@@ -23,7 +23,8 @@
 // prefill and §Les checkpoints sont en lecture seule).
 //
 // The decay factorisation divides by gamma; it is exact in fp32 as long as the product of
-// alpha over one chunk stays above ~1e-30 in every channel.
+// alpha over one chunk stays at or above 2^-100 (kMinChunkDecay) in every channel.  A chunk
+// below that sets KDA_DEV_RANGE.
 #include "common.cuh"
 
 namespace kda {
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) prefill_simt_kernel(PrefillAr
                     gs[r * D + i] = g;
                 }
                 gC[i] = g;
+                if (!(g >= kMinChunkDecay)) flag_status(a.status, KDA_DEV_RANGE);   // kh = k / gamma reaches 1 / g
             }
         }
         __syncthreads();

@@ -322,6 +322,9 @@ __global__ void __launch_bounds__(kAThreads, 3)
             if (hf == 0) {
                 gC[c0] = gCx;
                 gC[c0 + 1] = gCy;
+                // the row scales gamma_r / gamma_C reach 1 / gamma_C: report a chunk whose
+                // decay leaves the range they are exact in (NaN included)
+                if (!(gCx >= kMinChunkDecay && gCy >= kMinChunkDecay)) flag_status(pa.status, KDA_DEV_RANGE);
             }
             float2 g2 = hf ? h0 : make_float2(1.f, 1.f);
             uint32_t swz[8];

@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (hf == 0) {
                 gC[b * 128 + c0] = gCx;
                 gC[b * 128 + c0 + 1] = gCy;
+                if (!(gCx >= kMinChunkDecay && gCy >= kMinChunkDecay)) flag_status(a.status, KDA_DEV_RANGE);
             }
             float gx = hf ? h0.x : 1.f, gy = hf ? h0.y : 1.f;
             // One row: conv of q | k | v, running decay, scaled bf16 operands written in place

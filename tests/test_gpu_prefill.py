@@ -11,7 +11,7 @@ import kda_state_chunked_gb300 as kda
 from kda_state_chunked_gb300 import workloads
 from oracle import policy
 
-from kda_cases import (Prefill, TOL, compare_prefill, oracle_positions, oracle_prefill,
+from kda_cases import (Prefill, TOL, assert_close, compare_prefill, oracle_positions, oracle_prefill,
                        random_state, read_object, read_object_bytes, write_object)
 
 pytestmark = pytest.mark.gpu
@@ -95,7 +95,6 @@ def test_resume_from_every_512_boundary(dtype, d):
         o_part = part.o.float().cpu().numpy()
         S_p, W_p = read_object(pool, act2[0], H, d, dtype)
         for h in range(H):
-            from kda_cases import assert_close
             assert_close(o_part[:, h], o_full[:, h], TOL[dtype], f"resume {B} o head {h}")
             assert_close(o_part[:, h], ref_full["o"][B:, h], TOL[dtype], f"resume {B} o vs oracle",
                          name=f"prefill cases ({dtype})")
@@ -175,6 +174,54 @@ def test_bad_checkpoint_page_is_reported_not_faulted():
         kda.kda_prefill_varlen(pool, [0, T], [0], [0], dev["q"], dev["k"], dev["v"], dev["alpha"],
                                dev["beta"], dev["conv_w"], o, act, [0], [512], [[99]], ws, st)
     assert e.value.code == kda.KDA_EINVAL
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
+def test_decay_outside_the_factored_range_is_reported(dtype, d):
+    """A forget gate of exactly 0 (a full reset of one key channel) puts its chunk's decay
+    product below the 2^-100 the chunked kernels factor exactly: the call reports
+    KDA_DEV_RANGE, and the (sequence, head) pairs it does not touch still match the oracle.
+    A strong decay inside the range (a gate of about 0.377 over a whole chunk, product about
+    2^-90) reports nothing and matches the oracle everywhere."""
+    H, lens = 2, [300, 200]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    starts = [0, 0]
+    cpu, dev = _toks(int(cu[-1]), H, d, dtype, 41)
+    pool = kda.Pool(65536, 256, DEV)
+    P = pool.object_pages(H, d, kda.DTYPES[dtype])
+
+    # a gate of 0 in sequence 0, head 1, channel 5, token 70 (its second chunk)
+    cz, dz = {k: v.clone() for k, v in cpu.items()}, {k: v.clone() for k, v in dev.items()}
+    cz["alpha"][70, 1, 5] = 0.0
+    dz["alpha"][70, 1, 5] = 0.0
+    act = kda.kda_page_alloc(pool, 2 * P).reshape(2, P)
+    ws = kda.prefill_workspace(dz["q"], cu, starts, 0, P)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o = torch.full_like(dz["q"], float("nan"))
+    kda.kda_prefill_varlen(pool, cu, starts, [0, 0], dz["q"], dz["k"], dz["v"], dz["alpha"], dz["beta"],
+                           dz["conv_w"], o, act, workspace=ws, status=st)
+    rc, bits = kda.kda_sync_status(st)
+    assert rc == kda.KDA_EDEVICE and bits == kda.KDA_DEV_RANGE
+    ref = oracle_prefill(cz, cu, starts)
+    on = o.float().cpu().numpy()
+    for s, h in ((0, 0), (1, 0), (1, 1)):
+        a, b = int(cu[s]), int(cu[s + 1])
+        assert_close(on[a:b, h], ref["o"][a:b, h], TOL[dtype], f"gate 0: o seq {s} head {h}")
+        S, W = read_object(pool, act[s], H, d, dtype)
+        assert_close(S[h], ref["S"][s, h], TOL[dtype], f"gate 0: final S seq {s} head {h}")
+    kda.kda_page_decref(pool, act.reshape(-1))
+
+    # the same channel decaying by 0.377 per token over the whole second chunk
+    g = torch.tensor(0.377).to(cpu["alpha"].dtype)
+    cs, ds = {k: v.clone() for k, v in cpu.items()}, {k: v.clone() for k, v in dev.items()}
+    cs["alpha"][64:128, 1, 5] = g
+    ds["alpha"][64:128, 1, 5] = g.to(DEV)
+    assert float(g) ** 64 > 2.0 ** -100
+    act = kda.kda_page_alloc(pool, 2 * P).reshape(2, P)
+    run = Prefill(pool, ds, cu, starts, [0, 0], act, stride=1, include_last=True)
+    ck = oracle_positions(cu, starts, 1, True)
+    ref = oracle_prefill(cs, cu, starts, ckpt_abs=ck)
+    compare_prefill(pool, run, ref, cu, act, dtype, ck, name=f"prefill cases ({dtype})")
 
 
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
