@@ -158,3 +158,55 @@ def test_a_dropped_series_term_is_caught():
     E2_short = E[:, 16:32] @ E[16:32, :]           # K-block 2 dropped
     assert not np.allclose(np.tril(G + E2_short @ G) @ np.diag(beta), ref, atol=1e-6)
     assert np.allclose(np.tril(G + E @ E @ G) @ np.diag(beta), ref, atol=1e-11)
+
+
+def _factored_gram_fp32(k, al):
+    """G = Kt' Kb^T with the kernels' fp32 factors: gamma_r by running products, the row scale
+    gamma_r / gamma_C through the reciprocal of gamma_C, and Kb's scale as its reciprocal."""
+    f32 = np.float32
+    k, al = k.astype(f32), al.astype(f32)
+    gam = np.cumprod(al, axis=0, dtype=f32)
+    gC = gam[-1]
+    with np.errstate(divide="ignore", over="ignore", invalid="ignore"):
+        s = gam * (f32(1) / gC)
+        Kt, Kb = k * s, k * (f32(1) / s)
+        G = (Kt @ Kb.T).astype(f32)
+    return G, gC
+
+
+def _exact_gram_lower(k, al):
+    """Strictly lower G in fp64 from the per-pair decay prod_{s<u<=r} alpha_u, no factoring."""
+    C = k.shape[0]
+    G = np.zeros((C, C))
+    for r in range(C):
+        for s in range(r):
+            G[r, s] = np.sum(k[r] * k[s] * np.prod(al[s + 1:r + 1], axis=0))
+    return G
+
+
+def test_factored_decay_is_exact_down_to_the_range_limit():
+    """With a channel decaying to about 2^-99.5 over the chunk (just inside the 2^-100 the
+    prefill kernels accept), the fp32 factors stay finite, every sum of the Gram matrix
+    (the upper triangle's large ones included) stays finite, and the strictly lower part
+    the solve uses matches the unfactored per-pair decay to fp32 rounding.  A gate of 0
+    puts gamma_C below the limit and the factored form produces non-finite values, which is
+    why the kernels report such a chunk."""
+    rng = np.random.default_rng(21)
+    C, d = 64, 128
+    k = rng.standard_normal((C, d))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    al = rng.uniform(0.4, 1.0, (C, d))
+    al[:, :4] = 2.0 ** (-99.5 / 64)                  # four channels at the edge of the range
+    al = al.astype(np.float32).astype(np.float64)
+    G, gC = _factored_gram_fp32(k, al)
+    assert np.min(gC) >= np.float32(2.0 ** -100)
+    assert np.all(np.isfinite(G))
+    ref = _exact_gram_lower(k.astype(np.float32).astype(np.float64), al)
+    low = np.tril(G.astype(np.float64), -1)
+    assert np.max(np.abs(low - ref)) <= 1e-5 * np.max(np.abs(ref))
+
+    al0 = al.copy()
+    al0[30, 0] = 0.0
+    G0, gC0 = _factored_gram_fp32(k, al0)
+    assert not gC0[0] >= np.float32(2.0 ** -100)
+    assert not np.all(np.isfinite(G0))
