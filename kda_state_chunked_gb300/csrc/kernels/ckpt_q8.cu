@@ -200,9 +200,10 @@ __global__ void __launch_bounds__(kQThreads) dequantize_kernel(Q8Args a) {
 //     max-abs is a reduction over its four threads).
 // Quantising: 3 source slots (67,840 B) and 1 destination slot (19,200 B); dequantising: 3
 // source slots (19,200 B) and 2 destination slots (67,840 B), with up to two stores in flight.
-// The codes are those of the per-record kernels above, bit for bit: the division goes through
-// the reciprocal where that provably gives the same integer (see below), through the IEEE
-// division elsewhere.
+// For finite states the codes are those of the per-record kernels above, bit for bit: the
+// division goes through the reciprocal where that provably gives the same integer (see below),
+// through the IEEE division elsewhere.  (A state holding inf or NaN, which no valid recurrence
+// produces, gets unspecified codes from either kernel.)
 constexpr int kQtCompute = 512;
 constexpr int kQtThreads = kQtCompute + 64;   // + load warp + store warp
 constexpr uint32_t kQtFull = 67840, kQtQ8 = 19200;
