@@ -527,19 +527,31 @@ def _varlen_phase(dev, steps=5, warmup=3):
             "achieved_gbs": ab / (ms * 1e-3) / 1e9, "steps": steps}
 
 
-def _oracle_sample(toks_cpu_fn, threads_note=True):
-    """Time the oracle (as it stands) on one sequence of the batched workload."""
+def _oracle_sample(toks_cpu_fn, gpu_o=None):
+    """Time the oracle (as it stands) on one sequence of the batched workload.  With gpu_o
+    (the library's output for that sequence, [T, H, d] on the host) the result also holds the
+    worst max-relative error of the library's output per head against the oracle's."""
+    import numpy as np
     import oracle
     from kda_state_chunked_gb300 import workloads
     w = workloads.WORKLOADS[WORKLOAD]
     t = toks_cpu_fn()
     ck = [[p for p in range(2048, w.T + 1, 2048)]]
     t0 = time.perf_counter()
-    oracle.kda_run(t["q"], t["k"], t["v"], t["alpha"], t["beta"], t["conv_w"], [0, w.T], ckpt_counts=ck)
+    ref = oracle.kda_run(t["q"], t["k"], t["v"], t["alpha"], t["beta"], t["conv_w"], [0, w.T], ckpt_counts=ck)
     sec = time.perf_counter() - t0
-    return {"value": w.T / sec, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"sequence 0 of the batched workload: {w.T} tokens x {w.H} heads, conv + "
-                      f"fp64 token recurrence + 4 checkpoints ({sec:.2f} s wall)"}
+    out = {"value": w.T / sec, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"sequence 0 of the batched workload: {w.T} tokens x {w.H} heads, conv + "
+                     f"fp64 token recurrence + 4 checkpoints ({sec:.2f} s wall)"}
+    if gpu_o is not None:
+        worst = 0.0
+        for h in range(w.H):
+            r = ref["o"][:, h]
+            worst = max(worst, float(np.max(np.abs(gpu_o[:, h] - r)) / np.max(np.abs(r))))
+        out["parity"] = {"o_max_rel_err": worst, "tol": 2e-2,
+                         "of": f"the timed step's output for sequence 0, all {w.H} heads, max |x - ref| / "
+                               f"max |ref| per head against the oracle on the same inputs"}
+    return out
 
 
 def _oracle_workloads():
@@ -711,6 +723,8 @@ def run_ours(args, rank, world, dev):
         total_ms, per = _time_steps(bench.step, args.steps, args.warmup, stream, min_warm_s=1.0)
     rc, bits = bench.kda.kda_sync_status(bench.status)
     assert rc == bench.kda.KDA_OK, f"device status {bits}"
+    # the last timed step's output for sequence 0, read back after the timed region
+    o_seq0 = bench.o[:w.T].double().cpu().numpy() if rank == 0 and world == 1 and not args.no_cpu else None
     total_ms = _max_over_ranks(total_ms, world, dev)
     if world > 1:
         dist.barrier()
@@ -774,7 +788,8 @@ def run_ours(args, rank, world, dev):
     if rank == 0 and world == 1 and not args.no_cpu:
         def cpu_toks():
             return {k: (v[:w.T] if k != "conv_w" else v).cpu() for k, v in bench.toks.items()}
-        line["cpu_baseline"] = _oracle_sample(cpu_toks)
+        line["cpu_baseline"] = _oracle_sample(cpu_toks, gpu_o=o_seq0)
+        line["parity"] = line["cpu_baseline"].pop("parity")
         if not args.no_extras:
             line["cpu_baseline"]["workloads"] = _oracle_workloads()
     return line
