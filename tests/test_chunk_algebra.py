@@ -210,3 +210,59 @@ def test_factored_decay_is_exact_down_to_the_range_limit():
     G0, gC0 = _factored_gram_fp32(k, al0)
     assert not gC0[0] >= np.float32(2.0 ** -100)
     assert not np.all(np.isfinite(G0))
+
+
+def _block_anchored_products_fp32(a, b, al, blk=16):
+    """sum_i a_ri b_si prod_{s<u<=r} al_ui for s <= r, in fp32, with every decay factor <= 1:
+    an earlier key block is reached through the start b of the row's block,
+    (prod_{b<u<=r} al)(prod_{s<u<=b} al); inside a diagonal block the per-pair product is
+    taken directly.  (The form chunk prep would need to cover every gate in [0, 1].)"""
+    f32 = np.float32
+    a, b, al = a.astype(f32), b.astype(f32), al.astype(f32)
+    C = a.shape[0]
+    out = np.zeros((C, C), dtype=f32)
+    for R in range(C // blk):
+        r0 = R * blk
+        rows = slice(r0, r0 + blk)
+        # row factor prod_{r0<u<=r} al (1 at the block start)
+        f1 = np.ones((blk, a.shape[1]), dtype=f32)
+        for j in range(1, blk):
+            f1[j] = f1[j - 1] * al[r0 + j]
+        ar = a[rows] * f1
+        if r0 > 0:
+            # key factor prod_{s<u<=r0} al for every earlier key s, a suffix product
+            f2 = np.ones((r0, a.shape[1]), dtype=f32)
+            f2[r0 - 1] = al[r0]
+            for s in range(r0 - 2, -1, -1):
+                f2[s] = f2[s + 1] * al[s + 1]
+            out[rows, :r0] = (ar @ (b[:r0] * f2).T).astype(f32)
+        for r in range(blk):
+            dec = np.ones(a.shape[1], dtype=f32)
+            for s in range(r, -1, -1):
+                out[r0 + r, r0 + s] = np.sum(a[r0 + r] * b[r0 + s] * dec, dtype=f32)
+                dec = dec * al[r0 + s]
+    return out
+
+
+def test_block_anchored_decay_covers_a_zero_gate():
+    """The block-anchored form stays finite and exact to fp32 rounding where the chunk-end
+    anchoring breaks: a gate of exactly 0 in some channels and gates near 0 in others."""
+    rng = np.random.default_rng(22)
+    C, d = 64, 32
+    q = rng.standard_normal((C, d))
+    k = rng.standard_normal((C, d))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    al = rng.uniform(0.4, 1.0, (C, d))
+    al[30, 0] = 0.0                                  # a full reset of channel 0
+    al[:, 1] = 1e-3                                  # a channel decaying to 1e-192 over the chunk
+    al = al.astype(np.float32).astype(np.float64)
+    ref = np.zeros((C, C))
+    for r in range(C):
+        for s in range(r + 1):
+            ref[r, s] = np.sum(q[r].astype(np.float32) * k[s].astype(np.float32) * np.prod(al[s + 1:r + 1], axis=0))
+    got = _block_anchored_products_fp32(q, k, al)
+    assert np.all(np.isfinite(got))
+    assert np.max(np.abs(np.tril(got) - ref)) <= 1e-5 * np.max(np.abs(ref))
+    # the chunk-end anchoring on the same chunk does not survive
+    G, gC = _factored_gram_fp32(k, al)
+    assert not np.all(np.isfinite(G))
