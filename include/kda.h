@@ -95,7 +95,11 @@ int32_t kda_object_pages(const kda_pool *pool, int32_t H, int32_t d, int32_t dty
 
 /* page_bytes must be a positive multiple of 256; num_pages > 0.  *out receives the pool. */
 int kda_pool_create(int64_t page_bytes, int32_t num_pages, kda_pool **out);
+/* Frees the pool's host metadata and its pinned staging buffers, first waiting for any
+ * upload still reading them; the caller's device pages are untouched.  KDA_EINVAL for NULL. */
 int kda_pool_destroy(kda_pool *pool);
+/* The page size in bytes, the number of pages, and the number of free pages (reference count
+ * 0).  KDA_EINVAL for NULL. */
 int64_t kda_pool_page_bytes(const kda_pool *pool);
 int32_t kda_pool_num_pages(const kda_pool *pool);
 int32_t kda_pool_free_count(const kda_pool *pool);
@@ -391,6 +395,7 @@ int kda_ckpt_prefetch(kda_pool *pool, int32_t H, int32_t d, int32_t dtype, int32
  * code = round-to-nearest-even(S[i][j] / scale_i) clamped to [-127, 127], both divisions IEEE
  * fp32; a zero row has scale 0 and codes 0; dequantisation writes code * scale_i. */
 int64_t kda_record_bytes_q8(int32_t d, int32_t dtype);
+/* H INT8 records, and the pages of this pool they span; KDA_EINVAL for a bad shape or pool. */
 int64_t kda_object_bytes_q8(int32_t H, int32_t d, int32_t dtype);
 int32_t kda_object_pages_q8(const kda_pool *pool, int32_t H, int32_t d, int32_t dtype);
 
