@@ -40,6 +40,25 @@ def test_exports_every_declared_symbol():
                                                        "kda_pool_free_count", "kda_status_string")
 
 
+def test_header_documents_every_call():
+    """Each declaration in include/kda.h sits under a comment: directly, or as part of a run
+    of declarations that one comment introduces (no blank line between them)."""
+    lines = open(os.path.join(ROOT, "include", "kda.h")).read().splitlines()
+    undocumented = []
+    for i, ln in enumerate(lines):
+        m = re.match(r"^(?:int|int32_t|int64_t|void|const char \*)\s*\**\s*(kda_\w+)\s*\(", ln)
+        if not m:
+            continue
+        j = i - 1
+        # walk back over the run of declarations (and their continuation lines) above
+        while j >= 0 and lines[j].strip() and not lines[j].rstrip().endswith("*/"):
+            j -= 1
+        if j < 0 or not lines[j].rstrip().endswith("*/"):
+            undocumented.append(m.group(1))
+    assert len(_declared_functions()) >= 30
+    assert undocumented == []
+
+
 @pytest.mark.parametrize("H,d,dt", [(16, 128, "bf16"), (32, 128, "bf16"), (2, 64, "f32"),
                                     (3, 64, "bf16"), (5, 128, "f32")])
 def test_sizes_match_oracle(H, d, dt):
